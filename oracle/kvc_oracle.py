@@ -1,0 +1,280 @@
+"""CPU oracle for the KV-cached grouped-query attention step of autoregressive decoding.
+
+TEST INFRASTRUCTURE ONLY. Only `tests/`, `__graft_entry__.smoke()` and the CPU
+baseline leg of `bench.py` may import this module. The GPU library never calls
+it, links it or shares code with it; the product path fails loudly when its
+CUDA extension is missing rather than falling back to anything here.
+
+It computes the plain definitions, in float64, one (sequence, head) at a time:
+
+* the cache store and its bookkeeping: per-layer fill counts, a committed
+  length that moves once per forward, truncate for rollback, and the storage
+  dtype that rounds on the way in ("KV cache, incremental decode, incremental
+  UTF-8 detokenizer, generate", §2.3 "Committed length, positions, and the
+  mask", §2.4 "Rollback", §2.5 "Storage dtype", §4 "The interface");
+* the bottom-right-aligned causal mask, mask(T)_ij = [j <= s + i] for
+  0 <= i < T, 0 <= j < s + T (same page, §2.3 equation);
+* scaled dot-product attention over the cache, softmax(q K^T / sqrt(d_h)) V,
+  with masked scores removed ("Generation and the KV Cache", fence 3 "a toy
+  KV cache equals recomputation"; "KV cache decoding", step 6);
+* grouped-query head sharing, query head h reading K/V head h // G in the
+  order [0, 0, 1, 1] for 4 query and 2 K/V heads ("Heads, GQA and K/V cache",
+  "Four queries, two sets of K/V");
+* the uncached full recompute that the cached path must equal ("KV cache
+  decoding", "Why the causal mask makes caching exact").
+
+Readings where the pages are silent (each listed in the design doc):
+* rounding to float16/bfloat16 is round-to-nearest-even; NaN inputs are out of scope;
+* a query for a 16-bit cache is rounded to the cache dtype before use;
+* `commit` is explicit and requires every layer's fill to agree per sequence;
+* `truncate(n)` requires n <= the committed length and leaves stale rows in place.
+
+Parity status: every function here is pinned by `tests/test_oracle_pins.py`.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+DTYPES = ("f32", "f16", "bf16", "f64")
+ITEMSIZE = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8}
+
+
+# ----------------------------------------------------------------------------------------------
+# Storage rounding ("KV cache, incremental decode, ...", §2.5 "Storage dtype": values are
+# converted on the way in and the stored values are what every later read returns).
+# ----------------------------------------------------------------------------------------------
+
+def store_round(x, dtype: str) -> np.ndarray:
+    """Convert float32 input values to the cache's stored representation.
+
+    f32 -> float32 copy; f16 -> IEEE half (NumPy's astype, round to nearest even);
+    bf16 -> uint16 bit patterns, rounding float32 to its top 16 bits to nearest even;
+    f64 -> float64 (the NumPy default store of the "KV cache decoding" listing).
+    """
+    x = np.asarray(x)
+    if dtype == "f64":
+        return x.astype(np.float64)
+    x = x.astype(np.float32)
+    if dtype == "f32":
+        return x.copy()
+    if dtype == "f16":
+        return x.astype(np.float16)
+    if dtype == "bf16":
+        u = x.view(np.uint32).astype(np.uint64)
+        # keep the top 16 bits; add half an ulp minus one, plus the kept lsb, so ties go to even
+        u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+        return u.astype(np.uint16)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def stored_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact float64 value of stored elements."""
+    if dtype == "bf16":
+        return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def storage_np_dtype(dtype: str):
+    return {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "f64": np.float64}[dtype]
+
+
+# ----------------------------------------------------------------------------------------------
+# The offset causal mask ("KV cache, incremental decode, ...", §2.3 equation; "KV cache decoding",
+# step 3: row i of a chunk at positions t..t+m-1 may attend to columns 0..t+i).
+# ----------------------------------------------------------------------------------------------
+
+def offset_causal_mask(T: int, s: int) -> np.ndarray:
+    """Boolean [T, s + T]: entry (i, j) is True when key j is visible to query i, i.e. j <= s + i."""
+    if T < 0 or s < 0:
+        raise ValueError("T and s must be non-negative")
+    i = np.arange(T)[:, None]
+    j = np.arange(s + T)[None, :]
+    return j <= s + i
+
+
+def kv_bytes(layers: int, heads: int, head_dim: int, seq_len: int, batch: int = 1,
+             bytes_per_value: int = 2) -> int:
+    """K plus V bytes: 2 * layers * heads * head_dim * seq_len * batch * bytes ("KV cache decoding",
+    "What is cached, what is not, and what it costs"; "Heads, GQA and K/V cache", "Memory and the
+    window limit"; "Generation and the KV Cache", "Memory")."""
+    return 2 * layers * heads * head_dim * seq_len * batch * bytes_per_value
+
+
+# ----------------------------------------------------------------------------------------------
+# The cache ("KV cache, incremental decode, ...", §4 "The interface": seq_len, update, positions,
+# mask, truncate, nbytes; "Generation and the KV Cache": k, v of shape (L, B, H, max_len, d_head)).
+# ----------------------------------------------------------------------------------------------
+
+class OracleKVCache:
+    """Preallocated (L, B, H_kv, max_len, d_h) store with per-layer fills and committed lengths.
+
+    Every method validates before it mutates: on any error nothing changes ("KV cache,
+    incremental decode, ...", §4 test_update_copies_and_checks).
+    """
+
+    def __init__(self, n_layers: int, batch: int, n_kv_heads: int, d_head: int, max_len: int,
+                 dtype: str = "f32"):
+        if dtype not in DTYPES:
+            raise ValueError(f"unknown dtype {dtype!r}")
+        if min(n_layers, batch, n_kv_heads, d_head, max_len) <= 0:
+            raise ValueError("all sizes must be positive")
+        self.L, self.B, self.H, self.d, self.max_len, self.dtype = (
+            n_layers, batch, n_kv_heads, d_head, max_len, dtype)
+        shape = (n_layers, batch, n_kv_heads, max_len, d_head)
+        self.k = np.zeros(shape, dtype=storage_np_dtype(dtype))
+        self.v = np.zeros(shape, dtype=storage_np_dtype(dtype))
+        self.fill = np.zeros((n_layers, batch), dtype=np.int64)   # per-layer fill counts
+        self.lens = np.zeros(batch, dtype=np.int64)               # committed lengths s_b
+
+    # -- lengths ---------------------------------------------------------------------------
+    def seq_len(self, layer: int | None = None) -> np.ndarray:
+        """Committed length as the minimum fill over layers (§2.3), or one layer's fill count."""
+        if layer is None:
+            return self.fill.min(axis=0).copy()
+        return self.fill[layer].copy()
+
+    def committed(self) -> np.ndarray:
+        return self.lens.copy()
+
+    def positions(self, T: int) -> np.ndarray:
+        """[B, T] absolute positions [s_b, s_b + T) of the next chunk (what RoPE rotates by)."""
+        return self.lens[:, None] + np.arange(T)[None, :]
+
+    def mask(self, T: int, b: int = 0) -> np.ndarray:
+        """causal_mask(T, s + T, q_offset=s) for sequence b, read from the committed length."""
+        return offset_causal_mask(T, int(self.lens[b]))
+
+    # -- writes ----------------------------------------------------------------------------
+    def append(self, layer: int, k_new, v_new):
+        """Write a [B, H_kv, T, d_h] chunk at each sequence's fill of this layer; return all rows.
+
+        Returns, per sequence, the stored (rounded) keys and values [H_kv, fill, d_h] as float64:
+        the past and the new chunk both come back as stored ("KV cache, incremental decode, ...",
+        §2.5; "KV cache decoding", step 5).
+        """
+        if not 0 <= layer < self.L:
+            raise ValueError("layer out of range")
+        k_new = np.asarray(k_new)
+        v_new = np.asarray(v_new)
+        if k_new.ndim != 4 or k_new.shape != v_new.shape:
+            raise ValueError("k_new and v_new must both be [B, H_kv, T, d_h]")
+        B, H, T, d = k_new.shape
+        if (B, H, d) != (self.B, self.H, self.d):
+            raise ValueError("shape mismatch")
+        if np.any(self.fill[layer] + T > self.max_len):
+            raise OverflowError("append would exceed max_len")
+        kq = store_round(k_new, self.dtype)      # copies: the caller may reuse its buffers
+        vq = store_round(v_new, self.dtype)
+        for b in range(B):
+            f = int(self.fill[layer, b])
+            self.k[layer, b, :, f:f + T] = kq[b]
+            self.v[layer, b, :, f:f + T] = vq[b]
+        self.fill[layer] += T
+        return [(stored_to_f64(self.k[layer, b, :, :self.fill[layer, b]], self.dtype),
+                 stored_to_f64(self.v[layer, b, :, :self.fill[layer, b]], self.dtype))
+                for b in range(B)]
+
+    def commit(self) -> None:
+        """Advance every committed length to its fill, once per forward after the last layer."""
+        if np.any(self.fill != self.fill[0][None, :]):
+            raise RuntimeError("commit with unequal per-layer fills")
+        self.lens = self.fill[0].copy()
+
+    def truncate(self, n) -> None:
+        """Set every layer's fill and the committed length to n (scalar or per sequence).
+
+        Nothing is freed or zeroed; the next append overwrites from n (§2.4 "Rollback").
+        """
+        n = np.broadcast_to(np.asarray(n, dtype=np.int64), (self.B,)).copy()
+        if np.any(n < 0):
+            raise ValueError("negative length")
+        if np.any(n > self.lens):
+            raise RuntimeError("truncate beyond the committed length")
+        self.fill[:, :] = n[None, :]
+        self.lens = n
+
+    # -- sizes -----------------------------------------------------------------------------
+    def nbytes(self) -> int:
+        """Capacity: 2 * L * B * H_kv * max_len * d_h * itemsize (§2.5)."""
+        return 2 * self.L * self.B * self.H * self.max_len * self.d * ITEMSIZE[self.dtype]
+
+    def filled_bytes(self) -> int:
+        """Bytes of the committed part: 2 * L * H_kv * d_h * itemsize * sum_b s_b."""
+        return 2 * self.L * self.H * self.d * ITEMSIZE[self.dtype] * int(self.lens.sum())
+
+    def stored_f64(self, layer: int, b: int, kvh: int, n: int):
+        """Float64 view of the first n stored rows of one (layer, sequence, K/V head)."""
+        return (stored_to_f64(self.k[layer, b, kvh, :n], self.dtype),
+                stored_to_f64(self.v[layer, b, kvh, :n], self.dtype))
+
+
+# ----------------------------------------------------------------------------------------------
+# Attention
+# ----------------------------------------------------------------------------------------------
+
+def softmax_rows(scores: np.ndarray) -> np.ndarray:
+    """Row softmax with the row maximum subtracted first; -inf entries get weight 0."""
+    m = np.max(scores, axis=-1, keepdims=True)
+    e = np.exp(scores - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_offset: int) -> np.ndarray:
+    """One head: softmax(mask(q k^T / sqrt(d))) v with query i at absolute position q_offset + i.
+
+    q [T, d], k and v [N, d] with N = q_offset + T, all float64.
+    """
+    T, d = q.shape
+    N = k.shape[0]
+    if N != q_offset + T:
+        raise ValueError("key count must equal q_offset + T")
+    scores = (q @ k.T) / np.sqrt(d)
+    scores = np.where(offset_causal_mask(T, q_offset), scores, -np.inf)
+    return softmax_rows(scores) @ v
+
+
+def query_as_f64(q, dtype: str) -> np.ndarray:
+    """A float32 query rounded to the cache dtype (16-bit caches), as float64."""
+    q = np.asarray(q)
+    if dtype in ("f16", "bf16"):
+        return stored_to_f64(store_round(q, dtype), dtype)
+    if dtype == "f32":
+        return q.astype(np.float32).astype(np.float64)
+    return q.astype(np.float64)
+
+
+def gqa_cached_attention(cache: OracleKVCache, layer: int, q, T: int | None = None) -> np.ndarray:
+    """Attend a chunk's queries over every stored row of one layer.
+
+    q is [B, H_q, T, d_h]. The layer must already hold the chunk (fill = s_b + T, with s_b the
+    committed length). Query head h of sequence b reads K/V head h // G, G = H_q / H_kv, and
+    query t sees stored rows j <= s_b + t. Returns [B, H_q, T, d_h] float64.
+    """
+    q = np.asarray(q)
+    B, H_q, Tq, d = q.shape
+    T = Tq if T is None else T
+    if T != Tq or B != cache.B or d != cache.d or H_q % cache.H:
+        raise ValueError("query shape does not match the cache")
+    G = H_q // cache.H
+    q64 = query_as_f64(q, cache.dtype)
+    out = np.zeros((B, H_q, T, d), dtype=np.float64)
+    for b in range(B):
+        N = int(cache.fill[layer, b])
+        s = N - T
+        if s != int(cache.lens[b]):
+            raise RuntimeError("the layer must hold exactly the committed rows plus this chunk")
+        for h in range(H_q):
+            k, v = cache.stored_f64(layer, b, h // G, N)
+            out[b, h] = attend(q64[b, h], k, v, q_offset=s)
+    return out
+
+
+def full_recompute_attention(q_all: np.ndarray, k_all: np.ndarray, v_all: np.ndarray) -> np.ndarray:
+    """Uncached path: causal attention of every position of a whole sequence, q_offset = 0.
+
+    q_all [H_q, n, d], k_all and v_all [H_kv, n, d] (float64, already as stored). Query head h
+    uses K/V head h // G. Returns [H_q, n, d].
+    """
+    H_q, n, d = q_all.shape
+    G = H_q // k_all.shape[0]
+    return np.stack([attend(q_all[h], k_all[h // G], v_all[h // G], q_offset=0) for h in range(H_q)])

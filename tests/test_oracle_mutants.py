@@ -1,0 +1,115 @@
+"""Plant the pages' pitfalls in the oracle (on the CPU) and check that the pins catch each one.
+
+"KV cache, incremental decode, ...", §5 "Pitfalls" lists the mistakes; each mutant below is one
+of them, patched into a copy of the oracle's behaviour for the duration of one test.
+"""
+import numpy as np
+import pytest
+
+import oracle.kvc_oracle as ko
+from tests import test_oracle_pins as pins
+
+
+def _fails(test, *args):
+    with pytest.raises(AssertionError):
+        test(*args)
+
+
+def test_mask_without_offset_is_caught(monkeypatch):
+    """Pitfall 3: a decode mask without the offset."""
+    orig = ko.attend
+
+    def attend_no_offset(q, k, v, q_offset):
+        T, d = q.shape
+        scores = (q @ k.T) / np.sqrt(d)
+        mask = np.zeros((T, k.shape[0]), bool)
+        mask[:, :T] = np.tril(np.ones((T, T), bool))
+        return ko.softmax_rows(np.where(mask, scores, -np.inf)) @ v
+
+    monkeypatch.setattr(ko, "attend", attend_no_offset)
+    _fails(pins.test_cached_equals_full_recompute_every_step)
+    monkeypatch.setattr(ko, "attend", orig)
+
+
+def test_wrong_gqa_mapping_is_caught(monkeypatch):
+    """K/V head h % H_kv instead of h // G."""
+    def gqa_mod(cache, layer, q, T=None):
+        B, Hq, T, d = q.shape
+        out = np.zeros((B, Hq, T, d))
+        for b in range(B):
+            N = int(cache.fill[layer, b])
+            for h in range(Hq):
+                k, v = cache.stored_f64(layer, b, h % cache.H, N)
+                out[b, h] = ko.attend(ko.query_as_f64(q[b, h], cache.dtype), k, v, N - T)
+        return out
+
+    monkeypatch.setattr(pins, "gqa_cached_attention", gqa_mod)
+    _fails(pins.test_gqa_head_mapping_is_contiguous_groups)
+
+
+def test_update_returning_only_the_new_chunk_is_caught(monkeypatch):
+    """Pitfall 4."""
+    orig = ko.OracleKVCache.append
+
+    def append_new_only(self, layer, k_new, v_new):
+        T = np.asarray(k_new).shape[2]
+        rows = orig(self, layer, k_new, v_new)
+        return [(k[:, -T:], v[:, -T:]) for k, v in rows]
+
+    monkeypatch.setattr(ko.OracleKVCache, "append", append_new_only)
+    _fails(pins.test_hand_example)
+
+
+def test_truncating_one_layer_only_is_caught(monkeypatch):
+    """Pitfall 6."""
+    def truncate_first_layer(self, n):
+        n = np.broadcast_to(np.asarray(n, dtype=np.int64), (self.B,)).copy()
+        self.fill[0, :] = n
+        self.lens = n
+
+    monkeypatch.setattr(ko.OracleKVCache, "truncate", truncate_first_layer)
+    with pytest.raises((AssertionError, RuntimeError)):
+        pins.test_truncate_then_reappend_same_rows_restores_whole_buffer()
+
+
+def test_float16_cache_returning_the_raw_chunk_is_caught(monkeypatch):
+    """Pitfall 8."""
+    orig = ko.OracleKVCache.append
+
+    def append_raw(self, layer, k_new, v_new):
+        rows = orig(self, layer, k_new, v_new)
+        T = np.asarray(k_new).shape[2]
+        out = []
+        for b, (k, v) in enumerate(rows):
+            k = k.copy()
+            v = v.copy()
+            k[:, -T:] = np.asarray(k_new)[b]
+            v[:, -T:] = np.asarray(v_new)[b]
+            out.append((k, v))
+        return out
+
+    monkeypatch.setattr(ko.OracleKVCache, "append", append_raw)
+    _fails(pins.test_float16_cache_rounds_what_it_stores)
+
+
+def test_dropped_scale_is_caught(monkeypatch):
+    """Scores without the 1 / sqrt(d_h) factor."""
+    def attend_unscaled(q, k, v, q_offset):
+        T = q.shape[0]
+        scores = q @ k.T
+        return ko.softmax_rows(np.where(ko.offset_causal_mask(T, q_offset), scores, -np.inf)) @ v
+
+    monkeypatch.setattr(pins, "attend", attend_unscaled)
+    _fails(pins.test_hand_softmax)
+
+
+def test_bf16_truncation_instead_of_rounding_is_caught(monkeypatch):
+    orig = ko.store_round
+
+    def truncating(x, dtype):
+        if dtype == "bf16":
+            return (np.asarray(x, np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+        return orig(x, dtype)
+
+    monkeypatch.setattr(pins, "store_round", truncating)
+    _fails(pins.test_storage_rounding_golden, "bf16")
