@@ -1,0 +1,411 @@
+"""Benchmark of the KV-cached GQA decode step on one or more GB300s.
+
+A step is one decode forward of the Llama-3-8B-shaped batch (32 layers; H_q=32, H_kv=8, d_h=128,
+B=64, bf16 cache, ragged s_b ~ U[512, 4096], T=1): for every layer, append the new K/V row and
+attend; then commit; then truncate back to s_b so every timed step does the same work. Inputs are
+synthetic (seeded Philox draws) and already resident in HBM when timing starts; the K/V read per
+layer (~580 MB) is far larger than L2, so no flush is needed between iterations.
+
+Prints one JSON line (rank 0). `value` is algorithmic HBM GB/s of the whole job; `steps_per_s` and
+the roofline fraction of the attention kernel come with it. `--impl reference` times the CPU oracle
+instead, on a bounded sample of the same workload.
+
+Multi-GPU: the workload has no exchange step, so each rank runs an independent replica (weak
+scaling); timing is bracketed by barriers and the maximum over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "cached GQA decode-attention HBM GB/s (% of peak) and decode steps/sec"
+DEFAULT_WORKLOAD = "llama3-8b-decode-bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--split-keys", type=int, default=0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-sample-child", default=None, help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("kvc_splitk.cu",):
+        with open(os.path.join(ROOT, "kv_cached_gqa_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(workload):
+    """DRAM bytes per attention launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload]
+        if e.get("kernel_sha") == kernel_source_hash():
+            return e["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.device_index = device_index
+
+    def __enter__(self):
+        try:
+            import torch
+            ident = str(self.device_index)
+            uuid = getattr(torch.cuda.get_device_properties(self.device_index), "uuid", None)
+            if uuid is not None:
+                ident = "GPU-" + str(uuid) if not str(uuid).startswith("GPU-") else str(uuid)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", ident], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, RuntimeError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (run in a child process, one BLAS thread)
+# ------------------------------------------------------------------------------------------------
+
+def cpu_sample_child(arg):
+    """Time the oracle's attention over a few sequences of layer 0; print a JSON result."""
+    cfg = json.loads(arg)
+    import numpy as np
+
+    import kvc_workloads
+    from oracle.kvc_oracle import OracleKVCache, gqa_cached_attention
+    sp = kvc_workloads.spec(cfg["workload"])
+    seqs = list(range(cfg["n_seq"]))
+    caches, queries = [], []
+    for b in seqs:
+        s_b = int(sp.lengths[b])
+        c = OracleKVCache(1, 1, sp.H_kv, sp.d_h, s_b + sp.T, sp.dtype)
+        if s_b:
+            kk = np.stack([sp.host_prefill_rows(0, b, h, s_b)[0] for h in range(sp.H_kv)])[None]
+            vv = np.stack([sp.host_prefill_rows(0, b, h, s_b)[1] for h in range(sp.H_kv)])[None]
+            c.append(0, kk, vv)
+            c.commit()
+        kn = np.stack([sp.host_step_rows(0, 0, b, h)[0] for h in range(sp.H_kv)])[None]
+        vn = np.stack([sp.host_step_rows(0, 0, b, h)[1] for h in range(sp.H_kv)])[None]
+        c.append(0, kn, vn)
+        caches.append(c)
+        queries.append(sp.host_queries(0, 0, b, range(sp.H_q))[None])
+    bytes_per_pass = sp.attn_bytes(seqs)
+    t_end = time.perf_counter() + cfg["seconds"]
+    passes, elapsed = 0, 0.0
+    times = []
+    while time.perf_counter() < t_end or passes < cfg.get("min_passes", 1):
+        t0 = time.perf_counter()
+        for c, q in zip(caches, queries):
+            gqa_cached_attention(c, 0, q)
+        dt = time.perf_counter() - t0
+        times.append(dt)
+        elapsed += dt
+        passes += 1
+    print(json.dumps({"bytes_per_pass": bytes_per_pass, "passes": passes, "seconds": elapsed,
+                      "pass_seconds": times, "n_seq": len(seqs), "layer_bytes": sp.attn_bytes(),
+                      "step_bytes": sp.step_bytes()}))
+
+
+def run_cpu_sample(workload, n_seq, seconds, min_passes=1):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    arg = json.dumps({"workload": workload, "n_seq": n_seq, "seconds": seconds, "min_passes": min_passes})
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample-child", arg],
+                       capture_output=True, text=True, env=env, cwd=ROOT, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle sample failed:\n{r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_entry(workload, seconds, n_seq=2):
+    res = run_cpu_sample(workload, n_seq, seconds)
+    gbs = res["bytes_per_pass"] * res["passes"] / res["seconds"] / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"layer 0 attention of {res['n_seq']} of the batch's sequences (all their heads), "
+                       f"float64 NumPy oracle, {res['passes']} passes in {res['seconds']:.1f} s, one thread; "
+                       f"GB/s over the same algorithmic bytes as the GPU line"),
+            "steps_per_s_equiv": round(gbs * 1e9 / res["step_bytes"], 6)}
+
+
+# ------------------------------------------------------------------------------------------------
+# arms
+# ------------------------------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import kvc_workloads
+    sp = kvc_workloads.spec(args.workload)
+    n_seq = 4
+    per_step = []
+    res = run_cpu_sample(args.workload, n_seq, 0.0, min_passes=args.warmup + args.steps)
+    per_step = res["pass_seconds"][args.warmup:]
+    t = sum(per_step)
+    gbs = res["bytes_per_pass"] * len(per_step) / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t / len(per_step), 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": sp.dtype, "data": "synthetic (seeded Philox draws)",
+        "config": workload_config(sp, "each step is the oracle over a bounded sample: layer 0 of "
+                                      f"{n_seq} sequences"),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"layer 0 attention of {n_seq} sequences per step, float64 NumPy, one thread"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(sp, note=None):
+    import numpy as np
+    c = {"workload": sp.name, "L": sp.L, "B": sp.B, "H_q": sp.H_q, "H_kv": sp.H_kv, "d_h": sp.d_h,
+         "T": sp.T, "cache_dtype": sp.dtype, "max_len": sp.max_len,
+         "s_b": {"min": int(np.min(sp.lengths)), "mean": float(np.mean(sp.lengths)),
+                 "max": int(np.max(sp.lengths))},
+         "l2": "no flush: K/V read per layer is larger than the 129 MB L2"}
+    if note:
+        c["note"] = note
+    return c
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import kvc_workloads
+    from kv_cached_gqa_gb300 import _binding as kb
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    kb.load()
+    sp = kvc_workloads.spec(args.workload)
+    wl = kvc_workloads.GpuWorkload(sp, device=f"cuda:{local}")
+    if args.split_keys:
+        kb.kvc_set_split_keys(wl.cache, args.split_keys)
+    wl.prefill()
+    inputs = wl.step_inputs(0)
+    outs = [torch.empty((sp.B, sp.H_q, sp.T, sp.d_h), dtype=torch.float32, device=f"cuda:{local}")
+            for _ in range(sp.L)]
+    lengths = [int(x) for x in sp.lengths]
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        for layer, (q, k, v) in enumerate(inputs):
+            kb.kvc_append(wl.cache, layer, k, v)
+            if ev is not None:
+                ev[layer][0].record(stream)
+            kb.gqa_cached_attn(wl.cache, q, layer, out=outs[layer])
+            if ev is not None:
+                ev[layer][1].record(stream)
+        kb.kvc_commit(wl.cache)
+        kb.kvc_truncate_ragged(wl.cache, lengths)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    kb.kvc_status(wl.cache)
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(sp.L)]
+              for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = kb.kvc_launch_count(wl.cache)
+    barrier()
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(events[i])
+        t1.record(stream)
+        barrier()
+    launches = kb.kvc_launch_count(wl.cache) - launches0
+    kb.kvc_status(wl.cache)
+    ms = t0.elapsed_time(t1) / args.steps
+    attn_ms = [ev[l][0].elapsed_time(ev[l][1]) for ev in events for l in range(sp.L)]
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    if world > 1:
+        t = torch.tensor([ms, attn_avg_ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, attn_avg_ms = float(t[0]), float(t[1])
+
+    # end to end through the public API with host buffers: pinned inputs copied in and outputs
+    # read back inside the timed region, every step
+    e2e = None
+    if not args.no_e2e:
+        host_in = [tuple(x.cpu().pin_memory() for x in trio) for trio in inputs]
+        host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+        dev_in = [tuple(torch.empty_like(x) for x in trio) for trio in inputs]
+        h2d = sum(x.numel() * x.element_size() for trio in host_in for x in trio)
+        d2h = sum(o.numel() * o.element_size() for o in host_out)
+
+        def e2e_step():
+            for layer in range(sp.L):
+                for d_, h_ in zip(dev_in[layer], host_in[layer]):
+                    d_.copy_(h_, non_blocking=True)
+                q, k, v = dev_in[layer]
+                kb.kvc_append(wl.cache, layer, k, v)
+                kb.gqa_cached_attn(wl.cache, q, layer, out=outs[layer])
+                host_out[layer].copy_(outs[layer], non_blocking=True)
+            kb.kvc_commit(wl.cache)
+            kb.kvc_truncate_ragged(wl.cache, lengths)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        barrier()
+        t0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        t1.record(stream)
+        barrier()
+        e2e_ms = t0.elapsed_time(t1) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=f"cuda:{local}")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        e2e = {"value": round(world * sp.step_bytes() / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps_per_s": round(world * 1e3 / e2e_ms, 3)}
+    kb.kvc_status(wl.cache)
+
+    if rank != 0:
+        wl.close()
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind = measured_peaks()
+    attn_gbs = sp.attn_bytes() / (attn_avg_ms * 1e-3) / 1e9
+    value = world * sp.step_bytes() / (ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline_entry(args.workload, args.cpu_sample_seconds)
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": sp.dtype,
+        "data": "synthetic (seeded Philox draws; approximately N(0,1))",
+        "config": workload_config(sp),
+        "steps_per_s": round(world * 1e3 / ms, 3),
+        "pct_of_peak": {"measured_hbm": round(100 * value / world / peak, 2),
+                        "nominal_8tbs": round(100 * value / world / 8000.0, 2)},
+        "roofline": {"kernel": "gqa_cached_attn (split-K attention + combine)", "bound": "hbm",
+                     "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(attn_gbs / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "bytes_per_launch": sp.attn_bytes(), "launch_ms": round(attn_avg_ms, 5),
+                     "traffic": traffic_per_launch(args.workload)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+    }
+    print(json.dumps(line), flush=True)
+    wl.close()
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_sample_child is not None:
+        cpu_sample_child(args.cpu_sample_child)
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

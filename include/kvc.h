@@ -1,0 +1,184 @@
+/*
+ * kvc.h — C ABI of the KV-cached grouped-query attention library for GB300 (sm_103a).
+ *
+ * One decode (or prefill, or verify) forward of a decoder with a KV cache, per layer l:
+ *   kvc_append(l, k_new, v_new)   write the chunk's post-RoPE keys/values at positions [s_b, s_b + T)
+ *   gqa_cached_attn(q, l, ...)    attend the chunk's T queries over all s_b + T stored keys
+ * and once after the last layer:
+ *   kvc_commit()                  s_b += T for every sequence
+ * ("KV cache, incremental decode, incremental UTF-8 detokenizer, generate", §2.1-§2.4 and §4
+ * "The interface"; "KV cache decoding", steps 1-7).
+ *
+ * Conventions shared by every call
+ * - Shapes are row-major and contiguous. The cache holds K and V, each [L, B, H_kv, max_len, d_h],
+ *   in the cache dtype. A chunk's keys/values are [B, H_kv, T, d_h]; its queries and the output
+ *   are [B, H_q, T, d_h].
+ * - Pointers named *_dev are device pointers on the current CUDA device; *_host are host pointers.
+ *   `stream` is a cudaStream_t (NULL = the legacy default stream). Every device-side effect is
+ *   enqueued on `stream` in call order; no call synchronises the device except kvc_status and
+ *   kvc_destroy.
+ * - Every call validates its arguments against host-side mirrors of the lengths before it
+ *   enqueues anything. On any error it returns a negative code, changes no state (lengths,
+ *   store, handle) and records a message for kvc_last_error ("KV cache, incremental decode, ...",
+ *   §4, test_update_copies_and_checks: nothing changed on error).
+ * - A handle is not thread-safe; calls on one handle must come from one host thread at a time.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kvc_cache* kvc_handle;
+
+/* Storage / input element types. */
+typedef enum { KVC_F32 = 0, KVC_F16 = 1, KVC_BF16 = 2 } kvc_dtype;
+
+/* Return codes. */
+enum {
+  KVC_OK = 0,
+  KVC_E_INVAL = -1,          /* bad argument: null pointer, size, layer, dtype, misalignment */
+  KVC_E_CAPACITY = -2,       /* the write would pass max_len ("KV cache decoding", assert t + m <= max_len) */
+  KVC_E_STATE = -3,          /* call out of order: commit with unequal fills, truncate beyond s_b,
+                                attention on a layer that does not hold exactly s_b + T rows */
+  KVC_E_CUDA = -4,           /* a CUDA runtime/driver call failed (message in kvc_last_error) */
+  KVC_E_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait gave up; reported by kvc_status */
+  KVC_E_UNSUPPORTED = -6,    /* a size this build has no kernel for (d_h not in {32, 64, 128}, ...) */
+  KVC_E_NOMEM = -7           /* device or host allocation failed */
+};
+
+/* Pass as `s` to gqa_cached_attn to use each sequence's own committed length (ragged batches). */
+#define KVC_COMMITTED (-1)
+/* Largest batch a handle accepts. */
+#define KVC_MAX_BATCH 1024
+
+/*
+ * kvc_create — allocate and zero a cache of L layers, B sequences, H_kv K/V heads of width d_h and
+ * capacity max_len positions, stored as `dtype`.
+ * Defined by: "KV cache, incremental decode, ...", §2.5 "Storage dtype" (preallocated
+ * 2 L B H_kv N_max d_h elements); "Generation and the KV Cache" ("Module 32 built KVCache(cfg,
+ * batch_size, max_len): k, v of shape (L, B, H, max_len, d_head)"); "KV cache decoding",
+ * KVCache listing (np.zeros: unfilled slots are zero).
+ * The library owns the store (cudaMalloc) and frees it in kvc_destroy. All lengths start at 0.
+ * Limits: 1 <= B <= KVC_MAX_BATCH, d_h in {32, 64, 128}, L*B*H_kv < 2^31, max_len < 2^31 - 256.
+ */
+int kvc_create(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len, kvc_dtype dtype,
+               void* stream);
+
+/*
+ * kvc_create_external — the same cache over caller-owned storage: k_store_dev and v_store_dev each
+ * hold L*B*H_kv*max_len*d_h elements of `dtype`, 256-byte aligned and already zeroed by the
+ * caller. The caller keeps ownership and must keep them alive until kvc_destroy.
+ */
+int kvc_create_external(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len,
+                        kvc_dtype dtype, void* k_store_dev, void* v_store_dev, void* stream);
+
+/* kvc_destroy — synchronise the device, free everything the library allocated. NULL is a no-op. */
+int kvc_destroy(kvc_handle h);
+
+/*
+ * kvc_append — write one chunk of T positions for one layer.
+ * Defined by: "KV cache, incremental decode, ...", §4 update(layer, k_new, v_new) ([B, Hkv, T, dh]
+ * in; written at the layer's fill count, §2.3) and §2.5 (values converted to the storage dtype on
+ * the way in); "KV cache decoding", step 5 (write slots t .. t+m-1 of this layer).
+ * k_new_dev, v_new_dev: [B, H_kv, T, d_h] in `in_dtype`, which is KVC_F32 or the cache dtype. F32
+ * input to a 16-bit cache is rounded to nearest even. The inputs are copied (the caller may reuse
+ * its buffers once the stream reaches this call). Each sequence b writes rows
+ * [fill_b, fill_b + T) of layer `layer`, fill_b being that layer's fill count, and the layer's
+ * fill counts advance by T. The committed length does not move (see kvc_commit).
+ * Errors: KVC_E_INVAL (layer, T < 1, null, dtype), KVC_E_CAPACITY (fill_b + T > max_len for any b).
+ */
+int kvc_append(kvc_handle h, int layer, const void* k_new_dev, const void* v_new_dev,
+               kvc_dtype in_dtype, int T, void* stream);
+
+/*
+ * kvc_commit — advance every committed length s_b to its fill, once per forward after the last
+ * layer ("KV cache, incremental decode, ...", §2.3: the length advances only after the last layer;
+ * "KV cache decoding", step 7).
+ * Error: KVC_E_STATE if the layers' fill counts disagree for any sequence.
+ */
+int kvc_commit(kvc_handle h, void* stream);
+
+/*
+ * kvc_truncate — set every layer's fill count and every committed length to n, for speculative
+ * rollback ("KV cache, incremental decode, ...", §2.4 "Rollback": nothing is freed or copied; the
+ * next append overwrites from n). Rows at and past n keep their old contents until overwritten.
+ * Error: KVC_E_STATE if n exceeds any sequence's committed length; KVC_E_INVAL if n < 0.
+ */
+int kvc_truncate(kvc_handle h, int n, void* stream);
+
+/* kvc_truncate_ragged — the same with one length per sequence, n_host[B] (host memory, copied). */
+int kvc_truncate_ragged(kvc_handle h, const int32_t* n_host, void* stream);
+
+/*
+ * kvc_seq_len — copy lengths into out_host[B]: the committed lengths s_b for layer == -1, or one
+ * layer's fill counts ("KV cache, incremental decode, ...", §4 seq_len(layer=None)).
+ */
+int kvc_seq_len(kvc_handle h, int layer, int32_t* out_host);
+
+/*
+ * kvc_positions — write the absolute positions of the next chunk, [s_b, s_b + T), into
+ * out_dev[B, T] (int32), from the device's committed lengths ("KV cache, incremental decode, ...",
+ * §4 positions(t_new); the positions RoPE rotates by, read once at the start of a forward).
+ */
+int kvc_positions(kvc_handle h, int T, int32_t* out_dev, void* stream);
+
+/* kvc_nbytes — capacity in bytes, 2 * L * B * H_kv * max_len * d_h * itemsize (§2.5). 0 for NULL. */
+size_t kvc_nbytes(kvc_handle h);
+
+/*
+ * kvc_layer_ptrs — device addresses of layer `layer`'s K and V blocks, each [B, H_kv, max_len, d_h]
+ * in the cache dtype: the stored (rounded) rows that attention reads ("KV cache, incremental
+ * decode, ...", §4: update returns all stored rows). Valid until kvc_destroy.
+ */
+int kvc_layer_ptrs(kvc_handle h, int layer, void** k_dev, void** v_dev);
+
+/*
+ * gqa_cached_attn — attend a chunk's T queries over every stored row of one layer.
+ * Defined by: "KV cache, incremental decode, ...", §2.3 (query i at absolute position s + i sees
+ * keys j <= s + i: causal_mask(T, s + T, q_offset = s)); "Generation and the KV Cache", fence 3
+ * (scores q K^T / sqrt(d), offset mask, softmax, times V); "Heads, GQA and K/V cache" ("Four
+ * queries, two sets of K/V": query head h uses K/V head h / G, G = H_q / H_kv, without repeating
+ * K/V in memory).
+ * q_dev: [B, H_q, T, d_h] in `q_dtype` (KVC_F32, or the cache dtype). For a 16-bit cache an F32
+ * query is rounded to the cache dtype first. out_dev: [B, H_q, T, d_h] float32, caller-owned.
+ * s: KVC_COMMITTED to use each sequence's committed length s_b, or a value every s_b must equal.
+ * Precondition: `layer` already holds this chunk, i.e. its fill count is s_b + T for every b
+ * (kvc_append(layer, ...) with the same T since the last commit/truncate), else KVC_E_STATE.
+ * The library keeps a device workspace for partial results and grows it (stream-ordered
+ * cudaMallocAsync) the first time a larger one is needed.
+ */
+int gqa_cached_attn(kvc_handle h, const void* q_dev, kvc_dtype q_dtype, int layer, int s, int T,
+                    int H_q, float* out_dev, void* stream);
+
+/*
+ * kvc_status — synchronise `stream` and report device-side failures: KVC_E_DEVICE_TIMEOUT if a
+ * kernel's bounded wait gave up since the last call (the flag is then cleared), KVC_E_CUDA on a
+ * sticky CUDA error, else KVC_OK.
+ */
+int kvc_status(kvc_handle h, void* stream);
+
+/* kvc_last_error — copy the last error message (of h, or of the calling thread when h is NULL). */
+int kvc_last_error(kvc_handle h, char* buf, size_t n);
+
+/*
+ * kvc_set_split_keys — keys per split of the split-K attention kernel; 0 restores the automatic
+ * choice. Rounded up to the kernel's tile. A tuning knob: results do not depend on it beyond
+ * floating-point reassociation.
+ */
+int kvc_set_split_keys(kvc_handle h, int keys);
+
+/*
+ * kvc_launch_count — number of kernels this handle has enqueued since kvc_create (host counter,
+ * incremented at each successful launch). Instrumentation for benchmarks; 0 for NULL.
+ */
+uint64_t kvc_launch_count(kvc_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H */

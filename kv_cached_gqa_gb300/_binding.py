@@ -1,0 +1,221 @@
+"""ctypes binding to `libkvc.so` — argument marshalling only.
+
+Every function here has the name of the C entry point it calls, converts torch tensors to device
+pointers and the current CUDA stream to a `cudaStream_t`, and raises `KvcError` on a negative
+return code. No step of the attention path runs in Python: if the library is missing, `load()`
+raises instead of falling back to anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkvc.so")
+_lib = None
+
+KVC_F32, KVC_F16, KVC_BF16 = 0, 1, 2
+KVC_COMMITTED = -1
+KVC_MAX_BATCH = 1024
+ERRORS = {0: "KVC_OK", -1: "KVC_E_INVAL", -2: "KVC_E_CAPACITY", -3: "KVC_E_STATE", -4: "KVC_E_CUDA",
+          -5: "KVC_E_DEVICE_TIMEOUT", -6: "KVC_E_UNSUPPORTED", -7: "KVC_E_NOMEM"}
+
+# exported symbols and their C signatures (restype, argtypes)
+_c_int, _vp, _sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+_i32p = ctypes.POINTER(ctypes.c_int32)
+SIGNATURES = {
+    "kvc_create": (_c_int, [ctypes.POINTER(_vp), _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
+    "kvc_create_external": (_c_int, [ctypes.POINTER(_vp), _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                     _vp, _vp, _vp]),
+    "kvc_destroy": (_c_int, [_vp]),
+    "kvc_append": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _vp]),
+    "kvc_commit": (_c_int, [_vp, _vp]),
+    "kvc_truncate": (_c_int, [_vp, _c_int, _vp]),
+    "kvc_truncate_ragged": (_c_int, [_vp, _i32p, _vp]),
+    "kvc_seq_len": (_c_int, [_vp, _c_int, _i32p]),
+    "kvc_positions": (_c_int, [_vp, _c_int, _vp, _vp]),
+    "kvc_nbytes": (_sz, [_vp]),
+    "kvc_layer_ptrs": (_c_int, [_vp, _c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp)]),
+    "gqa_cached_attn": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
+    "kvc_status": (_c_int, [_vp, _vp]),
+    "kvc_last_error": (_c_int, [_vp, ctypes.c_char_p, _sz]),
+    "kvc_set_split_keys": (_c_int, [_vp, _c_int]),
+    "kvc_launch_count": (ctypes.c_uint64, [_vp]),
+    "kvc_synth_fill_normal_f32": (_c_int, [_vp, _sz, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32,
+                                           ctypes.c_float, _vp]),
+}
+
+
+class KvcError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load `libkvc.so` (built by `kv_cached_gqa_gb300.build`); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _err(h) -> str:
+    buf = ctypes.create_string_buffer(512)
+    load().kvc_last_error(h, buf, 512)
+    return buf.value.decode(errors="replace")
+
+
+def _check(rc: int, h=None):
+    if rc != 0:
+        raise KvcError(rc, _err(h))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(t) -> int:
+    torch = _torch()
+    return {torch.float32: KVC_F32, torch.float16: KVC_F16, torch.bfloat16: KVC_BF16}[t]
+
+
+def torch_dtype(code: int):
+    torch = _torch()
+    return {KVC_F32: torch.float32, KVC_F16: torch.float16, KVC_BF16: torch.bfloat16}[code]
+
+
+def _stream(stream):
+    if stream is None:
+        return _torch().cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _ptr(t):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor")
+    return t.data_ptr()
+
+
+class Cache:
+    """A KV cache handle over torch-allocated storage (caller-owned K and V tensors)."""
+
+    def __init__(self, L, B, H_kv, d_h, max_len, dtype, device="cuda", stream=None):
+        torch = _torch()
+        self.L, self.B, self.H_kv, self.d_h, self.max_len = L, B, H_kv, d_h, max_len
+        self.dtype = dtype if isinstance(dtype, int) else dtype_code(dtype)
+        shape = (L, B, H_kv, max_len, d_h)
+        self.k = torch.zeros(shape, dtype=torch_dtype(self.dtype), device=device)
+        self.v = torch.zeros(shape, dtype=torch_dtype(self.dtype), device=device)
+        h = ctypes.c_void_p()
+        _check(load().kvc_create_external(ctypes.byref(h), L, B, H_kv, d_h, max_len, self.dtype,
+                                          self.k.data_ptr(), self.v.data_ptr(), _stream(stream)))
+        self.h = h
+
+    def close(self):
+        if self.h is not None and self.h.value:
+            load().kvc_destroy(self.h)
+        self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def kvc_create(L, B, H_kv, d_h, max_len, dtype, stream=None) -> Cache:
+    return Cache(L, B, H_kv, d_h, max_len, dtype, stream=stream)
+
+
+def kvc_append(c: Cache, layer: int, k_new, v_new, stream=None):
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype or k_new.dim() != 4:
+        raise ValueError("k_new and v_new must both be [B, H_kv, T, d_h] of one dtype")
+    if tuple(k_new.shape[:2]) != (c.B, c.H_kv) or k_new.shape[3] != c.d_h:
+        raise ValueError("k_new shape does not match the cache")
+    _check(load().kvc_append(c.h, layer, _ptr(k_new), _ptr(v_new), dtype_code(k_new.dtype),
+                             int(k_new.shape[2]), _stream(stream)), c.h)
+
+
+def kvc_commit(c: Cache, stream=None):
+    _check(load().kvc_commit(c.h, _stream(stream)), c.h)
+
+
+def kvc_truncate(c: Cache, n: int, stream=None):
+    _check(load().kvc_truncate(c.h, int(n), _stream(stream)), c.h)
+
+
+def kvc_truncate_ragged(c: Cache, n, stream=None):
+    arr = (ctypes.c_int32 * c.B)(*[int(x) for x in n])
+    _check(load().kvc_truncate_ragged(c.h, arr, _stream(stream)), c.h)
+
+
+def kvc_seq_len(c: Cache, layer: int = -1):
+    arr = (ctypes.c_int32 * c.B)()
+    _check(load().kvc_seq_len(c.h, layer, arr), c.h)
+    return [int(x) for x in arr]
+
+
+def kvc_positions(c: Cache, T: int, stream=None):
+    torch = _torch()
+    out = torch.empty((c.B, T), dtype=torch.int32, device=c.k.device)
+    _check(load().kvc_positions(c.h, T, out.data_ptr(), _stream(stream)), c.h)
+    return out
+
+
+def kvc_nbytes(c: Cache) -> int:
+    return int(load().kvc_nbytes(c.h))
+
+
+def kvc_layer_ptrs(c: Cache, layer: int):
+    k, v = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(load().kvc_layer_ptrs(c.h, layer, ctypes.byref(k), ctypes.byref(v)), c.h)
+    return k.value, v.value
+
+
+def gqa_cached_attn(c: Cache, q, layer: int, s: int = KVC_COMMITTED, out=None, stream=None):
+    """q [B, H_q, T, d_h] (float32 or the cache dtype) -> out [B, H_q, T, d_h] float32."""
+    torch = _torch()
+    if q.dim() != 4 or q.shape[0] != c.B or q.shape[3] != c.d_h:
+        raise ValueError("q must be [B, H_q, T, d_h]")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _check(load().gqa_cached_attn(c.h, _ptr(q), dtype_code(q.dtype), layer, s, int(q.shape[2]),
+                                  int(q.shape[1]), _ptr(out), _stream(stream)), c.h)
+    return out
+
+
+def kvc_status(c: Cache, stream=None):
+    _check(load().kvc_status(c.h, _stream(stream)), c.h)
+
+
+def kvc_set_split_keys(c: Cache, keys: int):
+    _check(load().kvc_set_split_keys(c.h, keys), c.h)
+
+
+def kvc_launch_count(c: Cache) -> int:
+    return int(load().kvc_launch_count(c.h))
+
+
+def synth_fill_normal(out, seed: int, stream_id: int, std: float = 1.0, offset: int = 0, stream=None):
+    """Fill a float32 CUDA tensor with the seeded draws of `kvc_synth` (same bits as the host)."""
+    torch = _torch()
+    if out.dtype != torch.float32:
+        raise ValueError("float32 tensor expected")
+    rc = load().kvc_synth_fill_normal_f32(_ptr(out), out.numel(), offset, seed, stream_id, std,
+                                          _stream(stream))
+    if rc != 0:
+        raise KvcError(rc, "synthetic fill failed")
+    return out

@@ -1,0 +1,157 @@
+// Append and length bookkeeping kernels.
+//
+// Append ("KV cache, incremental decode, ...", §4 update and §2.5 "Storage dtype"; "KV cache
+// decoding", step 5): row t of a [B, H, T, D] chunk goes to position lens[b] + delta + t of
+// (layer, b, h), rounded to the cache dtype to nearest even. Each thread moves one 16-byte group of
+// output elements, so a warp writes 512 contiguous bytes of one row (or of consecutive rows):
+// coalesced, vectorised stores with no read-modify-write. The write position comes from the
+// device's committed lengths, so the kernel stays correct when replayed from a captured graph.
+//
+// Lengths: commit adds T to every committed length, truncate overwrites them; both are one tiny
+// kernel so the device copy changes in stream order with the rest of the forward.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+template <typename Tc>
+struct Pack;   // 16 bytes of output elements
+template <>
+struct Pack<float> {
+  static constexpr int N = 4;
+  __device__ static uint4 from_f32(const float* x) {
+    return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                      __float_as_uint(x[3]));
+  }
+};
+template <>
+struct Pack<__half> {
+  static constexpr int N = 8;
+  __device__ static uint4 from_f32(const float* x) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t lo = __half_as_ushort(__float2half_rn(x[2 * i]));
+      const uint16_t hi = __half_as_ushort(__float2half_rn(x[2 * i + 1]));
+      w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <>
+struct Pack<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static uint4 from_f32(const float* x) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * i]));
+      const uint16_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * i + 1]));
+      w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// One thread per 16-byte output group; grid covers 2 (K, V) x B x H x T x D / N groups.
+template <typename Tc, bool kF32In>
+__global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+  constexpr int N = Pack<Tc>::N;
+  const int groups_per_row = a.D / N;
+  const long long rows = static_cast<long long>(a.B) * a.H * a.T;
+  const long long per_tensor = rows * groups_per_row;
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= 2 * per_tensor) return;
+  const bool is_v = gid >= per_tensor;
+  const long long g = is_v ? gid - per_tensor : gid;
+  const long long row = g / groups_per_row;             // (b, h, t) row of the chunk
+  const int grp = static_cast<int>(g % groups_per_row);
+  const int t = static_cast<int>(row % a.T);
+  const int bh = static_cast<int>(row / a.T);
+  const int b = bh / a.H, h = bh % a.H;
+  const int pos = a.lens[b] + a.delta + t;
+  const long long dst_row = ((static_cast<long long>(a.layer) * a.B + b) * a.H + h) * a.max_len + pos;
+  Tc* dst = static_cast<Tc*>(is_v ? a.v_store : a.k_store) + dst_row * a.D + grp * N;
+  const long long src_off = row * a.D + grp * N;
+  uint4 out;
+  if constexpr (kF32In) {
+    const float* src = static_cast<const float*>(is_v ? a.v_new : a.k_new) + src_off;
+    float x[N];
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const float4 f = *reinterpret_cast<const float4*>(src + i);
+      x[i] = f.x; x[i + 1] = f.y; x[i + 2] = f.z; x[i + 3] = f.w;
+    }
+    out = Pack<Tc>::from_f32(x);
+  } else {
+    const Tc* src = static_cast<const Tc*>(is_v ? a.v_new : a.k_new) + src_off;
+    out = *reinterpret_cast<const uint4*>(src);
+  }
+  *reinterpret_cast<uint4*>(dst) = out;
+}
+
+__global__ void lens_add_kernel(int32_t* lens, int B, int delta) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < B) lens[i] += delta;
+}
+
+struct LensValues {
+  int32_t v[kMaxBatch];
+};
+
+__global__ void lens_set_kernel(int32_t* lens, int B, const __grid_constant__ LensValues n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < B) lens[i] = n.v[i];
+}
+
+__global__ void positions_kernel(const int32_t* lens, int B, int T, int32_t* out) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < static_cast<long long>(B) * T) out[i] = lens[i / T] + static_cast<int>(i % T);
+}
+
+template <typename Tc>
+cudaError_t run_append(const AppendArgs& a, cudaStream_t st) {
+  constexpr int N = Pack<Tc>::N;
+  const long long total = 2LL * a.B * a.H * a.T * (a.D / N);
+  const int threads = 256;
+  const long long blocks = (total + threads - 1) / threads;
+  if (a.in_dtype == KVC_F32)
+    append_kernel<Tc, true><<<static_cast<unsigned>(blocks), threads, 0, st>>>(a);
+  else
+    append_kernel<Tc, false><<<static_cast<unsigned>(blocks), threads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
+  switch (a.cache_dtype) {
+    case KVC_F32: return run_append<float>(a, st);
+    case KVC_F16: return run_append<__half>(a, st);
+    case KVC_BF16: return run_append<__nv_bfloat16>(a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_lens_add(int32_t* lens, int B, int delta, cudaStream_t st) {
+  lens_add_kernel<<<(B + 255) / 256, 256, 0, st>>>(lens, B, delta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lens_set(int32_t* lens, int B, const int32_t* n_host, cudaStream_t st) {
+  LensValues v;
+  for (int i = 0; i < B; ++i) v.v[i] = n_host[i];
+  lens_set_kernel<<<(B + 255) / 256, 256, 0, st>>>(lens, B, v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_positions(const int32_t* lens, int B, int T, int32_t* out, cudaStream_t st) {
+  const long long n = static_cast<long long>(B) * T;
+  positions_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(lens, B, T, out);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -1,0 +1,460 @@
+// Host side of the C ABI (include/kvc.h): argument validation, the host mirrors of the per-layer
+// fill counts and committed lengths, device allocation, TMA descriptors and the split-K planner.
+//
+// Bookkeeping follows "KV cache, incremental decode, ...", §2.3 (each layer keeps its own fill
+// count; the committed length moves once per forward, after the last layer) and §2.4 (truncate
+// sets every layer's count; nothing is freed or copied). Every call validates against the host
+// mirrors first and mutates nothing on error (§4, test_update_copies_and_checks).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <new>
+#include <string>
+
+#include "kvc_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(kvc_handle h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf;
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(kvc_handle h, cudaError_t e, const char* what) {
+  return fail(h, KVC_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool valid_dtype(int t) { return t == KVC_F32 || t == KVC_F16 || t == KVC_BF16; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(std::string* err) {
+  static EncodeTiledFn fn = nullptr;
+  if (fn) return fn;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return nullptr;
+  }
+  fn = reinterpret_cast<EncodeTiledFn>(p);
+  return fn;
+}
+
+int init_device_state(kvc_handle h, cudaStream_t st) {
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaDeviceGetAttribute");
+  e = cudaMalloc(&h->d_lens, sizeof(int32_t) * h->B);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(lengths)");
+  e = cudaMalloc(&h->d_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(status)");
+  e = cudaMemsetAsync(h->d_lens, 0, sizeof(int32_t) * h->B, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->d_status, 0, sizeof(int), st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync");
+  int rows = 0;
+  kvc::splitk_shape(h->dtype, h->D, 1, &rows, &h->split_tile_keys);
+  std::string err;
+  const long long planes = static_cast<long long>(h->L) * h->B * h->H;
+  if (!kvc::encode_store_map(&h->tmap_k_split, h->k, h->dtype, h->D, h->max_len, planes,
+                             h->split_tile_keys, &err) ||
+      !kvc::encode_store_map(&h->tmap_v_split, h->v, h->dtype, h->D, h->max_len, planes,
+                             h->split_tile_keys, &err))
+    return fail(h, KVC_E_CUDA, "%s", err.c_str());
+  return KVC_OK;
+}
+
+void release(kvc_handle h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  if (h->owns_store) {
+    cudaFree(h->k);
+    cudaFree(h->v);
+  }
+  cudaFree(h->d_lens);
+  cudaFree(h->d_status);
+  cudaFree(h->work);
+  delete h;
+}
+
+int check_sizes(int L, int B, int H_kv, int d_h, int max_len, int dtype) {
+  if (L < 1 || B < 1 || H_kv < 1 || max_len < 1)
+    return fail(nullptr, KVC_E_INVAL, "sizes must be positive (L=%d B=%d H_kv=%d max_len=%d)", L, B, H_kv, max_len);
+  if (!valid_dtype(dtype)) return fail(nullptr, KVC_E_INVAL, "unknown dtype %d", dtype);
+  if (B > KVC_MAX_BATCH) return fail(nullptr, KVC_E_INVAL, "B=%d exceeds KVC_MAX_BATCH", B);
+  if (d_h != 32 && d_h != 64 && d_h != 128)
+    return fail(nullptr, KVC_E_UNSUPPORTED, "d_h=%d: kernels exist for 32, 64 and 128", d_h);
+  if (static_cast<long long>(L) * B * H_kv >= (1LL << 31) || max_len >= (1 << 30))
+    return fail(nullptr, KVC_E_INVAL, "cache too large for 32-bit tile coordinates");
+  return KVC_OK;
+}
+
+kvc_handle new_handle(int L, int B, int H_kv, int d_h, int max_len, kvc_dtype dtype) {
+  kvc_handle h = new (std::nothrow) kvc_cache();
+  if (!h) return nullptr;
+  h->L = L; h->B = B; h->H = H_kv; h->D = d_h; h->max_len = max_len; h->dtype = dtype;
+  h->fill.assign(static_cast<size_t>(L) * B, 0);
+  h->lens.assign(B, 0);
+  return h;
+}
+
+size_t store_bytes(kvc_handle h) {
+  return static_cast<size_t>(h->L) * h->B * h->H * h->max_len * h->D * kvc::itemsize(h->dtype);
+}
+
+// Uniform difference between one layer's fills and the committed lengths.
+int layer_delta(kvc_handle h, int layer, int* delta) {
+  const int d0 = h->fill[static_cast<size_t>(layer) * h->B] - h->lens[0];
+  for (int b = 1; b < h->B; ++b)
+    if (h->fill[static_cast<size_t>(layer) * h->B + b] - h->lens[b] != d0)
+      return fail(h, KVC_E_STATE, "layer %d: appended rows differ between sequences", layer);
+  *delta = d0;
+  return KVC_OK;
+}
+
+}  // namespace
+
+namespace kvc {
+
+bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max_len,
+                      long long planes, int box_rows, std::string* err) {
+  EncodeTiledFn fn = encode_fn(err);
+  if (!fn) return false;
+  const int es = itemsize(dt);
+  const int row_bytes = D * es;
+  const int span = row_bytes >= 128 ? 128 : 64;
+  const CUtensorMapDataType ty = dt == KVC_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dt == KVC_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(max_len),
+                              static_cast<cuuint64_t>(planes)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
+                                 static_cast<cuuint64_t>(row_bytes) * max_len};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(span / es), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, ty, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[128];
+    snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    *err = buf;
+    return false;
+  }
+  return true;
+}
+
+}  // namespace kvc
+
+extern "C" {
+
+int kvc_create(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len, kvc_dtype dtype,
+               void* stream) {
+  if (!out) return fail(nullptr, KVC_E_INVAL, "null output handle");
+  *out = nullptr;
+  int rc = check_sizes(L, B, H_kv, d_h, max_len, dtype);
+  if (rc) return rc;
+  kvc_handle h = new_handle(L, B, H_kv, d_h, max_len, dtype);
+  if (!h) return fail(nullptr, KVC_E_NOMEM, "host allocation failed");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = store_bytes(h);
+  cudaError_t e = cudaMalloc(&h->k, bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->v, bytes);
+  h->owns_store = true;
+  if (e != cudaSuccess) {
+    rc = fail(nullptr, KVC_E_NOMEM, "cudaMalloc of 2 x %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+    cudaGetLastError();
+    release(h);
+    return rc;
+  }
+  e = cudaMemsetAsync(h->k, 0, bytes, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->v, 0, bytes, st);
+  if (e != cudaSuccess) {
+    rc = cuda_fail(nullptr, e, "cudaMemsetAsync(store)");
+    release(h);
+    return rc;
+  }
+  rc = init_device_state(h, st);
+  if (rc) {
+    g_err = h->err;
+    release(h);
+    return rc;
+  }
+  *out = h;
+  return KVC_OK;
+}
+
+int kvc_create_external(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len,
+                        kvc_dtype dtype, void* k_store, void* v_store, void* stream) {
+  if (!out) return fail(nullptr, KVC_E_INVAL, "null output handle");
+  *out = nullptr;
+  int rc = check_sizes(L, B, H_kv, d_h, max_len, dtype);
+  if (rc) return rc;
+  if (!k_store || !v_store) return fail(nullptr, KVC_E_INVAL, "null store pointer");
+  if (!aligned(k_store, 256) || !aligned(v_store, 256))
+    return fail(nullptr, KVC_E_INVAL, "store pointers must be 256-byte aligned");
+  kvc_handle h = new_handle(L, B, H_kv, d_h, max_len, dtype);
+  if (!h) return fail(nullptr, KVC_E_NOMEM, "host allocation failed");
+  h->k = k_store;
+  h->v = v_store;
+  rc = init_device_state(h, static_cast<cudaStream_t>(stream));
+  if (rc) {
+    g_err = h->err;
+    release(h);
+    return rc;
+  }
+  *out = h;
+  return KVC_OK;
+}
+
+int kvc_destroy(kvc_handle h) {
+  release(h);
+  return KVC_OK;
+}
+
+int kvc_append(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
+               int T, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
+  if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
+  if (!k_new || !v_new) return fail(h, KVC_E_INVAL, "null k_new/v_new");
+  if (!valid_dtype(in_dtype) || (in_dtype != KVC_F32 && in_dtype != h->dtype))
+    return fail(h, KVC_E_INVAL, "input dtype %d must be F32 or the cache dtype", in_dtype);
+  if (!aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(h, KVC_E_INVAL, "k_new/v_new must be 16-byte aligned");
+  int delta = 0;
+  int rc = layer_delta(h, layer, &delta);
+  if (rc) return rc;
+  for (int b = 0; b < h->B; ++b) {
+    const long long end = static_cast<long long>(h->fill[static_cast<size_t>(layer) * h->B + b]) + T;
+    if (end > h->max_len)
+      return fail(h, KVC_E_CAPACITY, "sequence %d: %lld positions exceed max_len=%d", b, end, h->max_len);
+  }
+  kvc::AppendArgs a{};
+  a.k_store = h->k; a.v_store = h->v; a.k_new = k_new; a.v_new = v_new; a.lens = h->d_lens;
+  a.layer = layer; a.B = h->B; a.H = h->H; a.D = h->D; a.T = T; a.max_len = h->max_len;
+  a.delta = delta; a.cache_dtype = h->dtype; a.in_dtype = in_dtype;
+  cudaError_t e = kvc::launch_append(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "append launch");
+  h->launches += 1;
+  for (int b = 0; b < h->B; ++b) h->fill[static_cast<size_t>(layer) * h->B + b] += T;
+  return KVC_OK;
+}
+
+int kvc_commit(kvc_handle h, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  for (int l = 1; l < h->L; ++l)
+    for (int b = 0; b < h->B; ++b)
+      if (h->fill[static_cast<size_t>(l) * h->B + b] != h->fill[b])
+        return fail(h, KVC_E_STATE, "commit: layer %d holds %d rows of sequence %d, layer 0 holds %d",
+                    l, h->fill[static_cast<size_t>(l) * h->B + b], b, h->fill[b]);
+  int delta = 0;
+  int rc = layer_delta(h, 0, &delta);
+  if (rc) return rc;
+  if (delta != 0) {
+    cudaError_t e = kvc::launch_lens_add(h->d_lens, h->B, delta, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "commit launch");
+    h->launches += 1;
+  }
+  for (int b = 0; b < h->B; ++b) h->lens[b] = h->fill[b];
+  return KVC_OK;
+}
+
+int kvc_truncate_ragged(kvc_handle h, const int32_t* n, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (!n) return fail(h, KVC_E_INVAL, "null lengths");
+  for (int b = 0; b < h->B; ++b) {
+    if (n[b] < 0) return fail(h, KVC_E_INVAL, "sequence %d: negative length %d", b, n[b]);
+    if (n[b] > h->lens[b])
+      return fail(h, KVC_E_STATE, "sequence %d: truncate to %d beyond committed length %d", b, n[b], h->lens[b]);
+  }
+  cudaError_t e = kvc::launch_lens_set(h->d_lens, h->B, n, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "truncate launch");
+  h->launches += 1;
+  for (int b = 0; b < h->B; ++b) {
+    h->lens[b] = n[b];
+    for (int l = 0; l < h->L; ++l) h->fill[static_cast<size_t>(l) * h->B + b] = n[b];
+  }
+  return KVC_OK;
+}
+
+int kvc_truncate(kvc_handle h, int n, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  std::unique_ptr<int32_t[]> v(new (std::nothrow) int32_t[h->B]);
+  if (!v) return fail(h, KVC_E_NOMEM, "host allocation failed");
+  for (int b = 0; b < h->B; ++b) v[b] = n;
+  return kvc_truncate_ragged(h, v.get(), stream);
+}
+
+int kvc_seq_len(kvc_handle h, int layer, int32_t* out) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (!out) return fail(h, KVC_E_INVAL, "null output");
+  if (layer < -1 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range", layer);
+  for (int b = 0; b < h->B; ++b)
+    out[b] = layer < 0 ? h->lens[b] : h->fill[static_cast<size_t>(layer) * h->B + b];
+  return KVC_OK;
+}
+
+int kvc_positions(kvc_handle h, int T, int32_t* out, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (T < 1 || !out) return fail(h, KVC_E_INVAL, "T must be >= 1 and out non-null");
+  cudaError_t e = kvc::launch_positions(h->d_lens, h->B, T, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "positions launch");
+  h->launches += 1;
+  return KVC_OK;
+}
+
+size_t kvc_nbytes(kvc_handle h) { return h ? 2 * store_bytes(h) : 0; }
+
+int kvc_layer_ptrs(kvc_handle h, int layer, void** k, void** v) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (layer < 0 || layer >= h->L || !k || !v) return fail(h, KVC_E_INVAL, "bad layer or null output");
+  const size_t off = static_cast<size_t>(layer) * h->B * h->H * h->max_len * h->D * kvc::itemsize(h->dtype);
+  *k = static_cast<char*>(h->k) + off;
+  *v = static_cast<char*>(h->v) + off;
+  return KVC_OK;
+}
+
+int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
+                    float* out, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
+  if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
+  if (!q || !out) return fail(h, KVC_E_INVAL, "null q/out");
+  if (H_q < 1 || H_q % h->H) return fail(h, KVC_E_INVAL, "H_q=%d must be a positive multiple of H_kv=%d", H_q, h->H);
+  if (!valid_dtype(q_dtype) || (q_dtype != KVC_F32 && q_dtype != h->dtype))
+    return fail(h, KVC_E_INVAL, "query dtype %d must be F32 or the cache dtype", q_dtype);
+  if (!aligned(q, 16) || !aligned(out, 16)) return fail(h, KVC_E_INVAL, "q/out must be 16-byte aligned");
+  if (s < KVC_COMMITTED) return fail(h, KVC_E_INVAL, "s=%d", s);
+  for (int b = 0; b < h->B; ++b) {
+    if (s >= 0 && h->lens[b] != s)
+      return fail(h, KVC_E_STATE, "s=%d but sequence %d has committed length %d", s, b, h->lens[b]);
+    if (h->fill[static_cast<size_t>(layer) * h->B + b] != h->lens[b] + T)
+      return fail(h, KVC_E_STATE, "layer %d holds %d rows of sequence %d; attention needs s_b + T = %d "
+                  "(append the chunk to this layer first)", layer, h->fill[static_cast<size_t>(layer) * h->B + b],
+                  b, h->lens[b] + T);
+  }
+  const int G = H_q / h->H;
+  const int R = T * G;
+  int rpt = 0, tile = 0;
+  if (!kvc::splitk_shape(h->dtype, h->D, R, &rpt, &tile))
+    return fail(h, KVC_E_UNSUPPORTED, "no split-K kernel for d_h=%d", h->D);
+  const int n_rt = (R + rpt - 1) / rpt;
+  if (static_cast<long long>(h->B) * n_rt > kvc::kMaxUnits)
+    return fail(h, KVC_E_UNSUPPORTED, "B * row tiles = %lld exceeds %d", static_cast<long long>(h->B) * n_rt,
+                kvc::kMaxUnits);
+
+  static thread_local kvc::SplitPlan plan;   // large: keep it off the stack
+  plan.n_units = h->B * n_rt;
+  plan.rows_per_tile = rpt;
+  plan.n_rowtiles = n_rt;
+  long long total_keys = 0;
+  for (int b = 0; b < h->B; ++b)
+    for (int rt = 0; rt < n_rt; ++rt) {
+      const int t_max = std::min(T - 1, ((rt + 1) * rpt - 1) / G);
+      total_keys += static_cast<long long>(h->lens[b]) + t_max + 1;
+    }
+  const int cmax = (4096 / rpt) / tile * tile;              // the kernel's score buffer
+  int split = h->split_keys_override;
+  if (split <= 0) {
+    // aim for ~8 CTAs per SM in total (two resident per SM, about four waves)
+    const long long target = 8LL * h->num_sms;
+    split = static_cast<int>((total_keys * h->H + target - 1) / target);
+  }
+  split = std::max(tile, std::min(cmax, (split + tile - 1) / tile * tile));
+  plan.split_keys = split;
+  long long items = 0;
+  plan.prefix[0] = 0;
+  for (int b = 0; b < h->B; ++b)
+    for (int rt = 0; rt < n_rt; ++rt) {
+      const int u = b * n_rt + rt;
+      const int t_max = std::min(T - 1, ((rt + 1) * rpt - 1) / G);
+      const long long n_eff = static_cast<long long>(h->lens[b]) + t_max + 1;
+      items += h->H * ((n_eff + split - 1) / split);
+      if (items >= (1LL << 31)) return fail(h, KVC_E_UNSUPPORTED, "too many work items");
+      plan.prefix[u + 1] = static_cast<int32_t>(items);
+      plan.unit_b[u] = b;
+    }
+  plan.n_items = static_cast<int>(items);
+
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (plan.n_items > plan.n_units * h->H) {
+    const size_t need = kvc::splitk_workspace_floats(plan, h->D);
+    if (need > h->work_floats) {
+      const size_t grow = need + need / 4;
+      float* p = nullptr;
+      cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&p), grow * sizeof(float), st);
+      if (e != cudaSuccess) return fail(h, KVC_E_NOMEM, "workspace cudaMallocAsync: %s", cudaGetErrorString(e));
+      if (h->work) cudaFreeAsync(h->work, st);
+      h->work = p;
+      h->work_floats = grow;
+    }
+  }
+  kvc::AttnArgs a{};
+  a.q = q; a.q_dtype = q_dtype; a.out = out;
+  a.part_o = h->work;
+  a.part_ml = h->work ? h->work + static_cast<size_t>(plan.n_items) * rpt * h->D : nullptr;
+  a.lens = h->d_lens; a.status = h->d_status;
+  a.layer = layer; a.B = h->B; a.H_kv = h->H; a.H_q = H_q; a.G = G; a.T = T; a.D = h->D;
+  a.max_len = h->max_len; a.delta = T; a.cache_dtype = h->dtype;
+  cudaError_t e = kvc::launch_splitk(a, plan, &h->tmap_k_split, &h->tmap_v_split, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
+  h->launches += (plan.n_items > plan.n_units * h->H) ? 2 : 1;
+  return KVC_OK;
+}
+
+int kvc_status(kvc_handle h, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+  int flag = 0;
+  e = cudaMemcpy(&flag, h->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "status read");
+  if (flag) {
+    const int zero = 0;
+    cudaMemcpy(h->d_status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return fail(h, KVC_E_DEVICE_TIMEOUT, "a kernel's bounded wait gave up (status %d)", flag);
+  }
+  return KVC_OK;
+}
+
+int kvc_last_error(kvc_handle h, char* buf, size_t n) {
+  if (!buf || n == 0) return KVC_E_INVAL;
+  const std::string& s = h ? h->err : g_err;
+  const size_t k = std::min(n - 1, s.size());
+  memcpy(buf, s.data(), k);
+  buf[k] = '\0';
+  return KVC_OK;
+}
+
+uint64_t kvc_launch_count(kvc_handle h) { return h ? h->launches : 0; }
+
+int kvc_set_split_keys(kvc_handle h, int keys) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (keys < 0) return fail(h, KVC_E_INVAL, "keys=%d", keys);
+  h->split_keys_override = keys;
+  return KVC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Internal declarations shared by the host side (kvc_host.cpp) and the kernels (*.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+constexpr int kMaxBatch = KVC_MAX_BATCH;
+// Units (sequence, row tile) a split-K launch can plan for; the plan travels in the kernel's
+// parameters, so this bounds their size (2 * 4 * kMaxUnits bytes).
+constexpr int kMaxUnits = 2048;
+
+inline int itemsize(kvc_dtype t) { return t == KVC_F32 ? 4 : 2; }
+
+// Device status word values written by kernels whose bounded waits give up.
+constexpr int kStatusTimeout = 1;
+
+// ------------------------------------------------------------------------------------------------
+// Append: writes a [B, H, T, D] chunk at row lens[b] + delta + t of each (layer, b, h).
+// ------------------------------------------------------------------------------------------------
+struct AppendArgs {
+  void* k_store;            // [L, B, H, max_len, D] cache dtype
+  void* v_store;
+  const void* k_new;        // [B, H, T, D] in_dtype
+  const void* v_new;
+  const int32_t* lens;      // device committed lengths [B]
+  int layer, B, H, D, T, max_len;
+  int delta;                // this layer's fill minus the committed length (uniform over b)
+  kvc_dtype cache_dtype, in_dtype;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
+
+// lens[b] += delta for all b
+cudaError_t launch_lens_add(int32_t* lens, int B, int delta, cudaStream_t st);
+// lens[b] = n[b]
+cudaError_t launch_lens_set(int32_t* lens, int B, const int32_t* n_host, cudaStream_t st);
+// out[b * T + t] = lens[b] + t
+cudaError_t launch_positions(const int32_t* lens, int B, int T, int32_t* out, cudaStream_t st);
+
+// ------------------------------------------------------------------------------------------------
+// Split-K attention on CUDA cores (decode and short chunks): plan built on the host from the
+// host mirror of the lengths; the kernel reads the lengths themselves from the device.
+// ------------------------------------------------------------------------------------------------
+struct SplitPlan {
+  int n_units;                       // units = (sequence b, row tile rt)
+  int n_items;                       // CTAs: sum over units of H_kv * nsplit
+  int split_keys;                    // keys per split (multiple of the kernel's tile)
+  int rows_per_tile;                 // query rows (t, g) per unit
+  int n_rowtiles;                    // row tiles per sequence
+  int32_t prefix[kMaxUnits + 1];     // item prefix over units
+  int32_t unit_b[kMaxUnits];         // sequence of each unit (rt = unit % n_rowtiles)
+};
+
+struct AttnArgs {
+  const void* q;            // [B, H_q, T, D]
+  kvc_dtype q_dtype;
+  float* out;               // [B, H_q, T, D]
+  float* part_o;            // [n_items, rows_per_tile, D] workspace
+  float* part_ml;           // [n_items, rows_per_tile, 2] workspace
+  const int32_t* lens;      // device committed lengths
+  int* status;              // device status word
+  int layer, B, H_kv, H_q, G, T, D, max_len;
+  int delta;                // fill - committed for this layer (== T when the chunk was appended)
+  kvc_dtype cache_dtype;
+};
+// Workspace floats the plan needs (0 when no unit splits).
+size_t splitk_workspace_floats(const SplitPlan& p, int D);
+// Choose rows per tile and tile keys for (dtype, D, rows); returns false if unsupported.
+bool splitk_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys);
+cudaError_t launch_splitk(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
+                          const CUtensorMap* tv, cudaStream_t st);
+
+// Tensor map over a store viewed as [L*B*H, max_len, D] with boxes of (swizzle span, box_rows, 1).
+bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max_len,
+                      long long planes, int box_rows, std::string* err);
+
+}  // namespace kvc
+
+struct kvc_cache {
+  int L = 0, B = 0, H = 0, D = 0, max_len = 0;
+  kvc_dtype dtype = KVC_F32;
+  bool owns_store = false;
+  void* k = nullptr;
+  void* v = nullptr;
+  int32_t* d_lens = nullptr;      // committed lengths on the device
+  int* d_status = nullptr;        // device status word
+  std::vector<int32_t> fill;      // host mirror [L * B]
+  std::vector<int32_t> lens;      // host mirror [B]
+  CUtensorMap tmap_k_split{}, tmap_v_split{};
+  int split_tile_keys = 0;
+  float* work = nullptr;          // split-K workspace
+  size_t work_floats = 0;
+  int split_keys_override = 0;
+  uint64_t launches = 0;          // kernels enqueued by this handle
+  int num_sms = 0;
+  int device = 0;
+  std::string err;
+};

@@ -1,0 +1,539 @@
+// Split-K grouped-query attention over the KV cache on CUDA cores (decode T = 1 and short chunks).
+//
+// What it computes ("KV cache, incremental decode, ...", §2.3; "Generation and the KV Cache",
+// fence 3; "Heads, GQA and K/V cache", "Four queries, two sets of K/V"): for sequence b, K/V head
+// g and the G query heads h = g*G .. g*G+G-1 that share it, every query row (t, h) of the chunk
+// attends over stored keys j <= s_b + t with weights softmax_j(q . k_j / sqrt(d_h)), summing v_j.
+//
+// How (GB300): the query rows of one K/V head are packed together ("row tile": rows r = t*G + g),
+// so each K/V tile read from HBM serves the whole group; K/V are never repeated per query head.
+// One CTA handles one (row tile, K/V head, key split). A producer warp streams the split's K tiles
+// and then its V tiles, HBM -> shared memory, with TMA (128-byte swizzle, so lane-per-key reads
+// are bank-conflict free) through a 4-stage mbarrier ring; four consumer warps compute.
+//   QK:  one lane per key (or 2-4 lanes per key for wide rows), q broadcast from shared memory,
+//        scores for the whole split kept in shared memory;
+//   softmax: exact within the split (max, exp2, sum) — no running rescale;
+//   PV:  one lane per d_h slice, weights broadcast from shared memory, warps split the keys and
+//        are reduced through shared memory at the end.
+// A split writes (m, l, o) partials unless it is its unit's only split, in which case it writes
+// the normalised output. `combine_kernel` merges partials with the log-sum-exp rule.
+//
+// Every wait is bounded (about one second); a wait that gives up sets the device status word and
+// the CTA skips its remaining work instead of hanging.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kStages = 4;
+constexpr int kTileBytes = 16384;
+constexpr int kScoreFloats = 4096;             // per-split score buffer (rows x keys)
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename Tc, int D, int RMAX>
+struct Cfg {
+  static constexpr int E = sizeof(Tc);
+  static constexpr int ROWB = D * E;                    // bytes per key row
+  static constexpr int SW = ROWB >= 128 ? 128 : 64;     // swizzle span (bytes) = TMA box row
+  static constexpr int CPB = SW / 16;                   // 16-byte chunks per box row
+  static constexpr int NBOX = ROWB / SW;                // boxes per key row
+  static constexpr int BOX_INNER = SW / E;              // elements per box row
+  static constexpr int TILE = kTileBytes / ROWB;        // keys per tile
+  static constexpr int EPC = 16 / E;                    // elements per 16-byte chunk
+  static constexpr int CPR = ROWB / 16;                 // chunks per key row
+  static constexpr int DSPLIT = TILE >= 128 ? 1 : 128 / TILE;   // lanes sharing one key in QK
+  static constexpr int KPT = TILE >= 128 ? TILE / 128 : 1;      // keys per lane in QK
+  static constexpr int LPK = 32 / DSPLIT;               // distinct keys per warp in QK
+  static constexpr int CPP = CPR / DSPLIT;              // chunks per lane in QK
+  static constexpr int DPART = D / DSPLIT;              // elements per lane part in QK
+  static constexpr int QSTRIDE = D + 4 * DSPLIT;        // padded q row (floats) in shared memory
+  static constexpr int EPL = D / 32;                    // V elements per lane in PV
+  static_assert(TILE <= 256 && TILE % kConsumerWarps == 0, "tile");
+  static_assert(CPR % DSPLIT == 0, "split");
+  static_assert(RMAX % 4 == 0, "row blocks of 4");
+};
+
+struct __align__(8) Smem {
+  unsigned long long full[kStages];
+  unsigned long long empty[kStages];
+  int abort;
+  float m[16];
+  float l[16];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase; false when it gave up (or another thread already did).
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  unsigned long long t0 = 0;
+  for (int it = 0;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 31) == 31) {
+      if (*abort_flag) return false;
+      unsigned long long t = now_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > kWaitLimitNs) { *abort_flag = 1; return false; }
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(dst), "l"(reinterpret_cast<unsigned long long>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" :: "n"(kConsumers) : "memory");
+}
+
+// Byte offset, inside one tile, of 16-byte chunk `chunk` of key row `key` (TMA swizzle layout).
+template <class C>
+__device__ __forceinline__ uint32_t tile_off(int key, int chunk) {
+  const int box = chunk / C::CPB, cc = chunk % C::CPB;
+  const int sw = (C::SW == 128) ? (key & 7) : ((key >> 1) & 3);
+  return box * (C::TILE * C::SW) + key * C::SW + ((cc ^ sw) << 4);
+}
+
+// 16 bytes of stored elements -> floats
+template <typename Tc> __device__ __forceinline__ void unpack16(const uint4& r, float* f);
+template <> __device__ __forceinline__ void unpack16<float>(const uint4& r, float* f) {
+  f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+  f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+}
+template <> __device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4& r, float* f) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+template <> __device__ __forceinline__ void unpack16<__half>(const uint4& r, float* f) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+    float2 x = __half22float2(h);
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
+}
+
+template <typename Tc> __device__ __forceinline__ float to_f32(Tc x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// A query element as the attention uses it: an F32 query meets a 16-bit cache rounded to it.
+template <typename Tc>
+__device__ __forceinline__ float load_query(const void* q, kvc_dtype qt, long long i) {
+  if (qt == KVC_F32) {
+    float x = static_cast<const float*>(q)[i];
+    if constexpr (sizeof(Tc) == 2) {
+      if constexpr (std::is_same<Tc, __half>::value) return __half2float(__float2half_rn(x));
+      else return __bfloat162float(__float2bfloat16_rn(x));
+    }
+    return x;
+  }
+  return to_f32<Tc>(static_cast<const Tc*>(q)[i]);
+}
+
+// V elements [lane*EPL, lane*EPL + EPL) of key row `key` in a V tile.
+template <typename Tc, class C>
+__device__ __forceinline__ void load_v(const unsigned char* tile, int key, int lane, float* v) {
+  constexpr int BYTES = C::EPL * C::E;                  // bytes per lane: 2, 4, 8 or 16
+  const int byte0 = lane * BYTES;
+  const unsigned char* p = tile + tile_off<C>(key, byte0 >> 4) + (byte0 & 15);
+  if constexpr (BYTES == 16) {
+    unpack16<Tc>(*reinterpret_cast<const uint4*>(p), v);
+  } else if constexpr (BYTES == 8) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    if constexpr (sizeof(Tc) == 4) {
+      v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
+    } else {
+      uint4 r4 = make_uint4(r.x, r.y, 0, 0);
+      float f[8];
+      unpack16<Tc>(r4, f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = f[i];
+    }
+  } else if constexpr (BYTES == 4) {
+    const uint32_t r = *reinterpret_cast<const uint32_t*>(p);
+    if constexpr (sizeof(Tc) == 4) {
+      v[0] = __uint_as_float(r);
+    } else {
+      uint4 r4 = make_uint4(r, 0, 0, 0);
+      float f[8];
+      unpack16<Tc>(r4, f);
+      v[0] = f[0]; v[1] = f[1];
+    }
+  } else {
+    v[0] = to_f32<Tc>(*reinterpret_cast<const Tc*>(p));
+  }
+}
+
+template <typename Tc, int D, int RMAX>
+__global__ void __launch_bounds__(kThreads, 2)
+splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
+              const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+  using C = Cfg<Tc, D, RMAX>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // layout: [stages x 16 KB tiles][scores][q rows][Smem]
+  unsigned char* tiles = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* S = reinterpret_cast<float*>(tiles + kStages * kTileBytes);
+  float* qs = S + kScoreFloats;
+  Smem* sm = reinterpret_cast<Smem*>(qs + RMAX * C::QSTRIDE);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- which (unit, K/V head, split) this CTA owns --------------------------------------------
+  const int item = blockIdx.x;
+  int lo = 0, hi = plan.n_units - 1;
+  while (lo < hi) {                        // last unit u with prefix[u] <= item
+    const int mid = (lo + hi + 1) >> 1;
+    if (plan.prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  const int unit = lo;
+  const int nsplit = (plan.prefix[unit + 1] - plan.prefix[unit]) / a.H_kv;
+  const int rem = item - plan.prefix[unit];
+  const int kvh = rem / nsplit, split = rem % nsplit;
+  const int b = plan.unit_b[unit];
+  const int rt = unit % plan.n_rowtiles;
+  const int R = a.T * a.G;                              // query rows of this K/V head
+  const int row0 = rt * RMAX;
+  const int nrows = min(RMAX, R - row0);
+  const int s_b = a.lens[b] + a.delta - a.T;            // committed length = first query position
+  const int t_max = (row0 + nrows - 1) / a.G;
+  const int n_eff = s_b + t_max + 1;                    // keys visible to the tile's last row
+  const int k_begin = split * plan.split_keys;
+  const int k_end = min(k_begin + plan.split_keys, n_eff);
+  const int n_keys = k_end - k_begin;
+  const int nkt = (n_keys + C::TILE - 1) / C::TILE;
+  const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), kConsumerWarps);
+    }
+    sm->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // queries of the tile, prescaled by log2(e) / sqrt(d_h): S holds scores in base-2 units
+  const float qscale = kLog2e * rsqrtf(static_cast<float>(D));
+  for (int i = tid; i < RMAX * D; i += kThreads) {
+    const int r = i / D, e = i % D;
+    float x = 0.f;
+    if (r < nrows) {
+      const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+      const long long qi = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + e;
+      x = load_query<Tc>(a.q, a.q_dtype, qi) * qscale;
+    }
+    qs[r * C::QSTRIDE + e + (e / C::DPART) * 4] = x;
+  }
+  __syncthreads();
+
+  volatile int* abort_flag = &sm->abort;
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------- producer ------------------------------------------
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<unsigned long long>(&tk)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<unsigned long long>(&tv)) : "memory");
+      for (int i = 0; i < 2 * nkt; ++i) {
+        const int st = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        if (!mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1, abort_flag)) break;
+        const bool isv = i >= nkt;
+        const int y = k_begin + (isv ? i - nkt : i) * C::TILE;
+        const uint32_t full = smem_u32(&sm->full[st]);
+        mbar_expect_tx(full, kTileBytes);
+        const uint32_t dst = smem_u32(tiles + st * kTileBytes);
+#pragma unroll
+        for (int bx = 0; bx < C::NBOX; ++bx)
+          tma_load_3d(dst + bx * C::TILE * C::SW, isv ? &tv : &tk, bx * C::BOX_INNER, y, plane, full);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------- consumers: QK ------------------------------------------
+  const int part = lane / C::LPK;
+  const int key_in_warp = lane % C::LPK;
+  for (int i = 0; i < nkt; ++i) {
+    const int st = i % kStages;
+    const bool ok = mbar_wait(smem_u32(&sm->full[st]), (i / kStages) & 1, abort_flag);
+    if (ok) {
+      const unsigned char* tile = tiles + st * kTileBytes;
+#pragma unroll
+      for (int kp = 0; kp < C::KPT; ++kp) {
+        const int key = kp * (kConsumerWarps * C::LPK) + warp * C::LPK + key_in_warp;
+        const int kabs = k_begin + i * C::TILE + key;
+#pragma unroll
+        for (int rb = 0; rb < RMAX / 4; ++rb) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < C::CPP; ++c) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(tile + tile_off<C>(key, part * C::CPP + c));
+            float kf[C::EPC];
+            unpack16<Tc>(raw, kf);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float* qr = qs + (rb * 4 + j) * C::QSTRIDE + part * (C::DPART + 4) + c * C::EPC;
+#pragma unroll
+              for (int e4 = 0; e4 < C::EPC; e4 += 4) {
+                const float4 qv = *reinterpret_cast<const float4*>(qr + e4);
+                acc[j] = fmaf(qv.x, kf[e4], acc[j]);
+                acc[j] = fmaf(qv.y, kf[e4 + 1], acc[j]);
+                acc[j] = fmaf(qv.z, kf[e4 + 2], acc[j]);
+                acc[j] = fmaf(qv.w, kf[e4 + 3], acc[j]);
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int o = C::LPK; o < 32; o <<= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+          }
+          if (part == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int r = rb * 4 + j;
+              const int t = (row0 + r) / a.G;
+              const bool vis = kabs < k_end && kabs <= s_b + t;
+              S[(i * C::TILE + key) * RMAX + r] = vis ? acc[j] : -INFINITY;
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm->empty[st]));
+  }
+  consumers_sync();
+
+  // ---------------------------------- softmax within the split ---------------------------------
+  const int n_slots = nkt * C::TILE;
+  for (int r = warp; r < RMAX; r += kConsumerWarps) {
+    float m = -INFINITY;
+    for (int k = lane; k < n_slots; k += 32) m = fmaxf(m, S[k * RMAX + r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float l = 0.f;
+    for (int k = lane; k < n_slots; k += 32) {
+      const float p = (m == -INFINITY) ? 0.f : exp2f(S[k * RMAX + r] - m);
+      S[k * RMAX + r] = p;
+      l += p;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) { sm->m[r] = m; sm->l[r] = l; }
+  }
+  consumers_sync();
+
+  // ---------------------------------- consumers: PV ------------------------------------------
+  float acc[RMAX][C::EPL];
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+    for (int e = 0; e < C::EPL; ++e) acc[r][e] = 0.f;
+  constexpr int KPW = C::TILE / kConsumerWarps;        // keys per warp per tile
+  for (int i = 0; i < nkt; ++i) {
+    const int ti = nkt + i;
+    const int st = ti % kStages;
+    const bool ok = mbar_wait(smem_u32(&sm->full[st]), (ti / kStages) & 1, abort_flag);
+    if (ok) {
+      const unsigned char* tile = tiles + st * kTileBytes;
+#pragma unroll 4
+      for (int kk = 0; kk < KPW; ++kk) {
+        const int key = warp * KPW + kk;
+        float v[C::EPL];
+        load_v<Tc, C>(tile, key, lane, v);
+        const float* pr = S + (i * C::TILE + key) * RMAX;
+#pragma unroll
+        for (int r4 = 0; r4 < RMAX; r4 += 4) {
+          const float4 p = *reinterpret_cast<const float4*>(pr + r4);
+#pragma unroll
+          for (int e = 0; e < C::EPL; ++e) {
+            acc[r4][e] = fmaf(p.x, v[e], acc[r4][e]);
+            acc[r4 + 1][e] = fmaf(p.y, v[e], acc[r4 + 1][e]);
+            acc[r4 + 2][e] = fmaf(p.z, v[e], acc[r4 + 2][e]);
+            acc[r4 + 3][e] = fmaf(p.w, v[e], acc[r4 + 3][e]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm->empty[st]));
+  }
+  consumers_sync();                                      // every tile consumed: ring is free
+
+  // ---------------------------------- reduce warps, write ------------------------------------
+  float* red = reinterpret_cast<float*>(tiles);          // [warps][RMAX][D]
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+    for (int e = 0; e < C::EPL; ++e) red[(warp * RMAX + r) * D + lane * C::EPL + e] = acc[r][e];
+  consumers_sync();
+  if (*abort_flag) {
+    if (tid == 0) atomicExch(a.status, kStatusTimeout);
+    return;
+  }
+  for (int i = tid; i < nrows * D; i += kConsumers) {
+    const int r = i / D, d = i % D;
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) o += red[(w * RMAX + r) * D + d];
+    const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+    if (nsplit == 1) {
+      const long long oi = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d;
+      a.out[oi] = o / sm->l[r];
+    } else {
+      a.part_o[(static_cast<long long>(item) * RMAX + r) * D + d] = o;
+      if (d == 0) {
+        a.part_ml[(static_cast<long long>(item) * RMAX + r) * 2] = sm->m[r];
+        a.part_ml[(static_cast<long long>(item) * RMAX + r) * 2 + 1] = sm->l[r];
+      }
+    }
+  }
+}
+
+// Merge the splits of each (unit, K/V head): o = sum_i 2^(m_i - m) o_i / sum_i 2^(m_i - m) l_i,
+// evaluated as a running merge over the splits (any number of them).
+template <int RMAX>
+__global__ void __launch_bounds__(128)
+combine_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan) {
+  const int unit = blockIdx.x / a.H_kv, kvh = blockIdx.x % a.H_kv;
+  const int nsplit = (plan.prefix[unit + 1] - plan.prefix[unit]) / a.H_kv;
+  if (nsplit == 1) return;
+  const int item0 = plan.prefix[unit] + kvh * nsplit;
+  const int b = plan.unit_b[unit], rt = unit % plan.n_rowtiles;
+  const int row0 = rt * RMAX;
+  const int nrows = min(RMAX, a.T * a.G - row0);
+  const int D = a.D;
+  for (int i = threadIdx.x; i < nrows * D; i += blockDim.x) {
+    const int r = i / D, d = i % D;
+    float m = -INFINITY, l = 0.f, o = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const long long base = static_cast<long long>(item0 + s) * RMAX + r;
+      const float ms = a.part_ml[base * 2], ls = a.part_ml[base * 2 + 1];
+      if (!(ls > 0.f)) continue;                         // a split that sees no key of this row
+      const float mn = fmaxf(m, ms);
+      const float c_old = exp2f(m - mn), c_new = exp2f(ms - mn);
+      l = l * c_old + ls * c_new;
+      o = o * c_old + a.part_o[base * D + d] * c_new;
+      m = mn;
+    }
+    const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+    a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / l;
+  }
+}
+
+template <typename Tc, int D, int RMAX>
+size_t smem_bytes() {
+  using C = Cfg<Tc, D, RMAX>;
+  return 1024 + kStages * kTileBytes + kScoreFloats * 4 + RMAX * C::QSTRIDE * 4 + sizeof(Smem);
+}
+
+template <typename Tc, int D, int RMAX>
+cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, const CUtensorMap* tv,
+                cudaStream_t st) {
+  const size_t smem = smem_bytes<Tc, D, RMAX>();
+  auto kern = splitk_kernel<Tc, D, RMAX>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<p.n_items, kThreads, smem, st>>>(a, p, *tk, *tv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.n_items > p.n_units * a.H_kv) {
+    combine_kernel<RMAX><<<p.n_units * a.H_kv, 128, 0, st>>>(a, p);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+template <typename Tc, int D>
+cudaError_t run_rows(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
+                     const CUtensorMap* tv, cudaStream_t st) {
+  switch (p.rows_per_tile) {
+    case 4: return run<Tc, D, 4>(a, p, tk, tv, st);
+    case 8: return run<Tc, D, 8>(a, p, tk, tv, st);
+    case 16: return run<Tc, D, 16>(a, p, tk, tv, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename Tc>
+cudaError_t run_d(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, const CUtensorMap* tv,
+                  cudaStream_t st) {
+  switch (a.D) {
+    case 32: return run_rows<Tc, 32>(a, p, tk, tv, st);
+    case 64: return run_rows<Tc, 64>(a, p, tk, tv, st);
+    case 128: return run_rows<Tc, 128>(a, p, tk, tv, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool splitk_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys) {
+  if (D != 32 && D != 64 && D != 128) return false;
+  *rows_per_tile = rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
+  *tile_keys = kTileBytes / (D * itemsize(dt));
+  return true;
+}
+
+size_t splitk_workspace_floats(const SplitPlan& p, int D) {
+  return static_cast<size_t>(p.n_items) * p.rows_per_tile * (D + 2);
+}
+
+cudaError_t launch_splitk(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
+                          const CUtensorMap* tv, cudaStream_t st) {
+  switch (a.cache_dtype) {
+    case KVC_F32: return run_d<float>(a, p, tk, tv, st);
+    case KVC_F16: return run_d<__half>(a, p, tk, tv, st);
+    case KVC_BF16: return run_d<__nv_bfloat16>(a, p, tk, tv, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvc

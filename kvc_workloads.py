@@ -1,0 +1,150 @@
+"""Synthetic workloads: their shapes, host redraws of their inputs, and GPU-resident instances.
+
+Used by the GPU tests and by `bench.py`. Inputs are drawn on the device by the library's Philox
+fill (`kvc_synth_fill_normal_f32`); `WorkloadSpec.host_*` redraw any slice of the same inputs on the
+host with `kvc_synth`, so expected values never come from the device.
+
+Layout of the draws (element index within each stream, row-major):
+* prefill keys/values of layer l: [B, H_kv, S0, d_h] from streams (K_PREFILL | V_PREFILL, l), with
+  S0 = max_b s_b; after committing S0 rows the cache is truncated to each s_b;
+* step n of layer l: k_new/v_new [B, H_kv, T, d_h] from (K_STEP | V_STEP, l, n + 1), queries
+  [B, H_q, T, d_h] from (Q, l, n + 1), all float32.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+import kvc_synth
+from kvc_synth import STREAM_K_PREFILL, STREAM_K_STEP, STREAM_Q, STREAM_V_PREFILL, STREAM_V_STEP, stream_id
+
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+ITEMSIZE = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+@dataclass
+class WorkloadSpec:
+    name: str
+    L: int
+    B: int
+    H_q: int
+    H_kv: int
+    d_h: int
+    max_len: int
+    dtype: str
+    lengths: np.ndarray
+    T: int = 1
+    seed: int = 0
+
+    @property
+    def S0(self) -> int:
+        return int(self.lengths.max())
+
+    @property
+    def G(self) -> int:
+        return self.H_q // self.H_kv
+
+    # -- host redraws ---------------------------------------------------------------------------
+    def host_prefill_rows(self, layer, b, kvh, n):
+        """Float32 draws of prefill rows [0, n) of (layer, b, kvh): ([n, d], [n, d])."""
+        base = ((b * self.H_kv + kvh) * self.S0) * self.d_h
+        idx = base + np.arange(n * self.d_h, dtype=np.int64)
+        k = kvc_synth.normal_f32_at(idx, self.seed, stream_id(STREAM_K_PREFILL, layer)).reshape(n, self.d_h)
+        v = kvc_synth.normal_f32_at(idx, self.seed, stream_id(STREAM_V_PREFILL, layer)).reshape(n, self.d_h)
+        return k, v
+
+    def host_step_rows(self, layer, step, b, kvh):
+        """Draws of step `step`'s T new rows of (layer, b, kvh): ([T, d], [T, d])."""
+        base = ((b * self.H_kv + kvh) * self.T) * self.d_h
+        idx = base + np.arange(self.T * self.d_h, dtype=np.int64)
+        k = kvc_synth.normal_f32_at(idx, self.seed, stream_id(STREAM_K_STEP, layer, step + 1))
+        v = kvc_synth.normal_f32_at(idx, self.seed, stream_id(STREAM_V_STEP, layer, step + 1))
+        return k.reshape(self.T, self.d_h), v.reshape(self.T, self.d_h)
+
+    def host_queries(self, layer, step, b, heads):
+        """Draws of the queries [len(heads), T, d] of sequence b at step `step`."""
+        rows = []
+        for h in heads:
+            base = ((b * self.H_q + h) * self.T) * self.d_h
+            idx = base + np.arange(self.T * self.d_h, dtype=np.int64)
+            rows.append(kvc_synth.normal_f32_at(idx, self.seed, stream_id(STREAM_Q, layer, step + 1)))
+        return np.stack(rows).reshape(len(heads), self.T, self.d_h)
+
+    # -- accounting -----------------------------------------------------------------------------
+    def attn_bytes(self, seqs=None) -> int:
+        """Algorithmic HBM bytes of one attention call over sequences `seqs` (default all): each
+        stored K and V row read once per K/V head, the float32 queries read, float32 outputs written."""
+        lens = self.lengths if seqs is None else self.lengths[list(seqs)]
+        n = len(lens)
+        kv = 2 * self.H_kv * self.d_h * ITEMSIZE[self.dtype] * int((lens + self.T).sum())
+        return kv + 2 * n * self.H_q * self.T * self.d_h * 4
+
+    def append_bytes(self) -> int:
+        """Float32 chunk read plus rounded rows written, for K and V, one layer."""
+        n = self.B * self.H_kv * self.T * self.d_h
+        return 2 * n * (4 + ITEMSIZE[self.dtype])
+
+    def step_bytes(self) -> int:
+        return self.L * (self.attn_bytes() + self.append_bytes())
+
+    def attn_flops(self) -> int:
+        """Multiply-adds of QK^T and PV counted as 2 flops each, unmasked pairs only, one layer."""
+        pairs = 0
+        for s in self.lengths:
+            pairs += self.T * int(s) + self.T * (self.T + 1) // 2
+        return 4 * self.d_h * self.H_q * pairs
+
+
+def spec(name: str, seed: int = 0) -> WorkloadSpec:
+    w = kvc_synth.WORKLOADS[name]
+    if "s_lo" in w:
+        lengths = kvc_synth.ragged_lengths(w["B"], w["s_lo"], w["s_hi"], seed)
+    else:
+        lengths = np.full(w["B"], w["s"], dtype=np.int64)
+    return WorkloadSpec(name, w["L"], w["B"], w["H_q"], w["H_kv"], w["d_h"], w["max_len"], w["dtype"],
+                        lengths, T=w["T"], seed=seed)
+
+
+class GpuWorkload:
+    """A workload's cache on the GPU (prefilled through the public API) and its step inputs."""
+
+    def __init__(self, sp: WorkloadSpec, device="cuda"):
+        import torch
+        from kv_cached_gqa_gb300 import _binding as kb
+        self.torch, self.kb, self.spec, self.device = torch, kb, sp, device
+        self.cache = kb.Cache(sp.L, sp.B, sp.H_kv, sp.d_h, sp.max_len, DTYPE_CODE[sp.dtype], device=device)
+
+    def __getattr__(self, name):                      # shape fields and host redraws of the spec
+        return getattr(self.__dict__["spec"], name)
+
+    def draw(self, shape, stream, std=1.0):
+        t = self.torch.empty(shape, dtype=self.torch.float32, device=self.device)
+        self.kb.synth_fill_normal(t, self.spec.seed, stream, std=std)
+        return t
+
+    def prefill(self):
+        """Append S0 rows to every layer, commit, then truncate each sequence to s_b."""
+        sp, kb = self.spec, self.kb
+        shape = (sp.B, sp.H_kv, sp.S0, sp.d_h)
+        for layer in range(sp.L):
+            k = self.draw(shape, stream_id(STREAM_K_PREFILL, layer))
+            v = self.draw(shape, stream_id(STREAM_V_PREFILL, layer))
+            kb.kvc_append(self.cache, layer, k, v)
+            del k, v
+        kb.kvc_commit(self.cache)
+        kb.kvc_truncate_ragged(self.cache, [int(x) for x in sp.lengths])
+
+    def step_inputs(self, step):
+        """(q, k_new, v_new) float32 device tensors of every layer for step `step`."""
+        sp = self.spec
+        out = []
+        for layer in range(sp.L):
+            q = self.draw((sp.B, sp.H_q, sp.T, sp.d_h), stream_id(STREAM_Q, layer, step + 1))
+            k = self.draw((sp.B, sp.H_kv, sp.T, sp.d_h), stream_id(STREAM_K_STEP, layer, step + 1))
+            v = self.draw((sp.B, sp.H_kv, sp.T, sp.d_h), stream_id(STREAM_V_STEP, layer, step + 1))
+            out.append((q, k, v))
+        return out
+
+    def close(self):
+        self.cache.close()

@@ -1,0 +1,119 @@
+"""Helpers for the GPU parity tests: run the same operations on the library and on the oracle.
+
+Inputs are float32 draws of `kvc_synth` made on the host and copied to the device, so the oracle and
+the GPU see the same values; expected values come from `oracle/` only.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import kvc_synth
+from oracle.kvc_oracle import OracleKVCache, gqa_cached_attention
+
+DT = {"f32": 0, "f16": 1, "bf16": 2}
+FP32_ATOL = 1e-5        # float32 caches: absolute, every output element
+REL_16 = 2e-3           # 16-bit caches: max |o - r| / max |r| over each (b, query head)
+
+
+def check_outputs(got: np.ndarray, want: np.ndarray, dtype: str, what: str = ""):
+    """Compare [B, H_q, T, d_h] outputs with the tolerance the cache dtype allows."""
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    if dtype == "f32":
+        err = np.abs(got - want).max()
+        assert err <= FP32_ATOL, f"{what}: max abs error {err:.3e} > {FP32_ATOL}"
+        return err
+    num = np.abs(got - want).max(axis=(2, 3))
+    den = np.abs(want).max(axis=(2, 3))
+    rel = (num / np.maximum(den, 1e-30)).max()
+    assert rel <= REL_16, f"{what}: relative max-abs error {rel:.3e} > {REL_16}"
+    return rel
+
+
+class Mirror:
+    """A GPU cache and an oracle cache driven by the same calls."""
+
+    def __init__(self, L, B, H_kv, d_h, max_len, dtype, seed=0):
+        import torch
+        from kv_cached_gqa_gb300 import _binding as kb
+        self.torch, self.kb = torch, kb
+        self.L, self.B, self.H, self.d, self.max_len, self.dtype, self.seed = L, B, H_kv, d_h, max_len, dtype, seed
+        self.gpu = kb.Cache(L, B, H_kv, d_h, max_len, DT[dtype])
+        self.ref = OracleKVCache(L, B, H_kv, d_h, max_len, dtype)
+        self.n_draws = 0
+
+    def draw(self, shape):
+        self.n_draws += 1
+        return kvc_synth.normal_f32(shape, self.seed, 1000 + self.n_draws)
+
+    def dev(self, x, dtype=None):
+        t = self.torch.from_numpy(np.ascontiguousarray(x)).cuda()
+        return t if dtype is None else t.to(dtype)
+
+    def append(self, layer, T, in_dtype="f32"):
+        k = self.draw((self.B, self.H, T, self.d))
+        v = self.draw((self.B, self.H, T, self.d))
+        self.ref.append(layer, k, v)
+        if in_dtype == "f32":
+            kd, vd = self.dev(k), self.dev(v)
+        else:
+            # input already in the cache dtype: hand the oracle's own rounding of it to both sides
+            tdt = self.kb.torch_dtype(DT[in_dtype])
+            kd, vd = self.dev(k).to(tdt), self.dev(v).to(tdt)
+        self.kb.kvc_append(self.gpu, layer, kd, vd)
+
+    def attend(self, layer, H_q, T, q_in="f32", split_keys=0):
+        q = self.draw((self.B, H_q, T, self.d))
+        want = gqa_cached_attention(self.ref, layer, q)
+        qd = self.dev(q) if q_in == "f32" else self.dev(q).to(self.kb.torch_dtype(DT[q_in]))
+        if split_keys:
+            self.kb.kvc_set_split_keys(self.gpu, split_keys)
+        got = self.kb.gqa_cached_attn(self.gpu, qd, layer).cpu().numpy()
+        if split_keys:
+            self.kb.kvc_set_split_keys(self.gpu, 0)
+        return got, want
+
+    def commit(self):
+        self.ref.commit()
+        self.kb.kvc_commit(self.gpu)
+
+    def truncate(self, n):
+        self.ref.truncate(n)
+        if np.ndim(n):
+            self.kb.kvc_truncate_ragged(self.gpu, list(n))
+        else:
+            self.kb.kvc_truncate(self.gpu, int(n))
+
+    def forward(self, T, H_q, check=True, what=""):
+        """One forward over every layer: append, attend, then commit."""
+        errs = []
+        for layer in range(self.L):
+            self.append(layer, T)
+            got, want = self.attend(layer, H_q, T)
+            if check:
+                errs.append(check_outputs(got, want, self.dtype, f"{what} layer {layer}"))
+        self.commit()
+        return errs
+
+    def store_bits(self):
+        """GPU store as raw bits and the oracle store as raw bits (same dtype/shape)."""
+        torch = self.torch
+        view = torch.int32 if self.dtype == "f32" else torch.int16
+        gk = self.gpu.k.view(view).cpu().numpy()
+        gv = self.gpu.v.view(view).cpu().numpy()
+        rk = self.ref.k.view(np.int32 if self.dtype == "f32" else np.int16)
+        rv = self.ref.v.view(np.int32 if self.dtype == "f32" else np.int16)
+        return (gk, gv), (rk, rv)
+
+    def check_state(self):
+        (gk, gv), (rk, rv) = self.store_bits()
+        np.testing.assert_array_equal(gk, rk)
+        np.testing.assert_array_equal(gv, rv)
+        assert self.kb.kvc_seq_len(self.gpu, -1) == [int(x) for x in self.ref.committed()]
+        for layer in range(self.L):
+            assert self.kb.kvc_seq_len(self.gpu, layer) == [int(x) for x in self.ref.seq_len(layer)]
+        pos = self.kb.kvc_positions(self.gpu, 3).cpu().numpy()
+        np.testing.assert_array_equal(pos, self.ref.positions(3))
+
+    def close(self):
+        self.gpu.close()

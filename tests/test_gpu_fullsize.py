@@ -1,0 +1,75 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the benchmark times.
+
+One forward (every layer: append, attend; then commit) runs on the full workload. The oracle then
+recomputes sampled (layer, sequence, K/V head) groups one by one from host redraws of the same
+seeded inputs: their G query heads' outputs within tolerance, and the stored rows bit-exactly.
+"""
+import numpy as np
+import pytest
+
+import kvc_workloads
+from oracle.kvc_oracle import OracleKVCache, gqa_cached_attention
+from tests.gpu_parity import check_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_and_sample(wl, samples):
+    import torch
+    from kv_cached_gqa_gb300 import _binding as kb
+    wl.prefill()
+    inputs = wl.step_inputs(0)
+    outs = []
+    for layer, (q, k, v) in enumerate(inputs):
+        kb.kvc_append(wl.cache, layer, k, v)
+        outs.append(kb.gqa_cached_attn(wl.cache, q, layer))
+    kb.kvc_commit(wl.cache)
+    kb.kvc_status(wl.cache)
+    G = wl.H_q // wl.H_kv
+    view = torch.int32 if wl.dtype == "f32" else torch.int16
+    for layer, b, kvh in samples:
+        s_b = int(wl.lengths[b])
+        ref = OracleKVCache(1, 1, 1, wl.d_h, s_b + wl.T, wl.dtype)
+        if s_b:
+            kp, vp = wl.host_prefill_rows(layer, b, kvh, s_b)
+            ref.append(0, kp[None, None], vp[None, None])
+            ref.commit()
+        kn, vn = wl.host_step_rows(layer, 0, b, kvh)
+        ref.append(0, kn[None, None], vn[None, None])
+        heads = list(range(kvh * G, (kvh + 1) * G))
+        qh = wl.host_queries(layer, 0, b, heads)
+        want = gqa_cached_attention(ref, 0, qh[None])
+        got = outs[layer][b, kvh * G:(kvh + 1) * G].cpu().numpy()[None]
+        check_outputs(got, want, wl.dtype, f"layer {layer} b {b} kvh {kvh}")
+        stored = wl.cache.k[layer, b, kvh, :s_b + wl.T].view(view).cpu().numpy()
+        np.testing.assert_array_equal(stored, ref.k[0, 0, 0].view(stored.dtype))
+        stored = wl.cache.v[layer, b, kvh, :s_b + wl.T].view(view).cpu().numpy()
+        np.testing.assert_array_equal(stored, ref.v[0, 0, 0].view(stored.dtype))
+    assert kb.kvc_seq_len(wl.cache) == [int(x) + wl.T for x in wl.lengths]
+    wl.close()
+
+
+def test_llama3_8b_decode_bf16_ragged_full_size():
+    """Llama-3-8B-shaped decode, bf16 cache: 32 layers, H_q=32, H_kv=8, d_h=128, B=64,
+    ragged s_b ~ U[512, 4096], T=1."""
+    wl = kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-decode-bf16"))
+    lo, hi = int(np.argmin(wl.lengths)), int(np.argmax(wl.lengths))
+    _run_and_sample(wl, [(0, lo, 0), (31, hi, 7), (13, 17, 3), (22, 40, 5)])
+
+
+def test_smollm2_decode_fp16_full_size():
+    """SmolLM2-135M-shaped attention, fp16 cache: 30 layers, H_q=9, H_kv=3, d_h=64, B=8, s=2048, T=1."""
+    _run_and_sample(kvc_workloads.GpuWorkload(kvc_workloads.spec("smollm2-135m-decode-fp16")),
+                    [(0, 0, 0), (29, 7, 2), (11, 3, 1)])
+
+
+def test_llama3_8b_verify_chunk_fp16_full_size():
+    """Speculative verify chunk, fp16: H_q=32, H_kv=8, d_h=128, B=16, s=2048, T=8."""
+    _run_and_sample(kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-verify-fp16")),
+                    [(0, 0, 0), (31, 15, 7), (7, 9, 2)])
+
+
+def test_llama3_8b_prefill_chunk_fp16_full_size():
+    """Prefill chunk, fp16: H_q=32, H_kv=8, d_h=128, B=16, T=512 at s=1024."""
+    _run_and_sample(kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-prefill-fp16")),
+                    [(0, 0, 0), (31, 15, 7), (16, 4, 3)])
