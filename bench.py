@@ -41,6 +41,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--split-keys", type=int, default=0)
+    p.add_argument("--layers", type=int, default=0,
+                   help="profiling only: fewer layers of the same per-layer shape (not a bench line)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=12.0)
@@ -267,6 +269,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     kb.load()
     sp = kvc_workloads.spec(args.workload)
+    if args.layers:
+        sp.L = args.layers
     wl = kvc_workloads.GpuWorkload(sp, device=f"cuda:{local}")
     if args.split_keys:
         kb.kvc_set_split_keys(wl.cache, args.split_keys)
@@ -375,7 +379,7 @@ def run_ours(args):
         "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": sp.dtype,
         "data": "synthetic (seeded Philox draws; approximately N(0,1))",
-        "config": workload_config(sp),
+        "config": workload_config(sp, None if not args.layers else "PROFILING CASE: fewer layers, not a bench line"),
         "steps_per_s": round(world * 1e3 / ms, 3),
         "pct_of_peak": {"measured_hbm": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / 8000.0, 2)},
