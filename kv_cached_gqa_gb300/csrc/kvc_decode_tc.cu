@@ -1,0 +1,408 @@
+// Grouped-query attention over the KV cache on the 5th-generation tensor cores (tcgen05 + TMEM),
+// for 16-bit caches with d_h = 128 and up to 32 query rows per K/V head (decode T = 1 and short
+// verify chunks).
+//
+// What it computes ("KV cache, incremental decode, ...", §2.3; "Generation and the KV Cache",
+// fence 3; "Heads, GQA and K/V cache", "Four queries, two sets of K/V"): for sequence b and K/V
+// head g, each query row (t, h) of the group h = g*G .. g*G+G-1 attends over stored keys
+// j <= s_b + t: softmax_j(q . k_j / sqrt(d_h)) weighted sum of v_j.
+//
+// How: the group's query rows are the N dimension of the MMAs (N = 16 or 32, padded with zero
+// rows) and the keys are the M dimension (128 per tile), so one K/V tile read from HBM serves every
+// query head of the group and nothing is repeated per head.
+//   S^T [128 keys x N] = K_tile . Q^T       A = K tile (K-major, TMA 128-byte swizzle), B = Q^T
+//   O^T [128 d   x N] += V_tile^T . P^T     A = V tile read MN-major, B = P^T (K-major)
+// One CTA owns one (sequence, row tile, K/V head, key split). Roles:
+//   warp 0     TMA producer: the split's K tiles, then its V tiles, through a 2-stage ring;
+//   warp 1     owns TMEM (256 columns) and issues every MMA from one thread;
+//   warps 2-5  one thread per key (= TMEM lane): the scores of every K tile of the split stay in
+//              TMEM, so the softmax over the split is exact (max, then exp2 and sum) with no
+//              running rescale; P is written to shared memory as a hi + lo pair of 16-bit values
+//              (P ~ hi + lo to ~2^-16 relative), so the PV product keeps fp32-level accuracy;
+//              then the epilogue: one thread per d reads O^T from TMEM.
+// A unit with several splits writes (m, l, o) partials; the CTA that finishes its last split
+// merges them (log-sum-exp) while they are in L2. Every wait is bounded (~1 s): a wait that gives
+// up sets the device status word and the CTA skips the rest of its work, frees its TMEM and exits.
+#include "kvc_device.cuh"
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+using namespace dev;
+
+constexpr int kTK = 128;                    // keys per tile = MMA M
+constexpr int kDh = 128;                    // head width = MMA K for QK, M for PV
+constexpr int kBoxBytes = kTK * 128;        // one 64-element (128-byte) swizzled column box
+constexpr int kTileBytes = 2 * kBoxBytes;   // 32 KB: a tile's K (or V) rows
+constexpr int kStages = 2;
+constexpr int kTmemCols = 256;
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+
+template <int NR>
+struct Layout {
+  static constexpr int kQBytes = NR * 256;                      // Q^T: two atoms of NR rows x 128 B
+  static constexpr int kPBytes = NR * 256;                      // one P^T operand (hi or lo)
+  static constexpr int kStageOff = 0;
+  static constexpr int kQOff = kStages * kTileBytes;
+  static constexpr int kPOff = kQOff + kQBytes;                 // 2 buffers x (hi, lo)
+  static constexpr int kCtlOff = kPOff + 4 * kPBytes;
+  static constexpr int kSTiles = (kTmemCols - NR) / NR;         // S^T tiles that fit beside O^T
+};
+
+template <int NR>
+struct __align__(8) Ctl {
+  unsigned long long full[kStages], empty[kStages];
+  unsigned long long p_full[2], p_empty[2];
+  unsigned long long s_full, o_full, done;
+  uint32_t tmem;
+  int abort, last;
+  float red[4][NR];
+  float m[NR], l[NR];
+};
+
+// Dynamic shared memory per CTA. At least 80 KB, so that no more than two CTAs are ever resident on
+// an SM: each holds 256 of the SM's 512 TMEM columns, and a third could wait forever on tcgen05.alloc.
+template <int NR>
+constexpr size_t smem_bytes() {
+  return (1024 + Layout<NR>::kCtlOff + sizeof(Ctl<NR>)) > 80 * 1024 ? (1024 + Layout<NR>::kCtlOff + sizeof(Ctl<NR>))
+                                                                     : 80 * 1024;
+}
+static_assert(3 * 80 * 1024 > 228 * 1024, "three CTAs must not fit on one SM");
+
+// Byte offset of element (row, col) in an [rows][128] 16-bit matrix stored as two 128-byte-swizzled
+// atoms of 64 columns (the layout TMA writes and the tensor cores read, K-major).
+__device__ __forceinline__ uint32_t sw128(int rows, int row, int col) {
+  const int atom = col >> 6, c = col & 63;
+  return atom * (rows * 128) + row * 128 + ((((c >> 3) ^ (row & 7))) << 4) + (c & 7) * 2;
+}
+
+// Bounded wait that ignores the abort flag (used only to drain in-flight copies and MMAs).
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = now_ns();
+  while (!mbar_try(bar, parity)) {
+    if (now_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+template <typename Tc, int NR>
+__global__ void __launch_bounds__(kThreads, 2)
+decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
+                 const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+  using Lo = Layout<NR>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctl<NR>* ctl = reinterpret_cast<Ctl<NR>*>(sm + Lo::kCtlOff);
+  const uint32_t s_stage = smem_u32(sm + Lo::kStageOff);
+  const uint32_t s_q = smem_u32(sm + Lo::kQOff);
+  unsigned char* p_base = sm + Lo::kPOff;
+  const uint32_t s_p = smem_u32(p_base);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr uint32_t kFmt = std::is_same<Tc, __nv_bfloat16>::value ? 1u : 0u;
+
+  // ---- which (unit, K/V head, split) this CTA owns --------------------------------------------
+  const int item = blockIdx.x;
+  int lo = 0, hi = plan.n_units - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (plan.prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  const int unit = lo;
+  const int nsplit = (plan.prefix[unit + 1] - plan.prefix[unit]) / a.H_kv;
+  const int rem = item - plan.prefix[unit];
+  const int kvh = rem / nsplit, split = rem % nsplit;
+  const int b = plan.unit_b[unit];
+  const int rt = unit % plan.n_rowtiles;
+  const int row0 = rt * NR;
+  const int nrows = min(NR, a.T * a.G - row0);
+  const int s_b = a.lens[b] + a.delta - a.T;
+  const int n_eff = s_b + (row0 + nrows - 1) / a.G + 1;
+  const int k_begin = split * plan.split_keys;
+  const int k_end = min(k_begin + plan.split_keys, n_eff);
+  const int nkt = (k_end - k_begin + kTK - 1) / kTK;
+  const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
+
+  // ---- set-up: TMEM, barriers, Q^T, zeroed P^T ------------------------------------------------
+  if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&ctl->tmem));
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&ctl->p_full[s]), kSoftmaxThreads / 32);
+      mbar_init(smem_u32(&ctl->p_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&ctl->s_full), 1);
+    mbar_init(smem_u32(&ctl->o_full), 1);
+    mbar_init(smem_u32(&ctl->done), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  for (int i = tid; i < NR * kDh; i += kThreads) {
+    const int r = i / kDh, d = i % kDh;
+    float x = 0.f;
+    if (r < nrows) {
+      const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+      x = load_query<Tc>(a.q, a.q_dtype, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d);
+    }
+    *reinterpret_cast<Tc*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tc>(x);
+  }
+  for (int i = tid; i < 4 * Lo::kPBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(p_base)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+  const uint32_t tmem_o = tmem + (kTmemCols - NR);
+  volatile int* abort_flag = &ctl->abort;
+
+  if (warp == 0) {
+    // ---------------------------------- TMA producer --------------------------------------------
+    if (lane == 0) {
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      int issued = 0;
+      for (int i = 0; i < 2 * nkt; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(smem_u32(&ctl->empty[st]), ((i / kStages) & 1) ^ 1, abort_flag)) break;
+        const bool isv = i >= nkt;
+        const int y = k_begin + (isv ? i - nkt : i) * kTK;
+        const uint32_t full = smem_u32(&ctl->full[st]);
+        mbar_expect_tx(full, kTileBytes);
+        const uint32_t dst = s_stage + st * kTileBytes;
+        tma_load_3d(dst, isv ? &tv : &tk, 0, y, plane, full);
+        tma_load_3d(dst + kBoxBytes, isv ? &tv : &tk, 64, y, plane, full);
+        issued = i + 1;
+      }
+      // drain: the last copy issued into each stage has landed before the CTA can exit
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        mbar_drain(smem_u32(&ctl->full[i % kStages]), (i / kStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------- MMA issuer ----------------------------------------------
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc(kTK, NR, kFmt, 0, 0);
+      const uint32_t idesc_o = umma_idesc(kDh, NR, kFmt, 1, 0);
+      bool ok = true;
+      for (int i = 0; i < nkt && ok; ++i) {                 // S^T_i = K_i . Q^T
+        const int st = i % kStages;
+        ok = mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kt = s_stage + st * kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kDh / 16; ++ks)
+          umma_f16(tmem + i * NR,
+                   umma_desc(kt + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024, kSwizzle128),
+                   umma_desc(s_q + (ks >> 2) * (NR * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128),
+                   idesc_s, ks > 0);
+        umma_commit(smem_u32(&ctl->empty[st]));
+      }
+      if (ok) umma_commit(smem_u32(&ctl->s_full));
+      for (int i = 0; i < nkt && ok; ++i) {                 // O^T += V_i^T . P_i^T (hi, then lo)
+        const int ti = nkt + i, st = ti % kStages, pb = i & 1;
+        ok = mbar_wait(smem_u32(&ctl->full[st]), (ti / kStages) & 1, abort_flag) &&
+             mbar_wait(smem_u32(&ctl->p_full[pb]), (i >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vt = s_stage + st * kTileBytes;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t pt = s_p + (pb * 2 + part) * Lo::kPBytes;
+#pragma unroll
+          for (int ks = 0; ks < kTK / 16; ++ks)
+            umma_f16(tmem_o,
+                     umma_desc(vt + ks * 2048, kBoxBytes, 1024, kSwizzle128),
+                     umma_desc(pt + (ks >> 2) * (NR * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128),
+                     idesc_o, (i | part | ks) != 0);
+        }
+        umma_commit(smem_u32(&ctl->empty[st]));
+        umma_commit(smem_u32(&ctl->p_empty[pb]));
+      }
+      if (ok) umma_commit(smem_u32(&ctl->o_full));
+      umma_commit(smem_u32(&ctl->done));
+      mbar_drain(smem_u32(&ctl->done), 0);                  // every MMA done before TMEM is freed
+    }
+  } else {
+    // ---------------------------------- softmax and epilogue ------------------------------------
+    const int quad = warp & 3;                              // this warp's TMEM lane quadrant
+    const int kslot = quad * 32 + lane;                     // key within a tile; d in the epilogue
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const int w4 = warp - 2;
+    const float scale = kLog2e * rsqrtf(static_cast<float>(kDh));
+    int trow[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) trow[r] = (r < nrows) ? s_b + (row0 + r) / a.G : -1;   // last visible key
+
+    bool ok = mbar_wait(smem_u32(&ctl->s_full), 0, abort_flag);
+    tc_fence_after();
+    float m_run[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) m_run[r] = -INFINITY;
+    for (int i = 0; i < nkt && ok; ++i) {
+      float v[NR];
+#pragma unroll
+      for (int c = 0; c < NR; c += 16) tmem_ld16(tmem + lane_base + i * NR + c, v + c);
+      const int kabs = k_begin + i * kTK + kslot;
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        if (kabs < k_end && kabs <= trow[r]) m_run[r] = fmaxf(m_run[r], v[r] * scale);
+    }
+    // row maxima over the split's keys: warp shuffles, then across the four warps
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m_run[r] = fmaxf(m_run[r], __shfl_xor_sync(0xffffffffu, m_run[r], o));
+      if (lane == 0) ctl->red[w4][r] = m_run[r];
+    }
+    named_sync(1, kSoftmaxThreads);
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      m_run[r] = fmaxf(fmaxf(ctl->red[0][r], ctl->red[1][r]), fmaxf(ctl->red[2][r], ctl->red[3][r]));
+    named_sync(1, kSoftmaxThreads);
+
+    float l_run[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) l_run[r] = 0.f;
+    for (int i = 0; i < nkt && ok; ++i) {
+      const int pb = i & 1;
+      ok = mbar_wait(smem_u32(&ctl->p_empty[pb]), ((i >> 1) & 1) ^ 1, abort_flag);
+      if (!ok) break;
+      float v[NR];
+#pragma unroll
+      for (int c = 0; c < NR; c += 16) tmem_ld16(tmem + lane_base + i * NR + c, v + c);
+      const int kabs = k_begin + i * kTK + kslot;
+      unsigned char* ph = p_base + (pb * 2) * Lo::kPBytes;
+      unsigned char* pl = ph + Lo::kPBytes;
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        if (r < nrows) {
+          const float p = (kabs < k_end && kabs <= trow[r]) ? exp2f(v[r] * scale - m_run[r]) : 0.f;
+          l_run[r] += p;
+          const Tc h16 = from_f32<Tc>(p);
+          const Tc l16 = from_f32<Tc>(p - to_f32<Tc>(h16));
+          const uint32_t off = sw128(NR, r, kslot);
+          *reinterpret_cast<Tc*>(ph + off) = h16;
+          *reinterpret_cast<Tc*>(pl + off) = l16;
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[pb]));
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], o);
+      if (lane == 0) ctl->red[w4][r] = l_run[r];
+    }
+    named_sync(1, kSoftmaxThreads);
+    if (tid == 64) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        ctl->m[r] = m_run[r];
+        ctl->l[r] = ctl->red[0][r] + ctl->red[1][r] + ctl->red[2][r] + ctl->red[3][r];
+      }
+    }
+    named_sync(1, kSoftmaxThreads);
+
+    // ---- epilogue: thread = d; O^T row d from TMEM -----------------------------------------------
+    ok = ok && mbar_wait(smem_u32(&ctl->o_full), 0, abort_flag);
+    tc_fence_after();
+    float o[NR];
+#pragma unroll
+    for (int c = 0; c < NR; c += 16) tmem_ld16(tmem_o + lane_base + c, o + c);
+    const bool aborted = *abort_flag != 0;
+    const int d = kslot;
+    const long long item_row0 = static_cast<long long>(item) * NR;
+    if (!aborted) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        if (r < nrows) {
+          const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+          if (nsplit == 1) {
+            a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = o[r] / ctl->l[r];
+          } else {
+            a.part_o[(item_row0 + r) * kDh + d] = o[r];
+            if (d == 0) {
+              a.part_ml[(item_row0 + r) * 2] = ctl->m[r];
+              a.part_ml[(item_row0 + r) * 2 + 1] = ctl->l[r];
+            }
+          }
+        }
+      }
+    } else if (tid == 64) {
+      atomicExch(a.status, kStatusTimeout);
+    }
+    if (nsplit > 1) {
+      // ---- the CTA that finishes a unit's last split merges its partials -----------------------
+      __threadfence();
+      named_sync(1, kSoftmaxThreads);
+      int* counter = a.counters + unit * a.H_kv + kvh;
+      if (tid == 64) ctl->last = (atomicAdd(counter, 1) == nsplit - 1);
+      named_sync(1, kSoftmaxThreads);
+      if (ctl->last) {
+        __threadfence();
+        const long long first_row = static_cast<long long>(plan.prefix[unit] + kvh * nsplit) * NR;
+        for (int r = 0; r < nrows; ++r) {
+          float m = -INFINITY, l = 0.f, acc = 0.f;
+          for (int s = 0; s < nsplit; ++s) {
+            const long long row = first_row + static_cast<long long>(s) * NR + r;
+            const float ms = __ldcg(a.part_ml + row * 2), ls = __ldcg(a.part_ml + row * 2 + 1);
+            if (!(ls > 0.f)) continue;
+            const float mn = fmaxf(m, ms);
+            const float c_old = exp2f(m - mn), c_new = exp2f(ms - mn);
+            l = l * c_old + ls * c_new;
+            acc = acc * c_old + __ldcg(a.part_o + row * kDh + d) * c_new;
+            m = mn;
+          }
+          const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+          if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l;
+        }
+        if (tid == 64) *counter = 0;
+      }
+    }
+  }
+
+  // ---- teardown: every TMEM access is complete before the allocating warp frees it -------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<kTmemCols>(tmem);
+  }
+}
+
+template <typename Tc, int NR>
+cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, const CUtensorMap* tv,
+                cudaStream_t st) {
+  auto kern = decode_tc_kernel<Tc, NR>;
+  const size_t smem = smem_bytes<NR>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<p.n_items, kThreads, smem, st>>>(a, p, *tk, *tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tc_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys, int* max_tiles) {
+  if ((dt != KVC_F16 && dt != KVC_BF16) || D != kDh) return false;
+  *rows_per_tile = rows <= 16 ? 16 : 32;
+  *tile_keys = kTK;
+  *max_tiles = *rows_per_tile == 16 ? Layout<16>::kSTiles : Layout<32>::kSTiles;
+  return true;
+}
+
+cudaError_t launch_decode_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
+                             const CUtensorMap* tv, cudaStream_t st) {
+  if (a.cache_dtype == KVC_BF16)
+    return p.rows_per_tile == 16 ? run<__nv_bfloat16, 16>(a, p, tk, tv, st) : run<__nv_bfloat16, 32>(a, p, tk, tv, st);
+  return p.rows_per_tile == 16 ? run<__half, 16>(a, p, tk, tv, st) : run<__half, 32>(a, p, tk, tv, st);
+}
+
+}  // namespace kvc

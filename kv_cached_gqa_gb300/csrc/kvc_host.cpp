@@ -70,8 +70,11 @@ int init_device_state(kvc_handle h, cudaStream_t st) {
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(lengths)");
   e = cudaMalloc(&h->d_status, sizeof(int));
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(status)");
+  e = cudaMalloc(&h->d_counters, sizeof(int) * kvc::kMaxUnits * h->H);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(counters)");
   e = cudaMemsetAsync(h->d_lens, 0, sizeof(int32_t) * h->B, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->d_status, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->d_counters, 0, sizeof(int) * kvc::kMaxUnits * h->H, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync");
   int rows = 0;
   kvc::splitk_shape(h->dtype, h->D, 1, &rows, &h->split_tile_keys);
@@ -82,6 +85,13 @@ int init_device_state(kvc_handle h, cudaStream_t st) {
       !kvc::encode_store_map(&h->tmap_v_split, h->v, h->dtype, h->D, h->max_len, planes,
                              h->split_tile_keys, &err))
     return fail(h, KVC_E_CUDA, "%s", err.c_str());
+  int tc_rows = 0, tc_tile = 0, tc_tiles = 0;
+  if (kvc::decode_tc_shape(h->dtype, h->D, 1, &tc_rows, &tc_tile, &tc_tiles)) {
+    if (!kvc::encode_store_map(&h->tmap_k_tc, h->k, h->dtype, h->D, h->max_len, planes, tc_tile, &err) ||
+        !kvc::encode_store_map(&h->tmap_v_tc, h->v, h->dtype, h->D, h->max_len, planes, tc_tile, &err))
+      return fail(h, KVC_E_CUDA, "%s", err.c_str());
+    h->has_tc = true;
+  }
   return KVC_OK;
 }
 
@@ -95,6 +105,7 @@ void release(kvc_handle h) {
   cudaFree(h->d_lens);
   cudaFree(h->d_status);
   cudaFree(h->work);
+  cudaFree(h->d_counters);
   delete h;
 }
 
@@ -357,9 +368,15 @@ int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, i
   }
   const int G = H_q / h->H;
   const int R = T * G;
-  int rpt = 0, tile = 0;
-  if (!kvc::splitk_shape(h->dtype, h->D, R, &rpt, &tile))
-    return fail(h, KVC_E_UNSUPPORTED, "no split-K kernel for d_h=%d", h->D);
+  // kernel choice: tensor cores for 16-bit caches with d_h = 128 and at most 32 query rows per K/V
+  // head; CUDA cores otherwise
+  int rpt = 0, tile = 0, max_tiles = 0;
+  const bool use_tc = h->has_tc && R <= 32 && kvc::decode_tc_shape(h->dtype, h->D, R, &rpt, &tile, &max_tiles);
+  if (!use_tc) {
+    if (!kvc::splitk_shape(h->dtype, h->D, R, &rpt, &tile))
+      return fail(h, KVC_E_UNSUPPORTED, "no attention kernel for d_h=%d", h->D);
+    max_tiles = (8192 / (2 * rpt)) / tile;                  // the kernel's weight buffer
+  }
   const int n_rt = (R + rpt - 1) / rpt;
   if (static_cast<long long>(h->B) * n_rt > kvc::kMaxUnits)
     return fail(h, KVC_E_UNSUPPORTED, "B * row tiles = %lld exceeds %d", static_cast<long long>(h->B) * n_rt,
@@ -375,7 +392,7 @@ int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, i
       const int t_max = std::min(T - 1, ((rt + 1) * rpt - 1) / G);
       total_keys += static_cast<long long>(h->lens[b]) + t_max + 1;
     }
-  const int cmax = (4096 / rpt) / tile * tile;              // the kernel's score buffer
+  const int cmax = max_tiles * tile;
   int split = h->split_keys_override;
   if (split <= 0) {
     // aim for ~8 CTAs per SM in total (two resident per SM, about four waves)
@@ -415,12 +432,14 @@ int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, i
   a.q = q; a.q_dtype = q_dtype; a.out = out;
   a.part_o = h->work;
   a.part_ml = h->work ? h->work + static_cast<size_t>(plan.n_items) * rpt * h->D : nullptr;
+  a.counters = h->d_counters;
   a.lens = h->d_lens; a.status = h->d_status;
   a.layer = layer; a.B = h->B; a.H_kv = h->H; a.H_q = H_q; a.G = G; a.T = T; a.D = h->D;
   a.max_len = h->max_len; a.delta = T; a.cache_dtype = h->dtype;
-  cudaError_t e = kvc::launch_splitk(a, plan, &h->tmap_k_split, &h->tmap_v_split, st);
+  cudaError_t e = use_tc ? kvc::launch_decode_tc(a, plan, &h->tmap_k_tc, &h->tmap_v_tc, st)
+                         : kvc::launch_splitk(a, plan, &h->tmap_k_split, &h->tmap_v_split, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
-  h->launches += (plan.n_items > plan.n_units * h->H) ? 2 : 1;
+  h->launches += 1;
   return KVC_OK;
 }
 

@@ -64,6 +64,7 @@ struct AttnArgs {
   float* out;               // [B, H_q, T, D]
   float* part_o;            // [n_items, rows_per_tile, D] workspace
   float* part_ml;           // [n_items, rows_per_tile, 2] workspace
+  int* counters;            // [kMaxUnits, H_kv] finished-split counters, zero between launches
   const int32_t* lens;      // device committed lengths
   int* status;              // device status word
   int layer, B, H_kv, H_q, G, T, D, max_len;
@@ -76,6 +77,12 @@ size_t splitk_workspace_floats(const SplitPlan& p, int D);
 bool splitk_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys);
 cudaError_t launch_splitk(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
                           const CUtensorMap* tv, cudaStream_t st);
+
+// Tensor-core decode/verify kernel (16-bit caches, d_h = 128, up to 32 query rows per K/V head per
+// row tile). Returns false when the shape has no tensor-core kernel.
+bool decode_tc_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys, int* max_tiles);
+cudaError_t launch_decode_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
+                             const CUtensorMap* tv, cudaStream_t st);
 
 // Tensor map over a store viewed as [L*B*H, max_len, D] with boxes of (swizzle span, box_rows, 1).
 bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max_len,
@@ -94,8 +101,11 @@ struct kvc_cache {
   std::vector<int32_t> fill;      // host mirror [L * B]
   std::vector<int32_t> lens;      // host mirror [B]
   CUtensorMap tmap_k_split{}, tmap_v_split{};
+  CUtensorMap tmap_k_tc{}, tmap_v_tc{};          // 128-key boxes for the tensor-core kernel
+  bool has_tc = false;
   int split_tile_keys = 0;
   float* work = nullptr;          // split-K workspace
+  int* d_counters = nullptr;      // split-K merge counters [kMaxUnits * H]
   size_t work_floats = 0;
   int split_keys_override = 0;
   uint64_t launches = 0;          // kernels enqueued by this handle

@@ -10,13 +10,17 @@
 // One CTA handles one (row tile, K/V head, key split). A producer warp streams the split's K tiles
 // and then its V tiles, HBM -> shared memory, with TMA (128-byte swizzle, so lane-per-key reads
 // are bank-conflict free) through a 4-stage mbarrier ring; four consumer warps compute.
-//   QK:  one lane per key (or 2-4 lanes per key for wide rows), q broadcast from shared memory,
-//        scores for the whole split kept in shared memory;
-//   softmax: exact within the split (max, exp2, sum) — no running rescale;
-//   PV:  one lane per d_h slice, weights broadcast from shared memory, warps split the keys and
-//        are reduced through shared memory at the end.
+//   QK:  a key's row is split over 1-8 lanes (4 x 16 bytes each), every lane scores 2 keys, so a
+//        query chunk broadcast from shared memory serves both; paired fp32 FMAs (fma.rn.f32x2);
+//        scores for the whole split are kept in shared memory;
+//   softmax: exact within the split (max, exp2, sum), no running rescale; each weight is stored
+//        twice so PV reads ready-made pairs;
+//   PV:  one lane per d_h slice, paired FMAs over d, warps split the keys and are reduced through
+//        shared memory at the end.
 // A split writes (m, l, o) partials unless it is its unit's only split, in which case it writes
-// the normalised output. `combine_kernel` merges partials with the log-sum-exp rule.
+// the normalised output. The CTA that finishes a unit's last split merges the partials with the
+// log-sum-exp rule (a per-unit counter in global memory tells it that it is last), so there is
+// no second launch.
 //
 // Every wait is bounded (about one second); a wait that gives up sets the device status word and
 // the CTA skips its remaining work instead of hanging.
@@ -25,19 +29,20 @@
 
 #include <type_traits>
 
+#include "kvc_device.cuh"
 #include "kvc_internal.h"
 
 namespace kvc {
 namespace {
+
+using namespace dev;
 
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kStages = 4;
 constexpr int kTileBytes = 16384;
-constexpr int kScoreFloats = 4096;             // per-split score buffer (rows x keys)
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kScoreFloats = 8192;             // per-split weights: keys x rows x 2 (duplicated)
 
 template <typename Tc, int D, int RMAX>
 struct Cfg {
@@ -50,15 +55,18 @@ struct Cfg {
   static constexpr int TILE = kTileBytes / ROWB;        // keys per tile
   static constexpr int EPC = 16 / E;                    // elements per 16-byte chunk
   static constexpr int CPR = ROWB / 16;                 // chunks per key row
-  static constexpr int DSPLIT = TILE >= 128 ? 1 : 128 / TILE;   // lanes sharing one key in QK
-  static constexpr int KPT = TILE >= 128 ? TILE / 128 : 1;      // keys per lane in QK
-  static constexpr int LPK = 32 / DSPLIT;               // distinct keys per warp in QK
-  static constexpr int CPP = CPR / DSPLIT;              // chunks per lane in QK
-  static constexpr int DPART = D / DSPLIT;              // elements per lane part in QK
+  // QK: a key's row is split over DSPLIT lanes, 4 chunks each; every lane handles KPT keys, so a
+  // query chunk read from shared memory serves KPT keys
+  static constexpr int CPL = CPR >= 4 ? 4 : CPR;        // chunks per lane
+  static constexpr int DSPLIT = CPR / CPL;              // lanes per key
+  static constexpr int KPW = 32 / DSPLIT;               // keys per warp per pass
+  static constexpr int KPC = kConsumerWarps * KPW;      // keys per CTA pass
+  static constexpr int KPT = TILE / KPC;                // keys per lane per tile
+  static constexpr int DPART = D / DSPLIT;              // elements per lane part
   static constexpr int QSTRIDE = D + 4 * DSPLIT;        // padded q row (floats) in shared memory
   static constexpr int EPL = D / 32;                    // V elements per lane in PV
   static_assert(TILE <= 256 && TILE % kConsumerWarps == 0, "tile");
-  static_assert(CPR % DSPLIT == 0, "split");
+  static_assert(KPT >= 1 && KPT * KPC == TILE, "keys per lane");
   static_assert(RMAX % 4 == 0, "row blocks of 4");
 };
 
@@ -66,60 +74,11 @@ struct __align__(8) Smem {
   unsigned long long full[kStages];
   unsigned long long empty[kStages];
   int abort;
+  int last;
   float m[16];
   float l[16];
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long now_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
-}
-
-// Bounded wait on an mbarrier phase; false when it gave up (or another thread already did).
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  unsigned long long t0 = 0;
-  for (int it = 0;; ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 31) == 31) {
-      if (*abort_flag) return false;
-      unsigned long long t = now_ns();
-      if (t0 == 0) t0 = t;
-      else if (t - t0 > kWaitLimitNs) { *abort_flag = 1; return false; }
-    }
-  }
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];"
-      :: "r"(dst), "l"(reinterpret_cast<unsigned long long>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" :: "n"(kConsumers) : "memory");
 }
@@ -157,25 +116,6 @@ template <> __device__ __forceinline__ void unpack16<__half>(const uint4& r, flo
   }
 }
 
-template <typename Tc> __device__ __forceinline__ float to_f32(Tc x);
-template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
-template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
-template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-// A query element as the attention uses it: an F32 query meets a 16-bit cache rounded to it.
-template <typename Tc>
-__device__ __forceinline__ float load_query(const void* q, kvc_dtype qt, long long i) {
-  if (qt == KVC_F32) {
-    float x = static_cast<const float*>(q)[i];
-    if constexpr (sizeof(Tc) == 2) {
-      if constexpr (std::is_same<Tc, __half>::value) return __half2float(__float2half_rn(x));
-      else return __bfloat162float(__float2bfloat16_rn(x));
-    }
-    return x;
-  }
-  return to_f32<Tc>(static_cast<const Tc*>(q)[i]);
-}
-
 // V elements [lane*EPL, lane*EPL + EPL) of key row `key` in a V tile.
 template <typename Tc, class C>
 __device__ __forceinline__ void load_v(const unsigned char* tile, int key, int lane, float* v) {
@@ -210,17 +150,24 @@ __device__ __forceinline__ void load_v(const unsigned char* tile, int key, int l
   }
 }
 
+// Two fp32 multiply-adds in one instruction: (c0, c1) += (a0, a1) * (b0, b1).
+__device__ __forceinline__ void ffma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+  const float2 r = __ffma2_rn(make_float2(a0, a1), make_float2(b0, b1), make_float2(c0, c1));
+  c0 = r.x;
+  c1 = r.y;
+}
+
 template <typename Tc, int D, int RMAX>
 __global__ void __launch_bounds__(kThreads, 2)
 splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
               const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
   using C = Cfg<Tc, D, RMAX>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // layout: [stages x 16 KB tiles][scores][q rows][Smem]
+  // layout: [stages x 16 KB tiles][weights: keys x RMAX x 2][q rows][Smem]
   unsigned char* tiles = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* S = reinterpret_cast<float*>(tiles + kStages * kTileBytes);
-  float* qs = S + kScoreFloats;
+  float* SP = reinterpret_cast<float*>(tiles + kStages * kTileBytes);
+  float* qs = SP + kScoreFloats;
   Smem* sm = reinterpret_cast<Smem*>(qs + RMAX * C::QSTRIDE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -258,7 +205,7 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     sm->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // queries of the tile, prescaled by log2(e) / sqrt(d_h): S holds scores in base-2 units
+  // queries of the tile, prescaled by log2(e) / sqrt(d_h): scores are in base-2 units
   const float qscale = kLog2e * rsqrtf(static_cast<float>(D));
   for (int i = tid; i < RMAX * D; i += kThreads) {
     const int r = i / D, e = i % D;
@@ -297,50 +244,57 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   }
 
   // ---------------------------------- consumers: QK ------------------------------------------
-  const int part = lane / C::LPK;
-  const int key_in_warp = lane % C::LPK;
+  // lane = (part, key): `part` owns CPL chunks of the row; each lane scores KPT keys of the tile
+  const int part = lane / C::KPW;
+  const int key_in_warp = lane % C::KPW;
   for (int i = 0; i < nkt; ++i) {
     const int st = i % kStages;
     const bool ok = mbar_wait(smem_u32(&sm->full[st]), (i / kStages) & 1, abort_flag);
     if (ok) {
       const unsigned char* tile = tiles + st * kTileBytes;
 #pragma unroll
-      for (int kp = 0; kp < C::KPT; ++kp) {
-        const int key = kp * (kConsumerWarps * C::LPK) + warp * C::LPK + key_in_warp;
-        const int kabs = k_begin + i * C::TILE + key;
+      for (int rb = 0; rb < RMAX / 4; ++rb) {
+        float acc[C::KPT][4][2];
 #pragma unroll
-        for (int rb = 0; rb < RMAX / 4; ++rb) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kp = 0; kp < C::KPT; ++kp)
 #pragma unroll
-          for (int c = 0; c < C::CPP; ++c) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(tile + tile_off<C>(key, part * C::CPP + c));
-            float kf[C::EPC];
-            unpack16<Tc>(raw, kf);
+          for (int j = 0; j < 4; ++j) acc[kp][j][0] = acc[kp][j][1] = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float* qr = qs + (rb * 4 + j) * C::QSTRIDE + part * (C::DPART + 4) + c * C::EPC;
+        for (int c = 0; c < C::CPL; ++c) {
+          float kf[C::KPT][C::EPC];
 #pragma unroll
-              for (int e4 = 0; e4 < C::EPC; e4 += 4) {
-                const float4 qv = *reinterpret_cast<const float4*>(qr + e4);
-                acc[j] = fmaf(qv.x, kf[e4], acc[j]);
-                acc[j] = fmaf(qv.y, kf[e4 + 1], acc[j]);
-                acc[j] = fmaf(qv.z, kf[e4 + 2], acc[j]);
-                acc[j] = fmaf(qv.w, kf[e4 + 3], acc[j]);
-              }
-            }
+          for (int kp = 0; kp < C::KPT; ++kp) {
+            const int key = kp * C::KPC + warp * C::KPW + key_in_warp;
+            unpack16<Tc>(*reinterpret_cast<const uint4*>(tile + tile_off<C>(key, part * C::CPL + c)), kf[kp]);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
+            const float* qr = qs + (rb * 4 + j) * C::QSTRIDE + part * (C::DPART + 4) + c * C::EPC;
 #pragma unroll
-            for (int o = C::LPK; o < 32; o <<= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+            for (int e4 = 0; e4 < C::EPC; e4 += 4) {
+              const float4 qv = *reinterpret_cast<const float4*>(qr + e4);
+#pragma unroll
+              for (int kp = 0; kp < C::KPT; ++kp) {
+                ffma2(acc[kp][j][0], acc[kp][j][1], qv.x, qv.y, kf[kp][e4], kf[kp][e4 + 1]);
+                ffma2(acc[kp][j][0], acc[kp][j][1], qv.z, qv.w, kf[kp][e4 + 2], kf[kp][e4 + 3]);
+              }
+            }
           }
-          if (part == 0) {
+        }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+        for (int kp = 0; kp < C::KPT; ++kp) {
+          const int key = kp * C::KPC + warp * C::KPW + key_in_warp;
+          const int kabs = k_begin + i * C::TILE + key;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float sc = acc[kp][j][0] + acc[kp][j][1];
+#pragma unroll
+            for (int o = C::KPW; o < 32; o <<= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
+            if (part == 0) {
               const int r = rb * 4 + j;
               const int t = (row0 + r) / a.G;
               const bool vis = kabs < k_end && kabs <= s_b + t;
-              S[(i * C::TILE + key) * RMAX + r] = vis ? acc[j] : -INFINITY;
+              SP[((i * C::TILE + key) * RMAX + r) * 2] = vis ? sc : -INFINITY;
             }
           }
         }
@@ -352,16 +306,19 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   consumers_sync();
 
   // ---------------------------------- softmax within the split ---------------------------------
+  // exact over the split's keys; each weight is stored twice so PV reads ready-made pairs
   const int n_slots = nkt * C::TILE;
   for (int r = warp; r < RMAX; r += kConsumerWarps) {
     float m = -INFINITY;
-    for (int k = lane; k < n_slots; k += 32) m = fmaxf(m, S[k * RMAX + r]);
+    for (int k = lane; k < n_slots; k += 32) m = fmaxf(m, SP[(k * RMAX + r) * 2]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float l = 0.f;
     for (int k = lane; k < n_slots; k += 32) {
-      const float p = (m == -INFINITY) ? 0.f : exp2f(S[k * RMAX + r] - m);
-      S[k * RMAX + r] = p;
+      float* slot = SP + (k * RMAX + r) * 2;
+      const float p = (m == -INFINITY) ? 0.f : exp2f(slot[0] - m);
+      slot[0] = p;
+      slot[1] = p;
       l += p;
     }
 #pragma unroll
@@ -371,12 +328,14 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   consumers_sync();
 
   // ---------------------------------- consumers: PV ------------------------------------------
-  float acc[RMAX][C::EPL];
+  constexpr int EPL = C::EPL;
+  constexpr int NP = EPL >= 2 ? EPL / 2 : 1;
+  float acc[RMAX][NP][2];
 #pragma unroll
   for (int r = 0; r < RMAX; ++r)
 #pragma unroll
-    for (int e = 0; e < C::EPL; ++e) acc[r][e] = 0.f;
-  constexpr int KPW = C::TILE / kConsumerWarps;        // keys per warp per tile
+    for (int e = 0; e < NP; ++e) acc[r][e][0] = acc[r][e][1] = 0.f;
+  constexpr int KPWV = C::TILE / kConsumerWarps;       // keys per warp per tile
   for (int i = 0; i < nkt; ++i) {
     const int ti = nkt + i;
     const int st = ti % kStages;
@@ -384,20 +343,23 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     if (ok) {
       const unsigned char* tile = tiles + st * kTileBytes;
 #pragma unroll 4
-      for (int kk = 0; kk < KPW; ++kk) {
-        const int key = warp * KPW + kk;
-        float v[C::EPL];
+      for (int kk = 0; kk < KPWV; ++kk) {
+        const int key = warp * KPWV + kk;
+        float v[EPL];
         load_v<Tc, C>(tile, key, lane, v);
-        const float* pr = S + (i * C::TILE + key) * RMAX;
+        const float4* pr = reinterpret_cast<const float4*>(SP + (i * C::TILE + key) * RMAX * 2);
 #pragma unroll
-        for (int r4 = 0; r4 < RMAX; r4 += 4) {
-          const float4 p = *reinterpret_cast<const float4*>(pr + r4);
+        for (int r2 = 0; r2 < RMAX / 2; ++r2) {
+          const float4 p = pr[r2];                       // (p_r, p_r, p_r+1, p_r+1)
+          if constexpr (EPL >= 2) {
 #pragma unroll
-          for (int e = 0; e < C::EPL; ++e) {
-            acc[r4][e] = fmaf(p.x, v[e], acc[r4][e]);
-            acc[r4 + 1][e] = fmaf(p.y, v[e], acc[r4 + 1][e]);
-            acc[r4 + 2][e] = fmaf(p.z, v[e], acc[r4 + 2][e]);
-            acc[r4 + 3][e] = fmaf(p.w, v[e], acc[r4 + 3][e]);
+            for (int e = 0; e < NP; ++e) {
+              ffma2(acc[2 * r2][e][0], acc[2 * r2][e][1], p.x, p.y, v[2 * e], v[2 * e + 1]);
+              ffma2(acc[2 * r2 + 1][e][0], acc[2 * r2 + 1][e][1], p.z, p.w, v[2 * e], v[2 * e + 1]);
+            }
+          } else {
+            acc[2 * r2][0][0] = fmaf(p.x, v[0], acc[2 * r2][0][0]);
+            acc[2 * r2 + 1][0][0] = fmaf(p.z, v[0], acc[2 * r2 + 1][0][0]);
           }
         }
       }
@@ -412,60 +374,59 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
 #pragma unroll
   for (int r = 0; r < RMAX; ++r)
 #pragma unroll
-    for (int e = 0; e < C::EPL; ++e) red[(warp * RMAX + r) * D + lane * C::EPL + e] = acc[r][e];
+    for (int e = 0; e < EPL; ++e)
+      red[(warp * RMAX + r) * D + lane * EPL + e] = EPL >= 2 ? acc[r][e / 2][e % 2] : acc[r][0][0];
   consumers_sync();
-  if (*abort_flag) {
-    if (tid == 0) atomicExch(a.status, kStatusTimeout);
-    return;
-  }
+  const bool aborted = *abort_flag != 0;
+  if (aborted && tid == 0) atomicExch(a.status, kStatusTimeout);
+  const long long item_row0 = static_cast<long long>(item) * RMAX;
   for (int i = tid; i < nrows * D; i += kConsumers) {
     const int r = i / D, d = i % D;
     float o = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) o += red[(w * RMAX + r) * D + d];
-    const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+    if (aborted) continue;
     if (nsplit == 1) {
-      const long long oi = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d;
-      a.out[oi] = o / sm->l[r];
+      const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+      a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / sm->l[r];
     } else {
-      a.part_o[(static_cast<long long>(item) * RMAX + r) * D + d] = o;
+      a.part_o[(item_row0 + r) * D + d] = o;
       if (d == 0) {
-        a.part_ml[(static_cast<long long>(item) * RMAX + r) * 2] = sm->m[r];
-        a.part_ml[(static_cast<long long>(item) * RMAX + r) * 2 + 1] = sm->l[r];
+        a.part_ml[(item_row0 + r) * 2] = sm->m[r];
+        a.part_ml[(item_row0 + r) * 2 + 1] = sm->l[r];
       }
     }
   }
-}
-
-// Merge the splits of each (unit, K/V head): o = sum_i 2^(m_i - m) o_i / sum_i 2^(m_i - m) l_i,
-// evaluated as a running merge over the splits (any number of them).
-template <int RMAX>
-__global__ void __launch_bounds__(128)
-combine_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan) {
-  const int unit = blockIdx.x / a.H_kv, kvh = blockIdx.x % a.H_kv;
-  const int nsplit = (plan.prefix[unit + 1] - plan.prefix[unit]) / a.H_kv;
   if (nsplit == 1) return;
-  const int item0 = plan.prefix[unit] + kvh * nsplit;
-  const int b = plan.unit_b[unit], rt = unit % plan.n_rowtiles;
-  const int row0 = rt * RMAX;
-  const int nrows = min(RMAX, a.T * a.G - row0);
-  const int D = a.D;
-  for (int i = threadIdx.x; i < nrows * D; i += blockDim.x) {
+
+  // ---------------------------------- the last split merges ----------------------------------
+  // o = sum_s 2^(m_s - m) o_s / sum_s 2^(m_s - m) l_s over this unit's splits, by the CTA that
+  // finishes last; the partials are still in L2. The counter is reset for the next launch.
+  __threadfence();
+  consumers_sync();
+  int* counter = a.counters + unit * a.H_kv + kvh;
+  if (tid == 0) sm->last = (atomicAdd(counter, 1) == nsplit - 1);
+  consumers_sync();
+  if (!sm->last) return;
+  __threadfence();
+  const long long first_row = static_cast<long long>(plan.prefix[unit] + kvh * nsplit) * RMAX;
+  for (int i = tid; i < nrows * D; i += kConsumers) {
     const int r = i / D, d = i % D;
     float m = -INFINITY, l = 0.f, o = 0.f;
     for (int s = 0; s < nsplit; ++s) {
-      const long long base = static_cast<long long>(item0 + s) * RMAX + r;
-      const float ms = a.part_ml[base * 2], ls = a.part_ml[base * 2 + 1];
+      const long long row = first_row + static_cast<long long>(s) * RMAX + r;
+      const float ms = __ldcg(a.part_ml + row * 2), ls = __ldcg(a.part_ml + row * 2 + 1);
       if (!(ls > 0.f)) continue;                         // a split that sees no key of this row
       const float mn = fmaxf(m, ms);
       const float c_old = exp2f(m - mn), c_new = exp2f(ms - mn);
       l = l * c_old + ls * c_new;
-      o = o * c_old + a.part_o[base * D + d] * c_new;
+      o = o * c_old + __ldcg(a.part_o + row * D + d) * c_new;
       m = mn;
     }
     const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-    a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / l;
+    if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / l;
   }
+  if (tid == 0) *counter = 0;
 }
 
 template <typename Tc, int D, int RMAX>
@@ -482,13 +443,7 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<p.n_items, kThreads, smem, st>>>(a, p, *tk, *tv);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (p.n_items > p.n_units * a.H_kv) {
-    combine_kernel<RMAX><<<p.n_units * a.H_kv, 128, 0, st>>>(a, p);
-    e = cudaGetLastError();
-  }
-  return e;
+  return cudaGetLastError();
 }
 
 template <typename Tc, int D>
