@@ -13,11 +13,11 @@
 //   S^T [128 keys x N] = K_tile . Q^T       A = K tile (K-major, TMA 128-byte swizzle), B = Q^T
 //   O^T [128 d   x N] += V_tile^T . P^T     A = V tile read MN-major, B = P^T (K-major)
 // One CTA owns one (sequence, row tile, K/V head, key split). Roles:
-//   warp 0     TMA producer: the split's K tiles, then its V tiles, through a 2-stage ring;
+//   warp 0     TMA producer: the split's K tiles, then its V tiles, through a 2- or 3-stage ring;
 //   warp 1     owns TMEM (256 columns) and issues every MMA from one thread;
 //   warps 2-5  one thread per key (= TMEM lane): the scores of every K tile of the split stay in
 //              TMEM, so the softmax over the split is exact (max, then exp2 and sum) with no
-//              running rescale; P is written to shared memory as a hi + lo pair of 16-bit values
+//              running rescale; the maxima are folded in tile by tile while K still streams; P is written to shared memory as a hi + lo pair of 16-bit values
 //              (P ~ hi + lo to ~2^-16 relative), so the PV product keeps fp32-level accuracy;
 //              then the epilogue: one thread per d reads O^T from TMEM.
 // A unit with several splits writes (m, l, o) partials; the CTA that finishes its last split
@@ -35,27 +35,31 @@ constexpr int kTK = 128;                    // keys per tile = MMA M
 constexpr int kDh = 128;                    // head width = MMA K for QK, M for PV
 constexpr int kBoxBytes = kTK * 128;        // one 64-element (128-byte) swizzled column box
 constexpr int kTileBytes = 2 * kBoxBytes;   // 32 KB: a tile's K (or V) rows
-constexpr int kStages = 2;
 constexpr int kTmemCols = 256;
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 
+// Shared memory per CTA stays under ~110 KB so that two CTAs share an SM: with 16 query rows the
+// K/V ring has 3 stages and one P^T buffer, with 32 rows 2 stages and two P^T buffers.
 template <int NR>
 struct Layout {
+  static constexpr int kStages = NR == 16 ? 3 : 2;
+  static constexpr int kPBufs = NR == 16 ? 1 : 2;
   static constexpr int kQBytes = NR * 256;                      // Q^T: two atoms of NR rows x 128 B
   static constexpr int kPBytes = NR * 256;                      // one P^T operand (hi or lo)
   static constexpr int kStageOff = 0;
   static constexpr int kQOff = kStages * kTileBytes;
-  static constexpr int kPOff = kQOff + kQBytes;                 // 2 buffers x (hi, lo)
-  static constexpr int kCtlOff = kPOff + 4 * kPBytes;
+  static constexpr int kPOff = kQOff + kQBytes;                 // kPBufs buffers x (hi, lo)
+  static constexpr int kCtlOff = kPOff + 2 * kPBufs * kPBytes;
   static constexpr int kSTiles = (kTmemCols - NR) / NR;         // S^T tiles that fit beside O^T
 };
 
 template <int NR>
 struct __align__(8) Ctl {
-  unsigned long long full[kStages], empty[kStages];
-  unsigned long long p_full[2], p_empty[2];
-  unsigned long long s_full, o_full, done;
+  unsigned long long full[Layout<NR>::kStages], empty[Layout<NR>::kStages];
+  unsigned long long p_full[Layout<NR>::kPBufs], p_empty[Layout<NR>::kPBufs];
+  unsigned long long s_ready[Layout<NR>::kSTiles];             // one per K tile, used once
+  unsigned long long o_full, done;
   uint32_t tmem;
   int abort, last;
   float red[4][NR];
@@ -91,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
                  const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
   using Lo = Layout<NR>;
+  constexpr int kStages = Lo::kStages, kPBufs = Lo::kPBufs;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -113,14 +118,15 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int nsplit = (plan.prefix[unit + 1] - plan.prefix[unit]) / a.H_kv;
   const int rem = item - plan.prefix[unit];
   const int kvh = rem / nsplit, split = rem % nsplit;
-  const int b = plan.unit_b[unit];
-  const int rt = unit % plan.n_rowtiles;
+  const int b = plan.unit_b[unit] / plan.n_rowtiles;
+  const int rt = plan.unit_b[unit] % plan.n_rowtiles;
   const int row0 = rt * NR;
   const int nrows = min(NR, a.T * a.G - row0);
   const int s_b = a.lens[b] + a.delta - a.T;
   const int n_eff = s_b + (row0 + nrows - 1) / a.G + 1;
-  const int k_begin = split * plan.split_keys;
-  const int k_end = min(k_begin + plan.split_keys, n_eff);
+  const int chunk = (n_eff + nsplit - 1) / nsplit;      // near-equal splits of the unit's keys
+  const int k_begin = split * chunk;
+  const int k_end = min(k_begin + chunk, n_eff);
   const int nkt = (k_end - k_begin + kTK - 1) / kTK;
   const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
 
@@ -131,11 +137,11 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kPBufs; ++s) {
       mbar_init(smem_u32(&ctl->p_full[s]), kSoftmaxThreads / 32);
       mbar_init(smem_u32(&ctl->p_empty[s]), 1);
     }
-    mbar_init(smem_u32(&ctl->s_full), 1);
+    for (int s = 0; s < Lo::kSTiles; ++s) mbar_init(smem_u32(&ctl->s_ready[s]), 1);
     mbar_init(smem_u32(&ctl->o_full), 1);
     mbar_init(smem_u32(&ctl->done), 1);
     ctl->abort = 0;
@@ -150,7 +156,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     }
     *reinterpret_cast<Tc*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tc>(x);
   }
-  for (int i = tid; i < 4 * Lo::kPBytes / 16; i += kThreads)
+  for (int i = tid; i < 2 * kPBufs * Lo::kPBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(p_base)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async();
   tc_fence_before();
@@ -201,12 +207,12 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
                    umma_desc(s_q + (ks >> 2) * (NR * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128),
                    idesc_s, ks > 0);
         umma_commit(smem_u32(&ctl->empty[st]));
+        umma_commit(smem_u32(&ctl->s_ready[i]));
       }
-      if (ok) umma_commit(smem_u32(&ctl->s_full));
       for (int i = 0; i < nkt && ok; ++i) {                 // O^T += V_i^T . P_i^T (hi, then lo)
-        const int ti = nkt + i, st = ti % kStages, pb = i & 1;
+        const int ti = nkt + i, st = ti % kStages, pb = i % kPBufs;
         ok = mbar_wait(smem_u32(&ctl->full[st]), (ti / kStages) & 1, abort_flag) &&
-             mbar_wait(smem_u32(&ctl->p_full[pb]), (i >> 1) & 1, abort_flag);
+             mbar_wait(smem_u32(&ctl->p_full[pb]), (i / kPBufs) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vt = s_stage + st * kTileBytes;
@@ -238,12 +244,16 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
 #pragma unroll
     for (int r = 0; r < NR; ++r) trow[r] = (r < nrows) ? s_b + (row0 + r) / a.G : -1;   // last visible key
 
-    bool ok = mbar_wait(smem_u32(&ctl->s_full), 0, abort_flag);
-    tc_fence_after();
+    // pass 1, overlapped with the K stream: fold each score tile into the row maxima as soon as
+    // its MMAs complete
+    bool ok = true;
     float m_run[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) m_run[r] = -INFINITY;
     for (int i = 0; i < nkt && ok; ++i) {
+      ok = mbar_wait(smem_u32(&ctl->s_ready[i]), 0, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
       float v[NR];
 #pragma unroll
       for (int c = 0; c < NR; c += 16) tmem_ld16(tmem + lane_base + i * NR + c, v + c);
@@ -269,8 +279,8 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
 #pragma unroll
     for (int r = 0; r < NR; ++r) l_run[r] = 0.f;
     for (int i = 0; i < nkt && ok; ++i) {
-      const int pb = i & 1;
-      ok = mbar_wait(smem_u32(&ctl->p_empty[pb]), ((i >> 1) & 1) ^ 1, abort_flag);
+      const int pb = i % kPBufs;
+      ok = mbar_wait(smem_u32(&ctl->p_empty[pb]), ((i / kPBufs) & 1) ^ 1, abort_flag);
       if (!ok) break;
       float v[NR];
 #pragma unroll

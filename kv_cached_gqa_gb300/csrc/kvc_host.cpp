@@ -382,38 +382,60 @@ int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, i
     return fail(h, KVC_E_UNSUPPORTED, "B * row tiles = %lld exceeds %d", static_cast<long long>(h->B) * n_rt,
                 kvc::kMaxUnits);
 
+  // ---- split plan: every CTA gets about the same number of keys -----------------------------
+  // The total work W = H_kv * sum_u n_u (n_u = keys visible to unit u) is cut into about k waves of
+  // resident CTAs (two per SM); each unit's keys are split into near-equal chunks of about
+  // W / (k * slots) keys, at most `cmax` (what one CTA can hold), and units are ordered longest
+  // chunk first so the hardware scheduler packs the last wave tightly.
   static thread_local kvc::SplitPlan plan;   // large: keep it off the stack
-  plan.n_units = h->B * n_rt;
+  static thread_local std::vector<std::pair<int, int>> order;
+  const int n_units = h->B * n_rt;
+  plan.n_units = n_units;
   plan.rows_per_tile = rpt;
   plan.n_rowtiles = n_rt;
+  const int cmax = max_tiles * tile;
+  std::vector<long long>& n_eff = h->plan_n_eff;
+  n_eff.resize(n_units);
   long long total_keys = 0;
   for (int b = 0; b < h->B; ++b)
     for (int rt = 0; rt < n_rt; ++rt) {
       const int t_max = std::min(T - 1, ((rt + 1) * rpt - 1) / G);
-      total_keys += static_cast<long long>(h->lens[b]) + t_max + 1;
+      n_eff[b * n_rt + rt] = static_cast<long long>(h->lens[b]) + t_max + 1;
+      total_keys += n_eff[b * n_rt + rt];
     }
-  const int cmax = max_tiles * tile;
-  int split = h->split_keys_override;
-  if (split <= 0) {
-    // aim for ~8 CTAs per SM in total (two resident per SM, about four waves)
-    const long long target = 8LL * h->num_sms;
-    split = static_cast<int>((total_keys * h->H + target - 1) / target);
+  const long long slots = 2LL * h->num_sms;
+  const long long work = total_keys * h->H;
+  long long w = h->split_keys_override;
+  if (w <= 0) {
+    const long long waves = std::max(1LL, (work + slots * 1536 - 1) / (slots * 1536));
+    w = (work + waves * slots - 1) / (waves * slots);
   }
-  split = std::max(tile, std::min(cmax, (split + tile - 1) / tile * tile));
-  plan.split_keys = split;
+  w = std::max(1LL, w);
+  order.resize(n_units);
+  h->plan_nsplit.resize(n_units);
+  for (int u = 0; u < n_units; ++u) {
+    long long ns = std::max(1LL, (n_eff[u] + w / 2) / w);
+    while ((n_eff[u] + ns - 1) / ns > cmax) ++ns;
+    const long long chunk = (n_eff[u] + ns - 1) / ns;
+    ns = (n_eff[u] + chunk - 1) / chunk;                    // same chunk, no empty trailing split
+    order[u] = {static_cast<int>(chunk), u};
+    h->plan_nsplit[u] = static_cast<int>(ns);
+  }
+  std::stable_sort(order.begin(), order.end(),
+                   [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; });
   long long items = 0;
   plan.prefix[0] = 0;
-  for (int b = 0; b < h->B; ++b)
-    for (int rt = 0; rt < n_rt; ++rt) {
-      const int u = b * n_rt + rt;
-      const int t_max = std::min(T - 1, ((rt + 1) * rpt - 1) / G);
-      const long long n_eff = static_cast<long long>(h->lens[b]) + t_max + 1;
-      items += h->H * ((n_eff + split - 1) / split);
-      if (items >= (1LL << 31)) return fail(h, KVC_E_UNSUPPORTED, "too many work items");
-      plan.prefix[u + 1] = static_cast<int32_t>(items);
-      plan.unit_b[u] = b;
-    }
+  int max_chunk = 0;
+  for (int i = 0; i < n_units; ++i) {
+    const int u = order[i].second;
+    items += static_cast<long long>(h->H) * h->plan_nsplit[u];
+    if (items >= (1LL << 31)) return fail(h, KVC_E_UNSUPPORTED, "too many work items");
+    plan.prefix[i + 1] = static_cast<int32_t>(items);
+    plan.unit_b[i] = u;                                     // = b * n_rowtiles + rt
+    max_chunk = std::max(max_chunk, order[i].first);
+  }
   plan.n_items = static_cast<int>(items);
+  plan.split_keys = max_chunk;
 
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (plan.n_items > plan.n_units * h->H) {

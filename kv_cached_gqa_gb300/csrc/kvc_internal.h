@@ -51,11 +51,11 @@ cudaError_t launch_positions(const int32_t* lens, int B, int T, int32_t* out, cu
 struct SplitPlan {
   int n_units;                       // units = (sequence b, row tile rt)
   int n_items;                       // CTAs: sum over units of H_kv * nsplit
-  int split_keys;                    // keys per split (multiple of the kernel's tile)
+  int split_keys;                    // largest split (keys); a unit's nsplit splits are near-equal
   int rows_per_tile;                 // query rows (t, g) per unit
   int n_rowtiles;                    // row tiles per sequence
   int32_t prefix[kMaxUnits + 1];     // item prefix over units
-  int32_t unit_b[kMaxUnits];         // sequence of each unit (rt = unit % n_rowtiles)
+  int32_t unit_b[kMaxUnits];         // b * n_rowtiles + rt of each unit, in dispatch order
 };
 
 struct AttnArgs {
@@ -108,6 +108,8 @@ struct kvc_cache {
   int* d_counters = nullptr;      // split-K merge counters [kMaxUnits * H]
   size_t work_floats = 0;
   int split_keys_override = 0;
+  std::vector<long long> plan_n_eff;  // planner scratch
+  std::vector<int> plan_nsplit;
   uint64_t launches = 0;          // kernels enqueued by this handle
   int num_sms = 0;
   int device = 0;

@@ -183,16 +183,17 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int nsplit = (plan.prefix[unit + 1] - plan.prefix[unit]) / a.H_kv;
   const int rem = item - plan.prefix[unit];
   const int kvh = rem / nsplit, split = rem % nsplit;
-  const int b = plan.unit_b[unit];
-  const int rt = unit % plan.n_rowtiles;
+  const int b = plan.unit_b[unit] / plan.n_rowtiles;
+  const int rt = plan.unit_b[unit] % plan.n_rowtiles;
   const int R = a.T * a.G;                              // query rows of this K/V head
   const int row0 = rt * RMAX;
   const int nrows = min(RMAX, R - row0);
   const int s_b = a.lens[b] + a.delta - a.T;            // committed length = first query position
   const int t_max = (row0 + nrows - 1) / a.G;
   const int n_eff = s_b + t_max + 1;                    // keys visible to the tile's last row
-  const int k_begin = split * plan.split_keys;
-  const int k_end = min(k_begin + plan.split_keys, n_eff);
+  const int chunk = (n_eff + nsplit - 1) / nsplit;      // near-equal splits of the unit's keys
+  const int k_begin = split * chunk;
+  const int k_end = min(k_begin + chunk, n_eff);
   const int n_keys = k_end - k_begin;
   const int nkt = (n_keys + C::TILE - 1) / C::TILE;
   const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
