@@ -173,6 +173,26 @@ int kvc_last_error(kvc_handle h, char* buf, size_t n);
 int kvc_set_split_keys(kvc_handle h, int keys);
 
 /*
+ * gqa_cached_attn_noalloc — gqa_cached_attn for callers that cannot let the library allocate device
+ * memory. The pages have no counterpart: it is an operational variant of the same computation.
+ * Who needs it: a serving process that reserves its device memory up front (most of the HBM goes to
+ * the KV cache) and forbids allocations while it serves; a caller whose memory is owned by another
+ * framework's pool; a latency-critical path that must not stall or fail on an allocation.
+ * Arguments, results, errors and kernels are those of gqa_cached_attn. The split-K partial results
+ * and merge counters live in one fixed 8 MiB device array inside the library instead of the handle's
+ * workspace; nothing is allocated (no cudaMalloc/cudaMallocAsync/cudaFree, no library allocator).
+ * - A call whose plan needs more than the 8 MiB returns KVC_E_UNSUPPORTED (the message gives both
+ *   sizes); every GPU that loads the library holds the array until the process exits.
+ * - The first call on each device looks up the array's address (cudaGetSymbolAddress, with that
+ *   device current); make that first call before any stream capture.
+ * - All calls share the array and it keeps the last call's contents; each call clears the counters it
+ *   needs (cudaMemsetAsync on `stream`) before its kernel. Calls that overlap on the GPU (unordered
+ *   streams) race on the array and give wrong results: order them on one stream.
+ */
+int gqa_cached_attn_noalloc(kvc_handle h, const void* q_dev, kvc_dtype q_dtype, int layer, int s, int T,
+                            int H_q, float* out_dev, void* stream);
+
+/*
  * kvc_launch_count — number of kernels this handle has enqueued since kvc_create (host counter,
  * incremented at each successful launch). Instrumentation for benchmarks; 0 for NULL.
  */

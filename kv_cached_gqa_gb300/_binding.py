@@ -36,6 +36,7 @@ SIGNATURES = {
     "kvc_nbytes": (_sz, [_vp]),
     "kvc_layer_ptrs": (_c_int, [_vp, _c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp)]),
     "gqa_cached_attn": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
+    "gqa_cached_attn_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
     "kvc_status": (_c_int, [_vp, _vp]),
     "kvc_last_error": (_c_int, [_vp, ctypes.c_char_p, _sz]),
     "kvc_set_split_keys": (_c_int, [_vp, _c_int]),
@@ -194,6 +195,16 @@ def gqa_cached_attn(c: Cache, q, layer: int, s: int = KVC_COMMITTED, out=None, s
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     _check(load().gqa_cached_attn(c.h, _ptr(q), dtype_code(q.dtype), layer, s, int(q.shape[2]),
                                   int(q.shape[1]), _ptr(out), _stream(stream)), c.h)
+    return out
+
+
+def gqa_cached_attn_noalloc(c: Cache, q, layer: int, out, s: int = KVC_COMMITTED, stream=None):
+    """gqa_cached_attn for callers that cannot let the library allocate: scratch comes from a fixed
+    8 MiB device array in the library, so `out` must be supplied by the caller."""
+    if q.dim() != 4 or q.shape[0] != c.B or q.shape[3] != c.d_h or out.shape != q.shape:
+        raise ValueError("q and out must be [B, H_q, T, d_h]")
+    _check(load().gqa_cached_attn_noalloc(c.h, _ptr(q), dtype_code(q.dtype), layer, s, int(q.shape[2]),
+                                          int(q.shape[1]), _ptr(out), _stream(stream)), c.h)
     return out
 
 

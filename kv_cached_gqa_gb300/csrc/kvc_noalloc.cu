@@ -1,0 +1,184 @@
+// gqa_cached_attn_noalloc: the attention call without any device allocation.
+//
+// gqa_cached_attn keeps a per-handle workspace for the split-K partial results and grows it with
+// cudaMallocAsync the first time a larger one is needed. Some callers cannot allow that: a serving
+// process that reserves all of its device memory up front (the KV cache takes most of the HBM) and
+// forbids allocations once it serves, a caller whose memory belongs to another framework's pool,
+// or a latency-critical path that must not stall or fail on an allocation under memory pressure.
+// This entry point runs the same kernels, but their scratch (the split partials and the per-unit
+// merge counters) lives in one fixed file-scope device array, so the call allocates nothing.
+//
+// Rules of use:
+// * The array holds kNoallocScratchBytes (8 MiB); a call whose plan needs more is rejected with
+//   KVC_E_UNSUPPORTED and a message giving both sizes. Every GPU that loads the library holds the
+//   array until the process exits.
+// * The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
+//   that device current) and caches it. Make that first call before any stream capture.
+// * All calls share the one array and it keeps the last call's contents. Each call clears the merge
+//   counters it uses (cudaMemsetAsync on its stream) before launching. Calls that overlap on the GPU
+//   (different streams, no ordering between them) race on the array and give wrong results.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "kvc_internal.h"
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = 8u << 20;
+constexpr int kMaxDevices = 64;
+
+// The scratch itself: split partials (float) preceded by the merge counters (int).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_addr_mutex;
+void* g_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device.
+int scratch_address(void** out, std::string* err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { *err = cudaGetErrorString(e); return KVC_E_CUDA; }
+  if (dev < 0 || dev >= kMaxDevices) { *err = "device index out of range"; return KVC_E_UNSUPPORTED; }
+  std::lock_guard<std::mutex> lock(g_addr_mutex);
+  if (!g_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      *err = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
+      return KVC_E_CUDA;
+    }
+    g_addr[dev] = p;
+  }
+  *out = g_addr[dev];
+  return KVC_OK;
+}
+
+int set_err(kvc_handle h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  h->err = buf;
+  return code;
+}
+
+}  // namespace
+
+extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s,
+                                       int T, int H_q, float* out, void* stream) {
+  if (!h) return KVC_E_INVAL;
+  // ---- the same argument and state checks as gqa_cached_attn -----------------------------------
+  if (layer < 0 || layer >= h->L) return set_err(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
+  if (T < 1) return set_err(h, KVC_E_INVAL, "T=%d must be >= 1", T);
+  if (!q || !out) return set_err(h, KVC_E_INVAL, "null q/out");
+  if (H_q < 1 || H_q % h->H) return set_err(h, KVC_E_INVAL, "H_q=%d must be a positive multiple of H_kv=%d", H_q, h->H);
+  if ((q_dtype != KVC_F32 && q_dtype != KVC_F16 && q_dtype != KVC_BF16) || (q_dtype != KVC_F32 && q_dtype != h->dtype))
+    return set_err(h, KVC_E_INVAL, "query dtype %d must be F32 or the cache dtype", q_dtype);
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return set_err(h, KVC_E_INVAL, "q/out must be 16-byte aligned");
+  if (s < KVC_COMMITTED) return set_err(h, KVC_E_INVAL, "s=%d", s);
+  for (int b = 0; b < h->B; ++b) {
+    if (s >= 0 && h->lens[b] != s)
+      return set_err(h, KVC_E_STATE, "s=%d but sequence %d has committed length %d", s, b, h->lens[b]);
+    if (h->fill[static_cast<size_t>(layer) * h->B + b] != h->lens[b] + T)
+      return set_err(h, KVC_E_STATE, "layer %d holds %d rows of sequence %d; attention needs s_b + T = %d",
+                     layer, h->fill[static_cast<size_t>(layer) * h->B + b], b, h->lens[b] + T);
+  }
+
+  // ---- the same kernel choice and split plan ----------------------------------------------------
+  const int G = H_q / h->H, R = T * G;
+  int rpt = 0, tile = 0, max_tiles = 0;
+  const bool use_tc = h->has_tc && R <= 32 && kvc::decode_tc_shape(h->dtype, h->D, R, &rpt, &tile, &max_tiles);
+  if (!use_tc) {
+    if (!kvc::splitk_shape(h->dtype, h->D, R, &rpt, &tile))
+      return set_err(h, KVC_E_UNSUPPORTED, "no attention kernel for d_h=%d", h->D);
+    max_tiles = (8192 / (2 * rpt)) / tile;
+  }
+  const int n_rt = (R + rpt - 1) / rpt;
+  const int n_units = h->B * n_rt;
+  if (n_units > kvc::kMaxUnits) return set_err(h, KVC_E_UNSUPPORTED, "B * row tiles = %d exceeds %d", n_units, kvc::kMaxUnits);
+  static thread_local kvc::SplitPlan plan;
+  static thread_local std::vector<long long> n_eff;
+  static thread_local std::vector<int> nsplit;
+  static thread_local std::vector<std::pair<int, int>> order;
+  n_eff.resize(n_units);
+  nsplit.resize(n_units);
+  order.resize(n_units);
+  long long total_keys = 0;
+  for (int b = 0; b < h->B; ++b)
+    for (int rt = 0; rt < n_rt; ++rt) {
+      const int t_max = std::min(T - 1, ((rt + 1) * rpt - 1) / G);
+      n_eff[b * n_rt + rt] = static_cast<long long>(h->lens[b]) + t_max + 1;
+      total_keys += n_eff[b * n_rt + rt];
+    }
+  const int cmax = max_tiles * tile;
+  const long long slots = 2LL * h->num_sms, work = total_keys * h->H;
+  long long w = h->split_keys_override;
+  if (w <= 0) {
+    const long long waves = std::max(1LL, (work + slots * 1536 - 1) / (slots * 1536));
+    w = (work + waves * slots - 1) / (waves * slots);
+  }
+  w = std::max(1LL, w);
+  for (int u = 0; u < n_units; ++u) {
+    long long ns = std::max(1LL, (n_eff[u] + w / 2) / w);
+    while ((n_eff[u] + ns - 1) / ns > cmax) ++ns;
+    const long long chunk = (n_eff[u] + ns - 1) / ns;
+    ns = (n_eff[u] + chunk - 1) / chunk;
+    order[u] = {static_cast<int>(chunk), u};
+    nsplit[u] = static_cast<int>(ns);
+  }
+  std::stable_sort(order.begin(), order.end(),
+                   [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; });
+  long long items = 0;
+  int max_chunk = 0;
+  plan.prefix[0] = 0;
+  for (int i = 0; i < n_units; ++i) {
+    const int u = order[i].second;
+    items += static_cast<long long>(h->H) * nsplit[u];
+    if (items >= (1LL << 31)) return set_err(h, KVC_E_UNSUPPORTED, "too many work items");
+    plan.prefix[i + 1] = static_cast<int32_t>(items);
+    plan.unit_b[i] = u;
+    max_chunk = std::max(max_chunk, order[i].first);
+  }
+  plan.n_units = n_units;
+  plan.n_items = static_cast<int>(items);
+  plan.rows_per_tile = rpt;
+  plan.n_rowtiles = n_rt;
+  plan.split_keys = max_chunk;
+
+  // ---- scratch from the fixed array: [counters | partial o | partial (m, l)] ------------------
+  const size_t counter_bytes = (static_cast<size_t>(n_units) * h->H * sizeof(int) + 255) / 256 * 256;
+  const size_t part_bytes = kvc::splitk_workspace_floats(plan, h->D) * sizeof(float);
+  if (counter_bytes + part_bytes > kNoallocScratchBytes)
+    return set_err(h, KVC_E_UNSUPPORTED, "this call needs %zu bytes of scratch; the fixed array holds %zu",
+                   counter_bytes + part_bytes, kNoallocScratchBytes);
+  void* base = nullptr;
+  std::string err;
+  int rc = scratch_address(&base, &err);
+  if (rc) return set_err(h, rc, "%s", err.c_str());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(base, 0, counter_bytes, st);
+  if (e != cudaSuccess) return set_err(h, KVC_E_CUDA, "clearing the merge counters: %s", cudaGetErrorString(e));
+
+  kvc::AttnArgs a{};
+  a.q = q; a.q_dtype = q_dtype; a.out = out;
+  a.counters = static_cast<int*>(base);
+  a.part_o = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + counter_bytes);
+  a.part_ml = a.part_o + static_cast<size_t>(plan.n_items) * rpt * h->D;
+  a.lens = h->d_lens; a.status = h->d_status;
+  a.layer = layer; a.B = h->B; a.H_kv = h->H; a.H_q = H_q; a.G = G; a.T = T; a.D = h->D;
+  a.max_len = h->max_len; a.delta = T; a.cache_dtype = h->dtype;
+  e = use_tc ? kvc::launch_decode_tc(a, plan, &h->tmap_k_tc, &h->tmap_v_tc, st)
+             : kvc::launch_splitk(a, plan, &h->tmap_k_split, &h->tmap_v_split, st);
+  if (e != cudaSuccess) return set_err(h, KVC_E_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  h->launches += 1;
+  return KVC_OK;
+}
