@@ -64,9 +64,13 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("kvc_decode_tc.cu", "kvc_splitk.cu", "kvc_device.cuh", "kvc_host.cpp")
+
+
 def kernel_source_hash():
+    """Hash of the sources that define the attention kernels and their launch plan."""
     h = hashlib.sha256()
-    for name in ("kvc_splitk.cu",):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "kv_cached_gqa_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -383,7 +387,8 @@ def run_ours(args):
         "steps_per_s": round(world * 1e3 / ms, 3),
         "pct_of_peak": {"measured_hbm": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / 8000.0, 2)},
-        "roofline": {"kernel": "gqa_cached_attn (split-K attention + combine)", "bound": "hbm",
+        "roofline": {"kernel": "gqa_cached_attn (decode_tc_kernel: tcgen05 split-K attention with fused merge)",
+                     "bound": "hbm",
                      "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(attn_gbs / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": sp.attn_bytes(), "launch_ms": round(attn_avg_ms, 5),
