@@ -15,6 +15,8 @@
 #include <memory>
 #include <new>
 #include <string>
+#include <utility>
+#include <vector>
 
 #include "kvc_internal.h"
 
@@ -174,6 +176,115 @@ bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max
     return false;
   }
   return true;
+}
+
+// ---- kernel choice and work plan ------------------------------------------------------------------
+// Tensor cores serve 16-bit caches with d_h = 128: the decode kernel for up to 32 query rows per K/V
+// head (decode and verify chunks), the chunk kernel beyond that (prefill). Everything else runs on
+// the CUDA-core split-K kernel. For the split kernels, the total key work W = H_kv * sum_u n_u (n_u =
+// keys visible to unit u) is cut into about k waves of resident CTAs (two per SM); each unit's keys
+// are split into near-equal chunks of about W / (k * slots) keys, at most what one CTA can hold, and
+// units are ordered longest chunk first so the hardware scheduler packs the last wave tightly.
+int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out, std::string* err) {
+  const int G = H_q / h->H;
+  const int R = T * G;
+  int rpt = 0, tile = 0, max_tiles = 0;
+  AttnKernel kind;
+  if (h->has_tc && R <= 32 && decode_tc_shape(h->dtype, h->D, R, &rpt, &tile, &max_tiles)) {
+    kind = AttnKernel::DecodeTC;
+  } else if (h->has_tc && R > 32 && prefill_tc_shape(h->dtype, h->D, &rpt)) {
+    kind = AttnKernel::PrefillTC;
+  } else {
+    if (!splitk_shape(h->dtype, h->D, R, &rpt, &tile)) {
+      *err = "no attention kernel for this d_h";
+      return KVC_E_UNSUPPORTED;
+    }
+    max_tiles = (8192 / (2 * rpt)) / tile;                  // the kernel's weight buffer
+    kind = AttnKernel::SplitK;
+  }
+  const int n_rt = (R + rpt - 1) / rpt;
+  if (static_cast<long long>(h->B) * n_rt > kMaxUnits) {
+    *err = "batch x row tiles exceeds the planner's limit of 2048 units";
+    return KVC_E_UNSUPPORTED;
+  }
+  const int n_units = h->B * n_rt;
+  plan->n_units = n_units;
+  plan->rows_per_tile = rpt;
+  plan->n_rowtiles = n_rt;
+  std::vector<long long>& n_eff = h->plan_n_eff;
+  std::vector<int>& nsplit = h->plan_nsplit;
+  std::vector<std::pair<int, int>>& order = h->plan_order;
+  n_eff.resize(n_units);
+  nsplit.resize(n_units);
+  order.resize(n_units);
+  long long total_keys = 0;
+  for (int b = 0; b < h->B; ++b)
+    for (int rt = 0; rt < n_rt; ++rt) {
+      const int t_max = std::min(T - 1, ((rt + 1) * rpt - 1) / G);
+      n_eff[b * n_rt + rt] = static_cast<long long>(h->lens[b]) + t_max + 1;
+      total_keys += n_eff[b * n_rt + rt];
+    }
+  auto longest_first = [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; };
+  out->kernel = kind;
+  out->rows_per_tile = rpt;
+  if (kind == AttnKernel::PrefillTC) {                      // one CTA per (unit, K/V head), longest first
+    for (int u = 0; u < n_units; ++u) order[u] = {static_cast<int>(std::min<long long>(n_eff[u], 1 << 30)), u};
+    std::stable_sort(order.begin(), order.end(), longest_first);
+    for (int i = 0; i < n_units; ++i) plan->unit_b[i] = order[i].second;
+    plan->n_items = n_units * h->H;
+    plan->split_keys = n_units ? order[0].first : 0;
+    plan->prefix[0] = 0;
+    out->workspace_floats = 0;
+    out->counters = 0;
+    return KVC_OK;
+  }
+  const int cmax = max_tiles * tile;
+  const long long slots = 2LL * h->num_sms;
+  const long long work = total_keys * h->H;
+  long long w = h->split_keys_override;
+  if (w <= 0) {
+    const long long waves = std::max(1LL, (work + slots * 1536 - 1) / (slots * 1536));
+    w = (work + waves * slots - 1) / (waves * slots);
+  }
+  w = std::max(1LL, w);
+  for (int u = 0; u < n_units; ++u) {
+    long long ns = std::max(1LL, (n_eff[u] + w / 2) / w);
+    while ((n_eff[u] + ns - 1) / ns > cmax) ++ns;
+    const long long chunk = (n_eff[u] + ns - 1) / ns;
+    ns = (n_eff[u] + chunk - 1) / chunk;                    // same chunk, no empty trailing split
+    order[u] = {static_cast<int>(chunk), u};
+    nsplit[u] = static_cast<int>(ns);
+  }
+  std::stable_sort(order.begin(), order.end(), longest_first);
+  long long items = 0;
+  int max_chunk = 0;
+  plan->prefix[0] = 0;
+  for (int i = 0; i < n_units; ++i) {
+    const int u = order[i].second;
+    items += static_cast<long long>(h->H) * nsplit[u];
+    if (items >= (1LL << 31)) {
+      *err = "too many work items";
+      return KVC_E_UNSUPPORTED;
+    }
+    plan->prefix[i + 1] = static_cast<int32_t>(items);
+    plan->unit_b[i] = u;                                    // = b * n_rowtiles + rt
+    max_chunk = std::max(max_chunk, order[i].first);
+  }
+  plan->n_items = static_cast<int>(items);
+  plan->split_keys = max_chunk;
+  out->workspace_floats = plan->n_items > n_units * h->H ? splitk_workspace_floats(*plan, h->D) : 0;
+  out->counters = static_cast<size_t>(n_units) * h->H;
+  return KVC_OK;
+}
+
+cudaError_t launch_attention(const AttnPlan& ap, const AttnArgs& a, const SplitPlan& p, kvc_handle h,
+                             cudaStream_t st) {
+  switch (ap.kernel) {
+    case AttnKernel::DecodeTC: return launch_decode_tc(a, p, &h->tmap_k_tc, &h->tmap_v_tc, st);
+    case AttnKernel::PrefillTC: return launch_prefill_tc(a, p, &h->tmap_k_tc, &h->tmap_v_tc, st);
+    case AttnKernel::SplitK: return launch_splitk(a, p, &h->tmap_k_split, &h->tmap_v_split, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvc
@@ -366,80 +477,17 @@ int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, i
                   "(append the chunk to this layer first)", layer, h->fill[static_cast<size_t>(layer) * h->B + b],
                   b, h->lens[b] + T);
   }
-  const int G = H_q / h->H;
-  const int R = T * G;
-  // kernel choice: tensor cores for 16-bit caches with d_h = 128 and at most 32 query rows per K/V
-  // head; CUDA cores otherwise
-  int rpt = 0, tile = 0, max_tiles = 0;
-  const bool use_tc = h->has_tc && R <= 32 && kvc::decode_tc_shape(h->dtype, h->D, R, &rpt, &tile, &max_tiles);
-  if (!use_tc) {
-    if (!kvc::splitk_shape(h->dtype, h->D, R, &rpt, &tile))
-      return fail(h, KVC_E_UNSUPPORTED, "no attention kernel for d_h=%d", h->D);
-    max_tiles = (8192 / (2 * rpt)) / tile;                  // the kernel's weight buffer
-  }
-  const int n_rt = (R + rpt - 1) / rpt;
-  if (static_cast<long long>(h->B) * n_rt > kvc::kMaxUnits)
-    return fail(h, KVC_E_UNSUPPORTED, "B * row tiles = %lld exceeds %d", static_cast<long long>(h->B) * n_rt,
-                kvc::kMaxUnits);
-
-  // ---- split plan: every CTA gets about the same number of keys -----------------------------
-  // The total work W = H_kv * sum_u n_u (n_u = keys visible to unit u) is cut into about k waves of
-  // resident CTAs (two per SM); each unit's keys are split into near-equal chunks of about
-  // W / (k * slots) keys, at most `cmax` (what one CTA can hold), and units are ordered longest
-  // chunk first so the hardware scheduler packs the last wave tightly.
   static thread_local kvc::SplitPlan plan;   // large: keep it off the stack
-  static thread_local std::vector<std::pair<int, int>> order;
-  const int n_units = h->B * n_rt;
-  plan.n_units = n_units;
-  plan.rows_per_tile = rpt;
-  plan.n_rowtiles = n_rt;
-  const int cmax = max_tiles * tile;
-  std::vector<long long>& n_eff = h->plan_n_eff;
-  n_eff.resize(n_units);
-  long long total_keys = 0;
-  for (int b = 0; b < h->B; ++b)
-    for (int rt = 0; rt < n_rt; ++rt) {
-      const int t_max = std::min(T - 1, ((rt + 1) * rpt - 1) / G);
-      n_eff[b * n_rt + rt] = static_cast<long long>(h->lens[b]) + t_max + 1;
-      total_keys += n_eff[b * n_rt + rt];
-    }
-  const long long slots = 2LL * h->num_sms;
-  const long long work = total_keys * h->H;
-  long long w = h->split_keys_override;
-  if (w <= 0) {
-    const long long waves = std::max(1LL, (work + slots * 1536 - 1) / (slots * 1536));
-    w = (work + waves * slots - 1) / (waves * slots);
-  }
-  w = std::max(1LL, w);
-  order.resize(n_units);
-  h->plan_nsplit.resize(n_units);
-  for (int u = 0; u < n_units; ++u) {
-    long long ns = std::max(1LL, (n_eff[u] + w / 2) / w);
-    while ((n_eff[u] + ns - 1) / ns > cmax) ++ns;
-    const long long chunk = (n_eff[u] + ns - 1) / ns;
-    ns = (n_eff[u] + chunk - 1) / chunk;                    // same chunk, no empty trailing split
-    order[u] = {static_cast<int>(chunk), u};
-    h->plan_nsplit[u] = static_cast<int>(ns);
-  }
-  std::stable_sort(order.begin(), order.end(),
-                   [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; });
-  long long items = 0;
-  plan.prefix[0] = 0;
-  int max_chunk = 0;
-  for (int i = 0; i < n_units; ++i) {
-    const int u = order[i].second;
-    items += static_cast<long long>(h->H) * h->plan_nsplit[u];
-    if (items >= (1LL << 31)) return fail(h, KVC_E_UNSUPPORTED, "too many work items");
-    plan.prefix[i + 1] = static_cast<int32_t>(items);
-    plan.unit_b[i] = u;                                     // = b * n_rowtiles + rt
-    max_chunk = std::max(max_chunk, order[i].first);
-  }
-  plan.n_items = static_cast<int>(items);
-  plan.split_keys = max_chunk;
+  kvc::AttnPlan ap{};
+  std::string perr;
+  const int prc = kvc::plan_attention(h, T, H_q, &plan, &ap, &perr);
+  if (prc) return fail(h, prc, "%s", perr.c_str());
+  const int G = H_q / h->H;
+  const int rpt = ap.rows_per_tile;
 
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (plan.n_items > plan.n_units * h->H) {
-    const size_t need = kvc::splitk_workspace_floats(plan, h->D);
+  if (ap.workspace_floats) {
+    const size_t need = ap.workspace_floats;
     if (need > h->work_floats) {
       const size_t grow = need + need / 4;
       float* p = nullptr;
@@ -458,8 +506,7 @@ int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, i
   a.lens = h->d_lens; a.status = h->d_status;
   a.layer = layer; a.B = h->B; a.H_kv = h->H; a.H_q = H_q; a.G = G; a.T = T; a.D = h->D;
   a.max_len = h->max_len; a.delta = T; a.cache_dtype = h->dtype;
-  cudaError_t e = use_tc ? kvc::launch_decode_tc(a, plan, &h->tmap_k_tc, &h->tmap_v_tc, st)
-                         : kvc::launch_splitk(a, plan, &h->tmap_k_split, &h->tmap_v_split, st);
+  cudaError_t e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
   h->launches += 1;
   return KVC_OK;

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/kvc.h"
@@ -84,6 +85,24 @@ bool decode_tc_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* til
 cudaError_t launch_decode_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
                              const CUtensorMap* tv, cudaStream_t st);
 
+// Tensor-core chunk (prefill) kernel: 16-bit caches, d_h = 128, 128 query rows per CTA.
+bool prefill_tc_shape(kvc_dtype dt, int D, int* rows_per_tile);
+cudaError_t launch_prefill_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
+                              const CUtensorMap* tv, cudaStream_t st);
+
+// Which attention kernel serves a call, and its work plan (built from the host mirror of the lengths).
+enum class AttnKernel { SplitK, DecodeTC, PrefillTC };
+struct AttnPlan {
+  AttnKernel kernel;
+  int rows_per_tile;
+  size_t workspace_floats;   // split partials (0 when no unit splits)
+  size_t counters;           // merge counters the kernel may use (units x H_kv)
+};
+// Fills `plan` (a large struct: keep it off the stack); returns KVC_OK or an error code with `err`.
+int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out, std::string* err);
+cudaError_t launch_attention(const AttnPlan& ap, const AttnArgs& a, const SplitPlan& p, kvc_handle h,
+                             cudaStream_t st);
+
 // Tensor map over a store viewed as [L*B*H, max_len, D] with boxes of (swizzle span, box_rows, 1).
 bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max_len,
                       long long planes, int box_rows, std::string* err);
@@ -110,6 +129,7 @@ struct kvc_cache {
   int split_keys_override = 0;
   std::vector<long long> plan_n_eff;  // planner scratch
   std::vector<int> plan_nsplit;
+  std::vector<std::pair<int, int>> plan_order;
   uint64_t launches = 0;          // kernels enqueued by this handle
   int num_sms = 0;
   int device = 0;

@@ -94,69 +94,17 @@ extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_
   }
 
   // ---- the same kernel choice and split plan ----------------------------------------------------
-  const int G = H_q / h->H, R = T * G;
-  int rpt = 0, tile = 0, max_tiles = 0;
-  const bool use_tc = h->has_tc && R <= 32 && kvc::decode_tc_shape(h->dtype, h->D, R, &rpt, &tile, &max_tiles);
-  if (!use_tc) {
-    if (!kvc::splitk_shape(h->dtype, h->D, R, &rpt, &tile))
-      return set_err(h, KVC_E_UNSUPPORTED, "no attention kernel for d_h=%d", h->D);
-    max_tiles = (8192 / (2 * rpt)) / tile;
-  }
-  const int n_rt = (R + rpt - 1) / rpt;
-  const int n_units = h->B * n_rt;
-  if (n_units > kvc::kMaxUnits) return set_err(h, KVC_E_UNSUPPORTED, "B * row tiles = %d exceeds %d", n_units, kvc::kMaxUnits);
   static thread_local kvc::SplitPlan plan;
-  static thread_local std::vector<long long> n_eff;
-  static thread_local std::vector<int> nsplit;
-  static thread_local std::vector<std::pair<int, int>> order;
-  n_eff.resize(n_units);
-  nsplit.resize(n_units);
-  order.resize(n_units);
-  long long total_keys = 0;
-  for (int b = 0; b < h->B; ++b)
-    for (int rt = 0; rt < n_rt; ++rt) {
-      const int t_max = std::min(T - 1, ((rt + 1) * rpt - 1) / G);
-      n_eff[b * n_rt + rt] = static_cast<long long>(h->lens[b]) + t_max + 1;
-      total_keys += n_eff[b * n_rt + rt];
-    }
-  const int cmax = max_tiles * tile;
-  const long long slots = 2LL * h->num_sms, work = total_keys * h->H;
-  long long w = h->split_keys_override;
-  if (w <= 0) {
-    const long long waves = std::max(1LL, (work + slots * 1536 - 1) / (slots * 1536));
-    w = (work + waves * slots - 1) / (waves * slots);
-  }
-  w = std::max(1LL, w);
-  for (int u = 0; u < n_units; ++u) {
-    long long ns = std::max(1LL, (n_eff[u] + w / 2) / w);
-    while ((n_eff[u] + ns - 1) / ns > cmax) ++ns;
-    const long long chunk = (n_eff[u] + ns - 1) / ns;
-    ns = (n_eff[u] + chunk - 1) / chunk;
-    order[u] = {static_cast<int>(chunk), u};
-    nsplit[u] = static_cast<int>(ns);
-  }
-  std::stable_sort(order.begin(), order.end(),
-                   [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; });
-  long long items = 0;
-  int max_chunk = 0;
-  plan.prefix[0] = 0;
-  for (int i = 0; i < n_units; ++i) {
-    const int u = order[i].second;
-    items += static_cast<long long>(h->H) * nsplit[u];
-    if (items >= (1LL << 31)) return set_err(h, KVC_E_UNSUPPORTED, "too many work items");
-    plan.prefix[i + 1] = static_cast<int32_t>(items);
-    plan.unit_b[i] = u;
-    max_chunk = std::max(max_chunk, order[i].first);
-  }
-  plan.n_units = n_units;
-  plan.n_items = static_cast<int>(items);
-  plan.rows_per_tile = rpt;
-  plan.n_rowtiles = n_rt;
-  plan.split_keys = max_chunk;
+  kvc::AttnPlan ap{};
+  std::string perr;
+  const int prc = kvc::plan_attention(h, T, H_q, &plan, &ap, &perr);
+  if (prc) return set_err(h, prc, "%s", perr.c_str());
+  const int G = H_q / h->H;
+  const int rpt = ap.rows_per_tile;
 
   // ---- scratch from the fixed array: [counters | partial o | partial (m, l)] ------------------
-  const size_t counter_bytes = (static_cast<size_t>(n_units) * h->H * sizeof(int) + 255) / 256 * 256;
-  const size_t part_bytes = kvc::splitk_workspace_floats(plan, h->D) * sizeof(float);
+  const size_t counter_bytes = (ap.counters * sizeof(int) + 255) / 256 * 256;
+  const size_t part_bytes = ap.workspace_floats * sizeof(float);
   if (counter_bytes + part_bytes > kNoallocScratchBytes)
     return set_err(h, KVC_E_UNSUPPORTED, "this call needs %zu bytes of scratch; the fixed array holds %zu",
                    counter_bytes + part_bytes, kNoallocScratchBytes);
@@ -165,8 +113,11 @@ extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_
   int rc = scratch_address(&base, &err);
   if (rc) return set_err(h, rc, "%s", err.c_str());
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(base, 0, counter_bytes, st);
-  if (e != cudaSuccess) return set_err(h, KVC_E_CUDA, "clearing the merge counters: %s", cudaGetErrorString(e));
+  cudaError_t e = cudaSuccess;
+  if (counter_bytes) {
+    e = cudaMemsetAsync(base, 0, counter_bytes, st);
+    if (e != cudaSuccess) return set_err(h, KVC_E_CUDA, "clearing the merge counters: %s", cudaGetErrorString(e));
+  }
 
   kvc::AttnArgs a{};
   a.q = q; a.q_dtype = q_dtype; a.out = out;
@@ -176,8 +127,7 @@ extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_
   a.lens = h->d_lens; a.status = h->d_status;
   a.layer = layer; a.B = h->B; a.H_kv = h->H; a.H_q = H_q; a.G = G; a.T = T; a.D = h->D;
   a.max_len = h->max_len; a.delta = T; a.cache_dtype = h->dtype;
-  e = use_tc ? kvc::launch_decode_tc(a, plan, &h->tmap_k_tc, &h->tmap_v_tc, st)
-             : kvc::launch_splitk(a, plan, &h->tmap_k_split, &h->tmap_v_split, st);
+  e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return set_err(h, KVC_E_CUDA, "attention launch: %s", cudaGetErrorString(e));
   h->launches += 1;
   return KVC_OK;

@@ -1,0 +1,397 @@
+// Chunk (prefill) attention over the KV cache on the 5th-generation tensor cores (tcgen05 + TMEM),
+// for 16-bit caches with d_h = 128 and many query rows per K/V head (G * T > 32).
+//
+// What it computes ("KV cache, incremental decode, ...", §2.3 and §4 test_chunked_prefill_equals_whole;
+// "KV cache decoding", "Prefill and decode"; "Heads, GQA and K/V cache"): query row (t, h) of a chunk
+// at positions s_b .. s_b + T - 1 attends over stored keys j <= s_b + t.
+//
+// How: the G query heads of one K/V head and 128 / G consecutive chunk positions form a tile of 128
+// query rows (rows r = t * G + g), the M dimension; 128-key tiles are N:
+//   S  [128 rows x 128 keys] = Q . K_j^T        A = Q (K-major), B = K tile (K-major)
+//   Ot [128 rows x 128 d   ] = P_j . V_j        A = P (K-major, shared memory), B = V tile (MN-major)
+// One CTA per (sequence, K/V head, row tile), one CTA per SM (all 512 TMEM columns):
+//   warp 0     TMA: K_j and V_j tiles through a ring;
+//   warp 1     owns TMEM, issues QK(j + 1) before PV(j) so the tensor cores run ahead of the softmax;
+//   warps 2-5  one thread per query row: online softmax in base 2 (row max, rescale, exp2, sum),
+//              P to shared memory (f16; for bf16 a hi + lo pair, so P keeps ~2^-16 relative
+//              accuracy), and the output accumulated in 128 registers per row: each tile's P_j V_j
+//              is read from its own TMEM buffer one tile later and added with the factor
+//              2^(m_j - m_current), so no rescale of TMEM is needed.
+// Tiles of keys past a row tile's last visible key are skipped; the diagonal tiles are masked per
+// row. Every wait is bounded (~1 s) and reported through the device status word.
+#include "kvc_device.cuh"
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+using namespace dev;
+
+constexpr int kRows = 128;                   // query rows per CTA (MMA M)
+constexpr int kKeys = 128;                   // keys per tile (MMA N of QK, K of PV)
+constexpr int kDh = 128;
+constexpr int kBox = 128 * 128;              // one 128-byte-swizzled atom column of 128 rows (16 KB)
+constexpr int kTile = 2 * kBox;              // 32 KB: 128 rows x 128 16-bit values
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kTmemCols = 512;
+
+template <typename Tc>
+struct PLayout {
+  static constexpr bool kHiLo = std::is_same<Tc, __nv_bfloat16>::value;
+  static constexpr int kParts = kHiLo ? 2 : 1;
+  static constexpr int kStages = kHiLo ? 3 : 4;             // K/V ring (each stage one 32 KB tile)
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = kQOff + kTile;
+  static constexpr int kPOff = kRingOff + kStages * kTile;
+  static constexpr int kCtlOff = kPOff + kParts * kTile;
+};
+
+struct __align__(8) PCtl {
+  unsigned long long full[4], empty[4];
+  unsigned long long s_full[2], s_free[2], o_full[2], o_free[2];
+  unsigned long long p_full, p_free, done;
+  uint32_t tmem;
+  int abort;
+};
+
+template <typename Tc>
+constexpr size_t prefill_smem() { return 1024 + PLayout<Tc>::kCtlOff + sizeof(PCtl); }
+
+// offset of 16-byte chunk `c` (0..15) of row `r` in a [128 rows][128 16-bit] swizzled tile
+__device__ __forceinline__ uint32_t chunk_off(int r, int c) {
+  return (c >> 3) * kBox + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = now_ns();
+  while (!mbar_try(bar, parity)) {
+    if (now_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <typename Tc>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  const Tc x = from_f32<Tc>(a), y = from_f32<Tc>(b);
+  uint16_t ux, uy;
+  if constexpr (std::is_same<Tc, __half>::value) { ux = __half_as_ushort(x); uy = __half_as_ushort(y); }
+  else { ux = __bfloat16_as_ushort(x); uy = __bfloat16_as_ushort(y); }
+  return static_cast<uint32_t>(ux) | (static_cast<uint32_t>(uy) << 16);
+}
+
+template <typename Tc>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
+                  const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+  using Lo = PLayout<Tc>;
+  constexpr int kStages = Lo::kStages;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PCtl* ctl = reinterpret_cast<PCtl*>(sm + Lo::kCtlOff);
+  const uint32_t s_q = smem_u32(sm + Lo::kQOff);
+  const uint32_t s_ring = smem_u32(sm + Lo::kRingOff);
+  unsigned char* p_base = sm + Lo::kPOff;
+  const uint32_t s_p = smem_u32(p_base);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr uint32_t kFmt = std::is_same<Tc, __nv_bfloat16>::value ? 1u : 0u;
+
+  // ---- work item: (unit = sequence x row tile, K/V head) -----------------------------------------
+  const int item = blockIdx.x;
+  const int unit = item / a.H_kv, kvh = item % a.H_kv;
+  const int b = plan.unit_b[unit] / plan.n_rowtiles;
+  const int rt = plan.unit_b[unit] % plan.n_rowtiles;
+  const int row0 = rt * kRows;
+  const int nrows = min(kRows, a.T * a.G - row0);
+  const int s_b = a.lens[b] + a.delta - a.T;
+  const int first_t = row0 / a.G, last_t = (row0 + nrows - 1) / a.G;
+  const int n_keys = s_b + last_t + 1;                       // keys visible to the tile's last row
+  const int nkt = (n_keys + kKeys - 1) / kKeys;
+  const int unmasked_keys = s_b + first_t + 1;               // keys visible to every row of the tile
+  const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
+
+  // ---- set-up ------------------------------------------------------------------------------------
+  if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&ctl->tmem));
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&ctl->s_full[s]), 1);
+      mbar_init(smem_u32(&ctl->s_free[s]), kSoftmaxThreads / 32);
+      mbar_init(smem_u32(&ctl->o_full[s]), 1);
+      mbar_init(smem_u32(&ctl->o_free[s]), kSoftmaxThreads / 32);
+    }
+    mbar_init(smem_u32(&ctl->p_full), kSoftmaxThreads / 32);
+    mbar_init(smem_u32(&ctl->p_free), 1);
+    mbar_init(smem_u32(&ctl->done), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  // Q tile: 128 rows x 128 d in the cache dtype, 128-byte swizzled (rows past the chunk are zero)
+  for (int i = tid; i < kRows * (kDh / 8); i += kThreads) {
+    const int r = i / (kDh / 8), c = i % (kDh / 8);
+    float x[8];
+    if (r < nrows) {
+      const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+      const long long base = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + c * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = load_query<Tc>(a.q, a.q_dtype, base + e);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = 0.f;
+    }
+    *reinterpret_cast<uint4*>(sm + Lo::kQOff + chunk_off(r, c)) =
+        make_uint4(pack2<Tc>(x[0], x[1]), pack2<Tc>(x[2], x[3]), pack2<Tc>(x[4], x[5]), pack2<Tc>(x[6], x[7]));
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+  volatile int* abort_flag = &ctl->abort;
+
+  if (warp == 0) {
+    // ---------------------------------- TMA producer: K0, V0, K1, V1, ... ---------------------------
+    if (lane == 0) {
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      int issued = 0;
+      for (int i = 0; i < 2 * nkt; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(smem_u32(&ctl->empty[st]), ((i / kStages) & 1) ^ 1, abort_flag)) break;
+        const uint32_t full = smem_u32(&ctl->full[st]);
+        mbar_expect_tx(full, kTile);
+        const uint32_t dst = s_ring + st * kTile;
+        const CUtensorMap* map = (i & 1) ? &tv : &tk;
+        const int y = (i >> 1) * kKeys;
+        tma_load_3d(dst, map, 0, y, plane, full);
+        tma_load_3d(dst + kBox, map, 64, y, plane, full);
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        mbar_drain(smem_u32(&ctl->full[i % kStages]), (i / kStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------- MMA issuer ------------------------------------------------
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc(kRows, kKeys, kFmt, 0, 0);
+      const uint32_t idesc_o = umma_idesc(kRows, kDh, kFmt, 0, 1);
+      bool ok = true;
+      auto issue_qk = [&](int j) -> bool {
+        const int i = 2 * j, st = i % kStages, sb = j & 1;
+        if (!mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag)) return false;
+        if (!mbar_wait(smem_u32(&ctl->s_free[sb]), ((j >> 1) & 1) ^ 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t kt = s_ring + st * kTile;
+#pragma unroll
+        for (int ks = 0; ks < kDh / 16; ++ks)
+          umma_f16(tmem + sb * kKeys,
+                   umma_desc(s_q + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128),
+                   umma_desc(kt + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128), idesc_s, ks > 0);
+        umma_commit(smem_u32(&ctl->empty[st]));
+        umma_commit(smem_u32(&ctl->s_full[sb]));
+        return true;
+      };
+      if (nkt > 0) ok = issue_qk(0);
+      for (int j = 0; j < nkt && ok; ++j) {
+        if (j + 1 < nkt) ok = issue_qk(j + 1);
+        if (!ok) break;
+        const int i = 2 * j + 1, st = i % kStages, ob = j & 1;
+        ok = mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag) &&
+             mbar_wait(smem_u32(&ctl->p_full), j & 1, abort_flag) &&
+             mbar_wait(smem_u32(&ctl->o_free[ob]), ((j >> 1) & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vt = s_ring + st * kTile;
+#pragma unroll
+        for (int part = 0; part < Lo::kParts; ++part)
+#pragma unroll
+          for (int ks = 0; ks < kKeys / 16; ++ks)
+            umma_f16(tmem + 2 * kKeys + ob * kDh,
+                     umma_desc(s_p + part * kTile + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128),
+                     umma_desc(vt + ks * 2048, kBox, 1024, kSwizzle128), idesc_o, (part | ks) != 0);
+        umma_commit(smem_u32(&ctl->empty[st]));
+        umma_commit(smem_u32(&ctl->p_free));
+        umma_commit(smem_u32(&ctl->o_full[ob]));
+      }
+      umma_commit(smem_u32(&ctl->done));
+      mbar_drain(smem_u32(&ctl->done), 0);
+    }
+  } else {
+    // ---------------------------------- softmax, accumulation, epilogue ---------------------------
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;                          // this thread's query row (TMEM lane)
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const bool row_ok = r < nrows;
+    const int t_row = row_ok ? (row0 + r) / a.G : 0;
+    const int last_key = s_b + t_row;                        // this row sees keys <= last_key
+    const float scale = kLog2e * rsqrtf(static_cast<float>(kDh));
+    float o[kDh];
+#pragma unroll
+    for (int i = 0; i < kDh; ++i) o[i] = 0.f;
+    float m_cur = -INFINITY, l = 0.f, m_prev_tile = -INFINITY;
+    bool ok = true;
+    for (int j = 0; j < nkt && ok; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait(smem_u32(&ctl->s_full[sb]), (j >> 1) & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const bool masked_tile = (j + 1) * kKeys > unmasked_keys;
+      const int key0 = j * kKeys;
+      // pass A: the row maximum of this tile
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKeys; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + sb * kKeys + c, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const bool vis = !masked_tile || key0 + c + e <= last_key;
+          tmax = fmaxf(tmax, vis ? v[e] * scale : -INFINITY);
+        }
+      }
+      const float m_new = fmaxf(m_cur, tmax);
+      const float alpha = (m_cur == -INFINITY) ? 0.f : exp2f(m_cur - m_new);
+      // pass B: P = 2^(s - m_new) into shared memory (after PV(j - 1) has read the previous P)
+      ok = mbar_wait(smem_u32(&ctl->p_free), (j & 1) ^ 1, abort_flag);
+      if (!ok) break;
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKeys; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + sb * kKeys + c, v);
+#pragma unroll
+        for (int e8 = 0; e8 < 32; e8 += 8) {
+          float p[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const bool vis = row_ok && (!masked_tile || key0 + c + e8 + e <= last_key);
+            p[e] = vis ? exp2f(v[e8 + e] * scale - m_new) : 0.f;
+            lsum += p[e];
+          }
+          const int chunk = (c + e8) >> 3;
+          *reinterpret_cast<uint4*>(p_base + chunk_off(r, chunk)) =
+              make_uint4(pack2<Tc>(p[0], p[1]), pack2<Tc>(p[2], p[3]), pack2<Tc>(p[4], p[5]), pack2<Tc>(p[6], p[7]));
+          if constexpr (Lo::kParts == 2) {
+            float lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) lo[e] = p[e] - to_f32<Tc>(from_f32<Tc>(p[e]));
+            *reinterpret_cast<uint4*>(p_base + kTile + chunk_off(r, chunk)) =
+                make_uint4(pack2<Tc>(lo[0], lo[1]), pack2<Tc>(lo[2], lo[3]), pack2<Tc>(lo[4], lo[5]), pack2<Tc>(lo[6], lo[7]));
+          }
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&ctl->s_free[sb]));
+        mbar_arrive(smem_u32(&ctl->p_full));
+      }
+      // the running state moves to m_new: the registers hold sum_{i < j - 1} P_i V_i at m_cur
+      l = l * alpha + lsum;
+#pragma unroll
+      for (int i = 0; i < kDh; ++i) o[i] *= alpha;
+      m_cur = m_new;
+      // add tile j - 1's P V (computed at m_prev_tile) now that its MMAs have had a tile's time
+      if (j > 0) {
+        const int ob = (j - 1) & 1;
+        ok = mbar_wait(smem_u32(&ctl->o_full[ob]), ((j - 1) >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const float f = exp2f(m_prev_tile - m_cur);
+#pragma unroll
+        for (int c = 0; c < kDh; c += 32) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + 2 * kKeys + ob * kDh + c, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[c + e] = fmaf(v[e], f, o[c + e]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->o_free[ob]));
+      }
+      m_prev_tile = m_new;
+    }
+    if (ok && nkt > 0) {
+      const int ob = (nkt - 1) & 1;
+      ok = mbar_wait(smem_u32(&ctl->o_full[ob]), ((nkt - 1) >> 1) & 1, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        const float f = exp2f(m_prev_tile - m_cur);
+#pragma unroll
+        for (int c = 0; c < kDh; c += 32) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + 2 * kKeys + ob * kDh + c, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[c + e] = fmaf(v[e], f, o[c + e]);
+        }
+      }
+    }
+    const bool aborted = *abort_flag != 0;
+    if (aborted) {
+      if (tid == 64) atomicExch(a.status, kStatusTimeout);
+    } else if (row_ok) {
+      const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+      float* dst = a.out + ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh;
+      const float inv = 1.f / l;
+#pragma unroll
+      for (int i = 0; i < kDh; i += 4)
+        *reinterpret_cast<float4*>(dst + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<kTmemCols>(tmem);
+  }
+}
+
+template <typename Tc>
+cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, const CUtensorMap* tv,
+                cudaStream_t st) {
+  auto kern = prefill_tc_kernel<Tc>;
+  const size_t smem = prefill_smem<Tc>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<p.n_units * a.H_kv, kThreads, smem, st>>>(a, p, *tk, *tv);
+  return cudaGetLastError();
+}
+
+static_assert(prefill_smem<__half>() > 114 * 1024 && prefill_smem<__nv_bfloat16>() > 114 * 1024,
+              "one CTA per SM: each holds all 512 TMEM columns");
+static_assert(prefill_smem<__half>() <= 227 * 1024 && prefill_smem<__nv_bfloat16>() <= 227 * 1024, "smem");
+
+}  // namespace
+
+bool prefill_tc_shape(kvc_dtype dt, int D, int* rows_per_tile) {
+  if ((dt != KVC_F16 && dt != KVC_BF16) || D != kDh) return false;
+  *rows_per_tile = kRows;
+  return true;
+}
+
+cudaError_t launch_prefill_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
+                              const CUtensorMap* tv, cudaStream_t st) {
+  return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16>(a, p, tk, tv, st) : run<__half>(a, p, tk, tv, st);
+}
+
+}  // namespace kvc

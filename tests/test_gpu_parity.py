@@ -108,6 +108,11 @@ CASES = [
     ("f32", 32, 4, 2, 17, [0, 40]),
     ("bf16", 32, 4, 1, 64, [0, 100]),
     ("f16", 64, 4, 4, 129, [1, 200]),
+    # chunks of more than 32 query rows per K/V head on the tensor-core chunk kernel
+    ("bf16", 128, 32, 8, 9, [0, 300]),         # 36 rows: one partial row tile
+    ("f16", 128, 32, 8, 64, [5, 700]),         # 256 rows: two full row tiles
+    ("bf16", 128, 16, 2, 17, [130, 0, 3]),     # G = 8, 136 rows: a ragged last tile
+    ("f16", 128, 8, 8, 200, [0, 129]),         # G = 1, 200 rows, diagonal masking over many tiles
 ]
 
 
