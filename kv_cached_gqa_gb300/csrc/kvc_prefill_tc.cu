@@ -12,11 +12,13 @@
 // One CTA per (sequence, K/V head, row tile), one CTA per SM (all 512 TMEM columns):
 //   warp 0     TMA: K_j and V_j tiles through a ring;
 //   warp 1     owns TMEM, issues QK(j + 1) before PV(j) so the tensor cores run ahead of the softmax;
-//   warps 2-5  one thread per query row: online softmax in base 2 (row max, rescale, exp2, sum),
-//              P to shared memory (f16; for bf16 a hi + lo pair, so P keeps ~2^-16 relative
-//              accuracy), and the output accumulated in 128 registers per row: each tile's P_j V_j
-//              is read from its own TMEM buffer one tile later and added with the factor
-//              2^(m_j - m_current), so no rescale of TMEM is needed.
+//   warps 2-5  one thread per query row: online softmax in base 2 against a per-row reference
+//              maximum m_ref; P = 2^(s - m_ref) goes to shared memory (f16; for bf16 a hi + lo pair,
+//              so P keeps ~2^-16 relative accuracy). The output accumulates in TMEM across tiles;
+//              it is rescaled (read, multiply, write back) only when a row's maximum passes
+//              m_ref + 8, which keeps P <= 2^8 and happens only on the first tiles of a row in
+//              practice. The final division by the row sum uses the same reference, so the result
+//              is the plain softmax.
 // Tiles of keys past a row tile's last visible key are skipped; the diagonal tiles are masked per
 // row. Every wait is bounded (~1 s) and reported through the device status word.
 #include "kvc_device.cuh"
@@ -49,8 +51,8 @@ struct PLayout {
 
 struct __align__(8) PCtl {
   unsigned long long full[4], empty[4];
-  unsigned long long s_full[2], s_free[2], o_full[2], o_free[2];
-  unsigned long long p_full, p_free, done;
+  unsigned long long s_full[2], s_free[2];
+  unsigned long long p_full, p_free, o_full, done;
   uint32_t tmem;
   int abort;
 };
@@ -85,13 +87,40 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      :: "r"(taddr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+         "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]),
+         "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]),
+         "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22), flushing subnormal results to zero
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// two floats -> one 32-bit word of two 16-bit values (round to nearest even), in one conversion
 template <typename Tc>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
-  const Tc x = from_f32<Tc>(a), y = from_f32<Tc>(b);
-  uint16_t ux, uy;
-  if constexpr (std::is_same<Tc, __half>::value) { ux = __half_as_ushort(x); uy = __half_as_ushort(y); }
-  else { ux = __bfloat16_as_ushort(x); uy = __bfloat16_as_ushort(y); }
-  return static_cast<uint32_t>(ux) | (static_cast<uint32_t>(uy) << 16);
+  if constexpr (std::is_same<Tc, __half>::value) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+// the two floats a packed word stands for
+template <typename Tc>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (std::is_same<Tc, __half>::value) return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  else return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 template <typename Tc>
@@ -135,11 +164,10 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&ctl->s_full[s]), 1);
       mbar_init(smem_u32(&ctl->s_free[s]), kSoftmaxThreads / 32);
-      mbar_init(smem_u32(&ctl->o_full[s]), 1);
-      mbar_init(smem_u32(&ctl->o_free[s]), kSoftmaxThreads / 32);
     }
     mbar_init(smem_u32(&ctl->p_full), kSoftmaxThreads / 32);
     mbar_init(smem_u32(&ctl->p_free), 1);
+    mbar_init(smem_u32(&ctl->o_full), 1);
     mbar_init(smem_u32(&ctl->done), 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -147,18 +175,19 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   // Q tile: 128 rows x 128 d in the cache dtype, 128-byte swizzled (rows past the chunk are zero)
   for (int i = tid; i < kRows * (kDh / 8); i += kThreads) {
     const int r = i / (kDh / 8), c = i % (kDh / 8);
-    float x[8];
+    uint4 w = make_uint4(0, 0, 0, 0);
     if (r < nrows) {
       const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
       const long long base = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + c * 8;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = load_query<Tc>(a.q, a.q_dtype, base + e);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      if (a.q_dtype == KVC_F32) {
+        const float4 x0 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + base);
+        const float4 x1 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + base + 4);
+        w = make_uint4(pack2<Tc>(x0.x, x0.y), pack2<Tc>(x0.z, x0.w), pack2<Tc>(x1.x, x1.y), pack2<Tc>(x1.z, x1.w));
+      } else {
+        w = *reinterpret_cast<const uint4*>(static_cast<const Tc*>(a.q) + base);
+      }
     }
-    *reinterpret_cast<uint4*>(sm + Lo::kQOff + chunk_off(r, c)) =
-        make_uint4(pack2<Tc>(x[0], x[1]), pack2<Tc>(x[2], x[3]), pack2<Tc>(x[4], x[5]), pack2<Tc>(x[6], x[7]));
+    *reinterpret_cast<uint4*>(sm + Lo::kQOff + chunk_off(r, c)) = w;
   }
   fence_proxy_async();
   tc_fence_before();
@@ -213,10 +242,9 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       for (int j = 0; j < nkt && ok; ++j) {
         if (j + 1 < nkt) ok = issue_qk(j + 1);
         if (!ok) break;
-        const int i = 2 * j + 1, st = i % kStages, ob = j & 1;
+        const int i = 2 * j + 1, st = i % kStages;
         ok = mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag) &&
-             mbar_wait(smem_u32(&ctl->p_full), j & 1, abort_flag) &&
-             mbar_wait(smem_u32(&ctl->o_free[ob]), ((j >> 1) & 1) ^ 1, abort_flag);
+             mbar_wait(smem_u32(&ctl->p_full), j & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vt = s_ring + st * kTile;
@@ -224,137 +252,127 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
         for (int part = 0; part < Lo::kParts; ++part)
 #pragma unroll
           for (int ks = 0; ks < kKeys / 16; ++ks)
-            umma_f16(tmem + 2 * kKeys + ob * kDh,
+            umma_f16(tmem + 2 * kKeys,
                      umma_desc(s_p + part * kTile + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128),
-                     umma_desc(vt + ks * 2048, kBox, 1024, kSwizzle128), idesc_o, (part | ks) != 0);
+                     umma_desc(vt + ks * 2048, kBox, 1024, kSwizzle128), idesc_o, (j | part | ks) != 0);
         umma_commit(smem_u32(&ctl->empty[st]));
         umma_commit(smem_u32(&ctl->p_free));
-        umma_commit(smem_u32(&ctl->o_full[ob]));
       }
+      if (ok) umma_commit(smem_u32(&ctl->o_full));
       umma_commit(smem_u32(&ctl->done));
       mbar_drain(smem_u32(&ctl->done), 0);
     }
   } else {
-    // ---------------------------------- softmax, accumulation, epilogue ---------------------------
+    // ---------------------------------- softmax and epilogue ---------------------------------------
     const int quad = warp & 3;
     const int r = quad * 32 + lane;                          // this thread's query row (TMEM lane)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tmem_o = tmem + lane_base + 2 * kKeys;
     const bool row_ok = r < nrows;
     const int t_row = row_ok ? (row0 + r) / a.G : 0;
     const int last_key = s_b + t_row;                        // this row sees keys <= last_key
     const float scale = kLog2e * rsqrtf(static_cast<float>(kDh));
-    float o[kDh];
-#pragma unroll
-    for (int i = 0; i < kDh; ++i) o[i] = 0.f;
-    float m_cur = -INFINITY, l = 0.f, m_prev_tile = -INFINITY;
+    constexpr float kSlack = 8.f;                            // P <= 2^kSlack before a rescale is forced
+    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkt && ok; ++j) {
       const int sb = j & 1;
       ok = mbar_wait(smem_u32(&ctl->s_full[sb]), (j >> 1) & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      const bool masked_tile = (j + 1) * kKeys > unmasked_keys;
+      float v[kKeys];
+#pragma unroll
+      for (int c = 0; c < kKeys; c += 32) tmem_ld32(tmem + lane_base + sb * kKeys + c, v + c);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free[sb]));  // S buffer may be overwritten now
       const int key0 = j * kKeys;
-      // pass A: the row maximum of this tile
-      float tmax = -INFINITY;
+      if ((j + 1) * kKeys > unmasked_keys || !row_ok) {        // diagonal tile (or padding row)
 #pragma unroll
-      for (int c = 0; c < kKeys; c += 32) {
-        float v[32];
-        tmem_ld32(tmem + lane_base + sb * kKeys + c, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const bool vis = !masked_tile || key0 + c + e <= last_key;
-          tmax = fmaxf(tmax, vis ? v[e] * scale : -INFINITY);
-        }
+        for (int e = 0; e < kKeys; ++e)
+          if (!row_ok || key0 + e > last_key) v[e] = -INFINITY;
       }
-      const float m_new = fmaxf(m_cur, tmax);
-      const float alpha = (m_cur == -INFINITY) ? 0.f : exp2f(m_cur - m_new);
-      // pass B: P = 2^(s - m_new) into shared memory (after PV(j - 1) has read the previous P)
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = v[k];
+#pragma unroll
+      for (int e = 8; e < kKeys; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
+      const float tmax = scale * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // a new reference when this row's maximum passes the old one by more than kSlack
+      const bool bump = tmax > m_ref + kSlack;
+      const float m_new = bump ? tmax : m_ref;
+      const float alpha = bump ? ((m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new)) : 1.f;
+      // the previous tile's PV must be done before P is overwritten or the output rescaled
       ok = mbar_wait(smem_u32(&ctl->p_free), (j & 1) ^ 1, abort_flag);
       if (!ok) break;
-      float lsum = 0.f;
+      if (j > 0 && __any_sync(0xffffffffu, bump)) {
+        tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kKeys; c += 32) {
-        float v[32];
-        tmem_ld32(tmem + lane_base + sb * kKeys + c, v);
+        for (int c = 0; c < kDh; c += 32) {
+          float ov[32];
+          tmem_ld32(tmem_o + c, ov);
 #pragma unroll
-        for (int e8 = 0; e8 < 32; e8 += 8) {
-          float p[8];
+          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+          tmem_st32(tmem_o + c, ov);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+      l *= alpha;
+      m_ref = m_new;
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;   // padding rows: every score is -inf
+      float ls[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const bool vis = row_ok && (!masked_tile || key0 + c + e8 + e <= last_key);
-            p[e] = vis ? exp2f(v[e8 + e] * scale - m_new) : 0.f;
-            lsum += p[e];
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < kKeys / 8; ++c8) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = fast_exp2(fmaf(v[c8 * 8 + e], scale, neg_m));  // 0 for masked keys (-inf)
+          ls[e] += p[e];
+        }
+        const uint4 w = make_uint4(pack2<Tc>(p[0], p[1]), pack2<Tc>(p[2], p[3]), pack2<Tc>(p[4], p[5]),
+                                   pack2<Tc>(p[6], p[7]));
+        *reinterpret_cast<uint4*>(p_base + chunk_off(r, c8)) = w;
+        if constexpr (Lo::kParts == 2) {
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          uint32_t lo[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 h = unpack2<Tc>(ww[k]);
+            lo[k] = pack2<Tc>(p[2 * k] - h.x, p[2 * k + 1] - h.y);
           }
-          const int chunk = (c + e8) >> 3;
-          *reinterpret_cast<uint4*>(p_base + chunk_off(r, chunk)) =
-              make_uint4(pack2<Tc>(p[0], p[1]), pack2<Tc>(p[2], p[3]), pack2<Tc>(p[4], p[5]), pack2<Tc>(p[6], p[7]));
-          if constexpr (Lo::kParts == 2) {
-            float lo[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) lo[e] = p[e] - to_f32<Tc>(from_f32<Tc>(p[e]));
-            *reinterpret_cast<uint4*>(p_base + kTile + chunk_off(r, chunk)) =
-                make_uint4(pack2<Tc>(lo[0], lo[1]), pack2<Tc>(lo[2], lo[3]), pack2<Tc>(lo[4], lo[5]), pack2<Tc>(lo[6], lo[7]));
-          }
+          *reinterpret_cast<uint4*>(p_base + kTile + chunk_off(r, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tc_fence_before();
       fence_proxy_async();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&ctl->s_free[sb]));
-        mbar_arrive(smem_u32(&ctl->p_full));
-      }
-      // the running state moves to m_new: the registers hold sum_{i < j - 1} P_i V_i at m_cur
-      l = l * alpha + lsum;
-#pragma unroll
-      for (int i = 0; i < kDh; ++i) o[i] *= alpha;
-      m_cur = m_new;
-      // add tile j - 1's P V (computed at m_prev_tile) now that its MMAs have had a tile's time
-      if (j > 0) {
-        const int ob = (j - 1) & 1;
-        ok = mbar_wait(smem_u32(&ctl->o_full[ob]), ((j - 1) >> 1) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const float f = exp2f(m_prev_tile - m_cur);
-#pragma unroll
-        for (int c = 0; c < kDh; c += 32) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + 2 * kKeys + ob * kDh + c, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[c + e] = fmaf(v[e], f, o[c + e]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->o_free[ob]));
-      }
-      m_prev_tile = m_new;
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
     }
-    if (ok && nkt > 0) {
-      const int ob = (nkt - 1) & 1;
-      ok = mbar_wait(smem_u32(&ctl->o_full[ob]), ((nkt - 1) >> 1) & 1, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        const float f = exp2f(m_prev_tile - m_cur);
-#pragma unroll
-        for (int c = 0; c < kDh; c += 32) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + 2 * kKeys + ob * kDh + c, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[c + e] = fmaf(v[e], f, o[c + e]);
-        }
-      }
-    }
+    // ---- epilogue: O / l ---------------------------------------------------------------------------
+    ok = ok && mbar_wait(smem_u32(&ctl->o_full), 0, abort_flag);
+    tc_fence_after();
     const bool aborted = *abort_flag != 0;
     if (aborted) {
       if (tid == 64) atomicExch(a.status, kStatusTimeout);
-    } else if (row_ok) {
+    } else {
       const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-      float* dst = a.out + ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh;
+      float* dst = row_ok ? a.out + ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh : nullptr;
       const float inv = 1.f / l;
 #pragma unroll
-      for (int i = 0; i < kDh; i += 4)
-        *reinterpret_cast<float4*>(dst + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+      for (int c = 0; c < kDh; c += 32) {
+        float ov[32];
+        tmem_ld32(tmem_o + c, ov);                             // warp-wide: every lane takes part
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + c + i) =
+                make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
+        }
+      }
     }
   }
 
