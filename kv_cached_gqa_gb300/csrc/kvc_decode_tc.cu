@@ -1,13 +1,12 @@
 // Grouped-query attention over the KV cache on the 5th-generation tensor cores (tcgen05 + TMEM),
-// for 16-bit caches with d_h = 128 and up to 32 query rows per K/V head (decode T = 1 and short
-// verify chunks).
+// for 16-bit caches with d_h = 128 and up to 16 query rows per K/V head (decode).
 //
 // What it computes ("KV cache, incremental decode, ...", §2.3; "Generation and the KV Cache",
 // fence 3; "Heads, GQA and K/V cache", "Four queries, two sets of K/V"): for sequence b and K/V
 // head g, each query row (t, h) of the group h = g*G .. g*G+G-1 attends over stored keys
 // j <= s_b + t: softmax_j(q . k_j / sqrt(d_h)) weighted sum of v_j.
 //
-// How: the group's query rows are the N dimension of the MMAs (N = 16 or 32, padded with zero
+// How: the group's query rows are the N dimension of the MMAs (N = 16, padded with zero
 // rows) and the keys are the M dimension (128 per tile), so one K/V tile read from HBM serves every
 // query head of the group and nothing is repeated per head.
 //   S^T [128 keys x N] = K_tile . Q^T       A = K tile (K-major, TMA 128-byte swizzle), B = Q^T
@@ -400,19 +399,20 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
 
 }  // namespace
 
+// Up to 16 query rows per K/V head (decode, G * T <= 16); longer chunks run on the chunk kernel,
+// which measured faster from 32 rows on.
 bool decode_tc_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys, int* max_tiles) {
-  if ((dt != KVC_F16 && dt != KVC_BF16) || D != kDh) return false;
-  *rows_per_tile = rows <= 16 ? 16 : 32;
+  if ((dt != KVC_F16 && dt != KVC_BF16) || D != kDh || rows > 16) return false;
+  *rows_per_tile = 16;
   *tile_keys = kTK;
-  *max_tiles = *rows_per_tile == 16 ? Layout<16>::kSTiles : Layout<32>::kSTiles;
+  *max_tiles = Layout<16>::kSTiles;
   return true;
 }
 
 cudaError_t launch_decode_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
                              const CUtensorMap* tv, cudaStream_t st) {
-  if (a.cache_dtype == KVC_BF16)
-    return p.rows_per_tile == 16 ? run<__nv_bfloat16, 16>(a, p, tk, tv, st) : run<__nv_bfloat16, 32>(a, p, tk, tv, st);
-  return p.rows_per_tile == 16 ? run<__half, 16>(a, p, tk, tv, st) : run<__half, 32>(a, p, tk, tv, st);
+  if (p.rows_per_tile != 16) return cudaErrorInvalidValue;
+  return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16>(a, p, tk, tv, st) : run<__half, 16>(a, p, tk, tv, st);
 }
 
 }  // namespace kvc

@@ -179,8 +179,8 @@ bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max
 }
 
 // ---- kernel choice and work plan ------------------------------------------------------------------
-// Tensor cores serve 16-bit caches with d_h = 128: the decode kernel for up to 32 query rows per K/V
-// head (decode and verify chunks), the chunk kernel beyond that (prefill). Everything else runs on
+// Tensor cores serve 16-bit caches with d_h = 128: the split decode kernel for up to 16 query rows
+// per K/V head, the chunk kernel beyond that (verify chunks and prefill). Everything else runs on
 // the CUDA-core split-K kernel. For the split kernels, the total key work W = H_kv * sum_u n_u (n_u =
 // keys visible to unit u) is cut into about k waves of resident CTAs (two per SM); each unit's keys
 // are split into near-equal chunks of about W / (k * slots) keys, at most what one CTA can hold, and
@@ -190,9 +190,9 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
   const int R = T * G;
   int rpt = 0, tile = 0, max_tiles = 0;
   AttnKernel kind;
-  if (h->has_tc && R <= 32 && decode_tc_shape(h->dtype, h->D, R, &rpt, &tile, &max_tiles)) {
+  if (h->has_tc && decode_tc_shape(h->dtype, h->D, R, &rpt, &tile, &max_tiles)) {
     kind = AttnKernel::DecodeTC;
-  } else if (h->has_tc && R > 32 && prefill_tc_shape(h->dtype, h->D, &rpt)) {
+  } else if (h->has_tc && R > 16 && prefill_tc_shape(h->dtype, h->D, &rpt)) {
     kind = AttnKernel::PrefillTC;
   } else {
     if (!splitk_shape(h->dtype, h->D, R, &rpt, &tile)) {

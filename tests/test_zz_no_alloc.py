@@ -54,14 +54,14 @@ def test_noalloc_matches_regular_entry_point_twice(gpu_lib, dtype, name, d, H_q,
 def test_noalloc_rejects_plans_beyond_the_fixed_array(gpu_lib):
     import torch
     from kv_cached_gqa_gb300 import _binding as kb
-    B, H_kv, d, T = 64, 8, 128, 32                           # 32 query rows x 4096 keys x 64 sequences
+    B, H_kv, H_q, d = 64, 8, 32, 128                         # 64 sequences of 4096 keys: ~12 MB of partials
     cache = kb.Cache(1, B, H_kv, d, 4200, 2)
     k = torch.zeros((B, H_kv, 4096, d), dtype=torch.bfloat16, device="cuda")
     kb.kvc_append(cache, 0, k, k)
     kb.kvc_commit(cache)
-    kb.kvc_append(cache, 0, k[:, :, :T].contiguous(), k[:, :, :T].contiguous())
-    q = torch.zeros((B, 8, T, d), dtype=torch.bfloat16, device="cuda")
-    out = torch.empty((B, 8, T, d), dtype=torch.float32, device="cuda")
+    kb.kvc_append(cache, 0, k[:, :, :1].contiguous(), k[:, :, :1].contiguous())
+    q = torch.zeros((B, H_q, 1, d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((B, H_q, 1, d), dtype=torch.float32, device="cuda")
     with pytest.raises(kb.KvcError) as ei:
         kb.gqa_cached_attn_noalloc(cache, q, 0, out)
     assert ei.value.code == -6 and "fixed array holds" in str(ei.value)
