@@ -1,5 +1,5 @@
 // Grouped-query attention over the KV cache on the 5th-generation tensor cores (tcgen05 + TMEM),
-// for 16-bit caches with d_h = 128 and up to 16 query rows per K/V head (decode).
+// for 16-bit caches with d_h = 64 or 128 and up to 16 query rows per K/V head (decode).
 //
 // What it computes ("KV cache, incremental decode, ...", §2.3; "Generation and the KV Cache",
 // fence 3; "Heads, GQA and K/V cache", "Four queries, two sets of K/V"): for sequence b and K/V
@@ -10,7 +10,7 @@
 // rows) and the keys are the M dimension (128 per tile), so one K/V tile read from HBM serves every
 // query head of the group and nothing is repeated per head.
 //   S^T [128 keys x N] = K_tile . Q^T       A = K tile (K-major, TMA 128-byte swizzle), B = Q^T
-//   O^T [128 d   x N] += V_tile^T . P^T     A = V tile read MN-major, B = P^T (K-major)
+//   O^T [d_h x N]     += V_tile^T . P^T     A = V tile read MN-major, B = P^T (K-major)
 // One CTA owns one (sequence, row tile, K/V head, key split). Roles:
 //   warp 0     TMA producer: the split's K tiles, then its V tiles, through a 2- or 3-stage ring;
 //   warp 1     owns TMEM (256 columns) and issues every MMA from one thread;
@@ -31,21 +31,21 @@ namespace {
 using namespace dev;
 
 constexpr int kTK = 128;                    // keys per tile = MMA M
-constexpr int kDh = 128;                    // head width = MMA K for QK, M for PV
-constexpr int kBoxBytes = kTK * 128;        // one 64-element (128-byte) swizzled column box
-constexpr int kTileBytes = 2 * kBoxBytes;   // 32 KB: a tile's K (or V) rows
+constexpr int kBoxBytes = kTK * 128;        // one 64-element (128-byte) swizzled column box of a tile
 constexpr int kTmemCols = 256;
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 
-// Shared memory per CTA stays under ~110 KB so that two CTAs share an SM: with 16 query rows the
-// K/V ring has 3 stages and one P^T buffer, with 32 rows 2 stages and two P^T buffers.
-template <int NR>
+// Shared memory per CTA stays under ~110 KB so that two CTAs share an SM: the K/V ring holds 96 KB
+// (3 tiles of 32 KB for d_h = 128, 6 of 16 KB for d_h = 64), plus Q^T and one P^T buffer (hi, lo).
+template <int NR, int DH>
 struct Layout {
-  static constexpr int kStages = NR == 16 ? 3 : 2;
-  static constexpr int kPBufs = NR == 16 ? 1 : 2;
-  static constexpr int kQBytes = NR * 256;                      // Q^T: two atoms of NR rows x 128 B
-  static constexpr int kPBytes = NR * 256;                      // one P^T operand (hi or lo)
+  static constexpr int kBoxes = DH / 64;                        // 64-element boxes per key row
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;         // a tile's K (or V) rows
+  static constexpr int kStages = 96 * 1024 / kTileBytes;
+  static constexpr int kPBufs = 1;
+  static constexpr int kQBytes = NR * DH * 2;                   // Q^T: atoms of NR rows x 128 B
+  static constexpr int kPBytes = NR * 256;                      // one P^T operand (hi or lo): 128 keys
   static constexpr int kStageOff = 0;
   static constexpr int kQOff = kStages * kTileBytes;
   static constexpr int kPOff = kQOff + kQBytes;                 // kPBufs buffers x (hi, lo)
@@ -53,11 +53,11 @@ struct Layout {
   static constexpr int kSTiles = (kTmemCols - NR) / NR;         // S^T tiles that fit beside O^T
 };
 
-template <int NR>
+template <int NR, int DH>
 struct __align__(8) Ctl {
-  unsigned long long full[Layout<NR>::kStages], empty[Layout<NR>::kStages];
-  unsigned long long p_full[Layout<NR>::kPBufs], p_empty[Layout<NR>::kPBufs];
-  unsigned long long s_ready[Layout<NR>::kSTiles];             // one per K tile, used once
+  unsigned long long full[Layout<NR, DH>::kStages], empty[Layout<NR, DH>::kStages];
+  unsigned long long p_full[Layout<NR, DH>::kPBufs], p_empty[Layout<NR, DH>::kPBufs];
+  unsigned long long s_ready[Layout<NR, DH>::kSTiles];         // one per K tile, used once
   unsigned long long o_full, done;
   uint32_t tmem;
   int abort, last;
@@ -67,10 +67,10 @@ struct __align__(8) Ctl {
 
 // Dynamic shared memory per CTA. At least 80 KB, so that no more than two CTAs are ever resident on
 // an SM: each holds 256 of the SM's 512 TMEM columns, and a third could wait forever on tcgen05.alloc.
-template <int NR>
+template <int NR, int DH>
 constexpr size_t smem_bytes() {
-  return (1024 + Layout<NR>::kCtlOff + sizeof(Ctl<NR>)) > 80 * 1024 ? (1024 + Layout<NR>::kCtlOff + sizeof(Ctl<NR>))
-                                                                     : 80 * 1024;
+  return (1024 + Layout<NR, DH>::kCtlOff + sizeof(Ctl<NR, DH>)) > 80 * 1024
+             ? (1024 + Layout<NR, DH>::kCtlOff + sizeof(Ctl<NR, DH>)) : 80 * 1024;
 }
 static_assert(3 * 80 * 1024 > 228 * 1024, "three CTAs must not fit on one SM");
 
@@ -89,16 +89,16 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <typename Tc, int NR>
+template <typename Tc, int NR, int DH>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
                  const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
-  using Lo = Layout<NR>;
-  constexpr int kStages = Lo::kStages, kPBufs = Lo::kPBufs;
+  using Lo = Layout<NR, DH>;
+  constexpr int kStages = Lo::kStages, kPBufs = Lo::kPBufs, kDh = DH, kTileBytes = Lo::kTileBytes;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctl<NR>* ctl = reinterpret_cast<Ctl<NR>*>(sm + Lo::kCtlOff);
+  Ctl<NR, DH>* ctl = reinterpret_cast<Ctl<NR, DH>*>(sm + Lo::kCtlOff);
   const uint32_t s_stage = smem_u32(sm + Lo::kStageOff);
   const uint32_t s_q = smem_u32(sm + Lo::kQOff);
   unsigned char* p_base = sm + Lo::kPOff;
@@ -179,8 +179,9 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
         const uint32_t full = smem_u32(&ctl->full[st]);
         mbar_expect_tx(full, kTileBytes);
         const uint32_t dst = s_stage + st * kTileBytes;
-        tma_load_3d(dst, isv ? &tv : &tk, 0, y, plane, full);
-        tma_load_3d(dst + kBoxBytes, isv ? &tv : &tk, 64, y, plane, full);
+#pragma unroll
+        for (int bx = 0; bx < Lo::kBoxes; ++bx)
+          tma_load_3d(dst + bx * kBoxBytes, isv ? &tv : &tk, 64 * bx, y, plane, full);
         issued = i + 1;
       }
       // drain: the last copy issued into each stage has landed before the CTA can exit
@@ -326,9 +327,12 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
 #pragma unroll
     for (int c = 0; c < NR; c += 16) tmem_ld16(tmem_o + lane_base + c, o + c);
     const bool aborted = *abort_flag != 0;
-    const int d = kslot;
+    // O^T row d sits in TMEM lane d for M = 128; for M = 64 in lane 32 * (d / 16) + d % 16, i.e. the
+    // lower 16 lanes of each warp's quadrant
+    const bool d_ok = DH == 128 || lane < 16;
+    const int d = DH == 128 ? kslot : quad * 16 + (lane & 15);
     const long long item_row0 = static_cast<long long>(item) * NR;
-    if (!aborted) {
+    if (!aborted && d_ok) {
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
         if (r < nrows) {
@@ -357,7 +361,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       if (ctl->last) {
         __threadfence();
         const long long first_row = static_cast<long long>(plan.prefix[unit] + kvh * nsplit) * NR;
-        for (int r = 0; r < nrows; ++r) {
+        for (int r = 0; r < nrows && d_ok; ++r) {
           float m = -INFINITY, l = 0.f, acc = 0.f;
           for (int s = 0; s < nsplit; ++s) {
             const long long row = first_row + static_cast<long long>(s) * NR + r;
@@ -370,7 +374,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
             m = mn;
           }
           const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-          if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l;
+          if (!aborted && d_ok) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l;
         }
         if (tid == 64) *counter = 0;
       }
@@ -386,11 +390,11 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   }
 }
 
-template <typename Tc, int NR>
+template <typename Tc, int NR, int DH>
 cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, const CUtensorMap* tv,
                 cudaStream_t st) {
-  auto kern = decode_tc_kernel<Tc, NR>;
-  const size_t smem = smem_bytes<NR>();
+  auto kern = decode_tc_kernel<Tc, NR, DH>;
+  const size_t smem = smem_bytes<NR, DH>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   kern<<<p.n_items, kThreads, smem, st>>>(a, p, *tk, *tv);
@@ -402,17 +406,19 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
 // Up to 16 query rows per K/V head (decode, G * T <= 16); longer chunks run on the chunk kernel,
 // which measured faster from 32 rows on.
 bool decode_tc_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys, int* max_tiles) {
-  if ((dt != KVC_F16 && dt != KVC_BF16) || D != kDh || rows > 16) return false;
+  if ((dt != KVC_F16 && dt != KVC_BF16) || (D != 64 && D != 128) || rows > 16) return false;
   *rows_per_tile = 16;
   *tile_keys = kTK;
-  *max_tiles = Layout<16>::kSTiles;
+  *max_tiles = Layout<16, 128>::kSTiles;
   return true;
 }
 
 cudaError_t launch_decode_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
                              const CUtensorMap* tv, cudaStream_t st) {
   if (p.rows_per_tile != 16) return cudaErrorInvalidValue;
-  return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16>(a, p, tk, tv, st) : run<__half, 16>(a, p, tk, tv, st);
+  if (a.D == 128)
+    return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16, 128>(a, p, tk, tv, st) : run<__half, 16, 128>(a, p, tk, tv, st);
+  return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16, 64>(a, p, tk, tv, st) : run<__half, 16, 64>(a, p, tk, tv, st);
 }
 
 }  // namespace kvc
