@@ -43,6 +43,8 @@ def parse_args(argv=None):
     p.add_argument("--split-keys", type=int, default=0)
     p.add_argument("--layers", type=int, default=0,
                    help="profiling only: fewer layers of the same per-layer shape (not a bench line)")
+    p.add_argument("--graph", action="store_true",
+                   help="replay the whole step from one CUDA graph (for launch-bound small workloads)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=12.0)
@@ -308,23 +310,57 @@ def run_ours(args):
     events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(sp.L)]
               for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    graph, graph_launches = None, 0
+    if args.graph:
+        # the step ends where it started (truncate back to s_b), so every replay does the same work
+        graph = torch.cuda.CUDAGraph()
+        before = kb.kvc_launch_count(wl.cache)
+        with torch.cuda.graph(graph):
+            step()
+        graph_launches = kb.kvc_launch_count(wl.cache) - before
+        graph.replay()
+        torch.cuda.synchronize()
     launches0 = kb.kvc_launch_count(wl.cache)
     barrier()
     with ClockSampler(local) as clocks:
         t0.record(stream)
         for i in range(args.steps):
-            step(events[i])
+            if graph is not None:
+                graph.replay()
+            else:
+                step(events[i])
         t1.record(stream)
         barrier()
-    launches = kb.kvc_launch_count(wl.cache) - launches0
+    launches = kb.kvc_launch_count(wl.cache) - launches0 + graph_launches * args.steps
     kb.kvc_status(wl.cache)
     ms = t0.elapsed_time(t1) / args.steps
+    if graph is not None:                  # kernel durations from a pass without the graph
+        for i in range(args.steps):
+            step(events[i])
+        torch.cuda.synchronize()
+        graph_ms = ms
+    else:                                  # the same step replayed from one CUDA graph, for reference
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2):
+            step()
+        g2.replay()
+        barrier()
+        t0.record(stream)
+        for i in range(args.steps):
+            g2.replay()
+        t1.record(stream)
+        barrier()
+        graph_ms = t0.elapsed_time(t1) / args.steps
+        del g2
     attn_ms = [ev[l][0].elapsed_time(ev[l][1]) for ev in events for l in range(sp.L)]
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     if world > 1:
         t = torch.tensor([ms, attn_avg_ms], device=f"cuda:{local}")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, attn_avg_ms = float(t[0]), float(t[1])
+        t = torch.tensor([graph_ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        graph_ms = float(t[0])
 
     # end to end through the public API with host buffers: pinned inputs copied in and outputs
     # read back inside the timed region, every step
@@ -383,8 +419,12 @@ def run_ours(args):
         "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": sp.dtype,
         "data": "synthetic (seeded Philox draws; approximately N(0,1))",
-        "config": workload_config(sp, None if not args.layers else "PROFILING CASE: fewer layers, not a bench line"),
+        "config": dict(workload_config(sp, None if not args.layers else "PROFILING CASE: fewer layers, not a bench line"),
+                       graph=bool(args.graph)),
         "steps_per_s": round(world * 1e3 / ms, 3),
+        "graph_replay": {"value": round(world * sp.step_bytes() / (graph_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                         "ms_per_step": round(graph_ms, 4), "steps_per_s": round(world * 1e3 / graph_ms, 3),
+                         "note": "the same step captured once in a CUDA graph and replayed (no host launches)"},
         "pct_of_peak": {"measured_hbm": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / 8000.0, 2)},
         "roofline": {"kernel": "gqa_cached_attn (decode_tc_kernel: tcgen05 split-K attention with fused merge)",
@@ -392,6 +432,8 @@ def run_ours(args):
                      "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(attn_gbs / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": sp.attn_bytes(), "launch_ms": round(attn_avg_ms, 5),
+                     "timing": "CUDA events around each attention call" + (
+                         " (in a pass without the graph)" if args.graph else " inside the timed region"),
                      "traffic": traffic_per_launch(args.workload)},
         "cpu_baseline": cpu,
         "e2e": e2e,

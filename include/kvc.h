@@ -193,6 +193,14 @@ int gqa_cached_attn_noalloc(kvc_handle h, const void* q_dev, kvc_dtype q_dtype, 
                             int H_q, float* out_dev, void* stream);
 
 /*
+ * kvc_selftest_wait_timeout — operational self-test (no counterpart on the pages): launch one thread
+ * that waits on a barrier phase nothing completes and gives up after `limit_us` microseconds
+ * (1 .. 1,000,000), exactly as the attention kernels' bounded waits do. The next kvc_status then
+ * returns KVC_E_DEVICE_TIMEOUT and clears the flag; the handle stays usable. No fault is raised.
+ */
+int kvc_selftest_wait_timeout(kvc_handle h, int limit_us, void* stream);
+
+/*
  * kvc_launch_count — number of kernels this handle has enqueued since kvc_create (host counter,
  * incremented at each successful launch). Instrumentation for benchmarks; 0 for NULL.
  */

@@ -41,6 +41,7 @@ SIGNATURES = {
     "kvc_last_error": (_c_int, [_vp, ctypes.c_char_p, _sz]),
     "kvc_set_split_keys": (_c_int, [_vp, _c_int]),
     "kvc_launch_count": (ctypes.c_uint64, [_vp]),
+    "kvc_selftest_wait_timeout": (_c_int, [_vp, _c_int, _vp]),
     "kvc_synth_fill_normal_f32": (_c_int, [_vp, _sz, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32,
                                            ctypes.c_float, _vp]),
 }
@@ -214,6 +215,10 @@ def kvc_status(c: Cache, stream=None):
 
 def kvc_set_split_keys(c: Cache, keys: int):
     _check(load().kvc_set_split_keys(c.h, keys), c.h)
+
+
+def kvc_selftest_wait_timeout(c: Cache, limit_us: int, stream=None):
+    _check(load().kvc_selftest_wait_timeout(c.h, int(limit_us), _stream(stream)), c.h)
 
 
 def kvc_launch_count(c: Cache) -> int:

@@ -35,6 +35,7 @@ constexpr int kBoxBytes = kTK * 128;        // one 64-element (128-byte) swizzle
 constexpr int kTmemCols = 256;
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
+constexpr int kMergeSplits = 31;            // splits merged through shared memory (else a running merge)
 
 // Shared memory per CTA stays under ~110 KB so that two CTAs share an SM: the K/V ring holds 96 KB
 // (3 tiles of 32 KB for d_h = 128, 6 of 16 KB for d_h = 64), plus Q^T and one P^T buffer (hi, lo).
@@ -73,6 +74,7 @@ constexpr size_t smem_bytes() {
              ? (1024 + Layout<NR, DH>::kCtlOff + sizeof(Ctl<NR, DH>)) : 80 * 1024;
 }
 static_assert(3 * 80 * 1024 > 228 * 1024, "three CTAs must not fit on one SM");
+static_assert((2 * 16 * kMergeSplits + 16) * 4 <= 2 * Layout<16, 64>::kPBytes, "merge scratch fits the P buffer");
 
 // Byte offset of element (row, col) in an [rows][128] 16-bit matrix stored as two 128-byte-swizzled
 // atoms of 64 columns (the layout TMA writes and the tensor cores read, K-major).
@@ -361,20 +363,59 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       if (ctl->last) {
         __threadfence();
         const long long first_row = static_cast<long long>(plan.prefix[unit] + kvh * nsplit) * NR;
-        for (int r = 0; r < nrows && d_ok; ++r) {
-          float m = -INFINITY, l = 0.f, acc = 0.f;
-          for (int s = 0; s < nsplit; ++s) {
-            const long long row = first_row + static_cast<long long>(s) * NR + r;
-            const float ms = __ldcg(a.part_ml + row * 2), ls = __ldcg(a.part_ml + row * 2 + 1);
-            if (!(ls > 0.f)) continue;
-            const float mn = fmaxf(m, ms);
-            const float c_old = exp2f(m - mn), c_new = exp2f(ms - mn);
-            l = l * c_old + ls * c_new;
-            acc = acc * c_old + __ldcg(a.part_o + row * kDh + d) * c_new;
-            m = mn;
+        if (nsplit <= kMergeSplits) {
+          // every split's (m, l) at once into the P buffer (free now), then one set of weights per
+          // row, then independent loads of the partial outputs
+          float* wm = reinterpret_cast<float*>(p_base);            // [NR][kMergeSplits] m, then weight
+          float* wl = wm + NR * kMergeSplits;                      // [NR][kMergeSplits] l
+          float* linv = wl + NR * kMergeSplits;                    // [NR]
+          for (int i = tid - 64; i < nrows * nsplit; i += kSoftmaxThreads) {
+            const int r = i / nsplit, sp = i % nsplit;
+            const long long row = first_row + static_cast<long long>(sp) * NR + r;
+            wm[r * kMergeSplits + sp] = __ldcg(a.part_ml + row * 2);
+            wl[r * kMergeSplits + sp] = __ldcg(a.part_ml + row * 2 + 1);
           }
-          const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-          if (!aborted && d_ok) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l;
+          named_sync(1, kSoftmaxThreads);
+          if (tid - 64 < nrows) {
+            const int r = tid - 64;
+            float m = -INFINITY;
+            for (int sp = 0; sp < nsplit; ++sp)
+              if (wl[r * kMergeSplits + sp] > 0.f) m = fmaxf(m, wm[r * kMergeSplits + sp]);
+            float lsum = 0.f;
+            for (int sp = 0; sp < nsplit; ++sp) {
+              const float ls = wl[r * kMergeSplits + sp];
+              const float w = ls > 0.f ? exp2f(wm[r * kMergeSplits + sp] - m) : 0.f;
+              wm[r * kMergeSplits + sp] = w;
+              lsum += w * ls;
+            }
+            linv[r] = 1.f / lsum;
+          }
+          named_sync(1, kSoftmaxThreads);
+          for (int r = 0; r < nrows && d_ok; ++r) {
+            float acc = 0.f;
+#pragma unroll 4
+            for (int sp = 0; sp < nsplit; ++sp)
+              acc = fmaf(wm[r * kMergeSplits + sp],
+                         __ldcg(a.part_o + (first_row + static_cast<long long>(sp) * NR + r) * kDh + d), acc);
+            const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+            if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc * linv[r];
+          }
+        } else {
+          for (int r = 0; r < nrows && d_ok; ++r) {
+            float m = -INFINITY, l = 0.f, acc = 0.f;
+            for (int sp = 0; sp < nsplit; ++sp) {
+              const long long row = first_row + static_cast<long long>(sp) * NR + r;
+              const float ms = __ldcg(a.part_ml + row * 2), ls = __ldcg(a.part_ml + row * 2 + 1);
+              if (!(ls > 0.f)) continue;
+              const float mn = fmaxf(m, ms);
+              const float c_old = exp2f(m - mn), c_new = exp2f(ms - mn);
+              l = l * c_old + ls * c_new;
+              acc = acc * c_old + __ldcg(a.part_o + row * kDh + d) * c_new;
+              m = mn;
+            }
+            const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+            if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l;
+          }
         }
         if (tid == 64) *counter = 0;
       }
@@ -395,7 +436,7 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
                 cudaStream_t st) {
   auto kern = decode_tc_kernel<Tc, NR, DH>;
   const size_t smem = smem_bytes<NR, DH>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = ensure_smem_limit<decode_tc_kernel<Tc, NR, DH>>(smem);
   if (e != cudaSuccess) return e;
   kern<<<p.n_items, kThreads, smem, st>>>(a, p, *tk, *tv);
   return cudaGetLastError();

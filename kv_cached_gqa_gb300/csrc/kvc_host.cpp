@@ -246,6 +246,9 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
     const long long waves = std::max(1LL, (work + slots * 1536 - 1) / (slots * 1536));
     w = (work + waves * slots - 1) / (waves * slots);
   }
+  // at least 4 tiles per split unless overridden: shorter splits cost more in set-up and merging
+  // than their parallelism returns
+  if (h->split_keys_override <= 0) w = std::max<long long>(w, 4LL * tile);
   w = std::max(1LL, w);
   for (int u = 0; u < n_units; ++u) {
     long long ns = std::max(1LL, (n_eff[u] + w / 2) / w);

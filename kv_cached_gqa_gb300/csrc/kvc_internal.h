@@ -107,6 +107,22 @@ cudaError_t launch_attention(const AttnPlan& ap, const AttnArgs& a, const SplitP
 bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max_len,
                       long long planes, int box_rows, std::string* err);
 
+// Raise a kernel's dynamic shared-memory limit once per device instead of on every launch (the
+// attribute persists for the process; the call costs host time that decode launches cannot spare).
+// Keyed on the kernel itself: every instantiation keeps its own flags.
+template <auto Kernel>
+cudaError_t ensure_smem_limit(size_t bytes) {
+  static unsigned long long done = 0;          // bit d: set on device d
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0;
+  if (bit && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && bit) __atomic_fetch_or(&done, bit, __ATOMIC_RELEASE);
+  return e;
+}
+
 }  // namespace kvc
 
 struct kvc_cache {

@@ -389,7 +389,7 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
                 cudaStream_t st) {
   auto kern = prefill_tc_kernel<Tc>;
   const size_t smem = prefill_smem<Tc>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = ensure_smem_limit<prefill_tc_kernel<Tc>>(smem);
   if (e != cudaSuccess) return e;
   kern<<<p.n_units * a.H_kv, kThreads, smem, st>>>(a, p, *tk, *tv);
   return cudaGetLastError();

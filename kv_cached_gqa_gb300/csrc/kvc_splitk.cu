@@ -441,7 +441,7 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
                 cudaStream_t st) {
   const size_t smem = smem_bytes<Tc, D, RMAX>();
   auto kern = splitk_kernel<Tc, D, RMAX>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_limit<splitk_kernel<Tc, D, RMAX>>(smem);
   if (e != cudaSuccess) return e;
   kern<<<p.n_items, kThreads, smem, st>>>(a, p, *tk, *tv);
   return cudaGetLastError();

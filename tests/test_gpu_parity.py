@@ -287,3 +287,21 @@ def test_tiny_decoder_cached_vs_uncached_logits():
         new = [ids_ref[len(prompt) + step]]
     assert kb.kvc_seq_len(cache) == [len(prompt) + w["new_tokens"] - 1]
     cache.close()
+
+
+def test_bounded_wait_gives_up_and_reports_without_fault():
+    """A kernel wait that runs out sets the status word; kvc_status reports it once, and the handle
+    (and the CUDA context) keep working."""
+    import torch
+    from kv_cached_gqa_gb300 import _binding as kb
+    m = Mirror(L=1, B=2, H_kv=2, d_h=128, max_len=64, dtype="bf16", seed=9)
+    m.append(0, 40)
+    kb.kvc_selftest_wait_timeout(m.gpu, 2000)                 # 2 ms
+    with pytest.raises(kb.KvcError) as ei:
+        kb.kvc_status(m.gpu)
+    assert ei.value.code == -5
+    kb.kvc_status(m.gpu)                                       # the flag was cleared
+    got, want = m.attend(0, 8, 40)
+    check_outputs(got, want, "bf16", "after a reported timeout")
+    kb.kvc_status(m.gpu)
+    m.close()
