@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "kvc_device.cuh"
 #include "kvc_internal.h"
 
 namespace kvc {
@@ -59,6 +60,8 @@ struct Pack<__nv_bfloat16> {
 // One thread per 16-byte output group; grid covers 2 (K, V) x B x H x T x D / N groups.
 template <typename Tc, bool kF32In>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   constexpr int N = Pack<Tc>::N;
   const int groups_per_row = a.D / N;
   const long long rows = static_cast<long long>(a.B) * a.H * a.T;
@@ -94,6 +97,8 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
 }
 
 __global__ void lens_add_kernel(int32_t* lens, int B, int delta) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < B) lens[i] += delta;
 }
@@ -103,11 +108,15 @@ struct LensValues {
 };
 
 __global__ void lens_set_kernel(int32_t* lens, int B, const __grid_constant__ LensValues n) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < B) lens[i] = n.v[i];
 }
 
 __global__ void positions_kernel(const int32_t* lens, int B, int T, int32_t* out) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i < static_cast<long long>(B) * T) out[i] = lens[i / T] + static_cast<int>(i % T);
 }
@@ -119,10 +128,9 @@ cudaError_t run_append(const AppendArgs& a, cudaStream_t st) {
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   if (a.in_dtype == KVC_F32)
-    append_kernel<Tc, true><<<static_cast<unsigned>(blocks), threads, 0, st>>>(a);
+    return launch_pdl(append_kernel<Tc, true>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, a);
   else
-    append_kernel<Tc, false><<<static_cast<unsigned>(blocks), threads, 0, st>>>(a);
-  return cudaGetLastError();
+    return launch_pdl(append_kernel<Tc, false>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, a);
 }
 
 }  // namespace
@@ -137,21 +145,19 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_lens_add(int32_t* lens, int B, int delta, cudaStream_t st) {
-  lens_add_kernel<<<(B + 255) / 256, 256, 0, st>>>(lens, B, delta);
-  return cudaGetLastError();
+  return launch_pdl(lens_add_kernel, dim3((B + 255) / 256), dim3(256), 0, st, lens, B, delta);
 }
 
 cudaError_t launch_lens_set(int32_t* lens, int B, const int32_t* n_host, cudaStream_t st) {
   LensValues v;
   for (int i = 0; i < B; ++i) v.v[i] = n_host[i];
-  lens_set_kernel<<<(B + 255) / 256, 256, 0, st>>>(lens, B, v);
-  return cudaGetLastError();
+  return launch_pdl(lens_set_kernel, dim3((B + 255) / 256), dim3(256), 0, st, lens, B, v);
 }
 
 cudaError_t launch_positions(const int32_t* lens, int B, int T, int32_t* out, cudaStream_t st) {
   const long long n = static_cast<long long>(B) * T;
-  positions_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(lens, B, T, out);
-  return cudaGetLastError();
+  return launch_pdl(positions_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, st,
+                    lens, B, T, out);
 }
 
 }  // namespace kvc

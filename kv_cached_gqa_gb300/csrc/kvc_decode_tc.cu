@@ -123,12 +123,6 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int rt = plan.unit_b[unit] % plan.n_rowtiles;
   const int row0 = rt * NR;
   const int nrows = min(NR, a.T * a.G - row0);
-  const int s_b = a.lens[b] + a.delta - a.T;
-  const int n_eff = s_b + (row0 + nrows - 1) / a.G + 1;
-  const int chunk = (n_eff + nsplit - 1) / nsplit;      // near-equal splits of the unit's keys
-  const int k_begin = split * chunk;
-  const int k_end = min(k_begin + chunk, n_eff);
-  const int nkt = (k_end - k_begin + kTK - 1) / kTK;
   const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
 
   // ---- set-up: TMEM, barriers, Q^T, zeroed P^T ------------------------------------------------
@@ -148,6 +142,15 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     ctl->abort = 0;
     fence_mbar_init();
   }
+  // from here on the lengths and the queries, which earlier kernels write, are read
+  pdl_wait();
+  pdl_trigger();
+  const int s_b = a.lens[b] + a.delta - a.T;
+  const int n_eff = s_b + (row0 + nrows - 1) / a.G + 1;
+  const int chunk = (n_eff + nsplit - 1) / nsplit;      // near-equal splits of the unit's keys
+  const int k_begin = split * chunk;
+  const int k_end = min(k_begin + chunk, n_eff);
+  const int nkt = (k_end - k_begin + kTK - 1) / kTK;
   for (int i = tid; i < NR * kDh; i += kThreads) {
     const int r = i / kDh, d = i % kDh;
     float x = 0.f;
@@ -438,8 +441,7 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
   const size_t smem = smem_bytes<NR, DH>();
   cudaError_t e = ensure_smem_limit<decode_tc_kernel<Tc, NR, DH>>(smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.n_items, kThreads, smem, st>>>(a, p, *tk, *tv);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(p.n_items), dim3(kThreads), smem, st, a, p, *tk, *tv);
 }
 
 }  // namespace

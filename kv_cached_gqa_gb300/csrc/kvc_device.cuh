@@ -84,6 +84,15 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------------------------------
+// Every kernel of the library is launched so that it may start while its stream predecessor is
+// still finishing. Each kernel first does set-up that touches no global data another kernel writes,
+// then `pdl_wait` (the predecessor has completed and its memory is visible), then `pdl_trigger`
+// (its own successor may now be scheduled), then its work. Triggering only after waiting keeps the
+// usual guarantee: when a kernel starts, every kernel two or more launches back has completed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- tcgen05 ------------------------------------------------------------------------------------
 
 // Shared-memory matrix descriptor: start address, leading and stride byte offsets (16-byte units),

@@ -107,6 +107,24 @@ cudaError_t launch_attention(const AttnPlan& ap, const AttnArgs& a, const SplitP
 bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max_len,
                       long long planes, int box_rows, std::string* err);
 
+// Launch with programmatic stream serialization: the kernel may be scheduled before its stream
+// predecessor finishes and orders itself with griddepcontrol.wait (see kvc_device.cuh).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Raise a kernel's dynamic shared-memory limit once per device instead of on every launch (the
 // attribute persists for the process; the call costs host time that decode launches cannot spare).
 // Keyed on the kernel itself: every instantiation keeps its own flags.

@@ -147,11 +147,6 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int rt = plan.unit_b[unit] % plan.n_rowtiles;
   const int row0 = rt * kRows;
   const int nrows = min(kRows, a.T * a.G - row0);
-  const int s_b = a.lens[b] + a.delta - a.T;
-  const int first_t = row0 / a.G, last_t = (row0 + nrows - 1) / a.G;
-  const int n_keys = s_b + last_t + 1;                       // keys visible to the tile's last row
-  const int nkt = (n_keys + kKeys - 1) / kKeys;
-  const int unmasked_keys = s_b + first_t + 1;               // keys visible to every row of the tile
   const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
 
   // ---- set-up ------------------------------------------------------------------------------------
@@ -172,6 +167,14 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     ctl->abort = 0;
     fence_mbar_init();
   }
+  // from here on the lengths and the queries, which earlier kernels write, are read
+  pdl_wait();
+  pdl_trigger();
+  const int s_b = a.lens[b] + a.delta - a.T;
+  const int first_t = row0 / a.G, last_t = (row0 + nrows - 1) / a.G;
+  const int n_keys = s_b + last_t + 1;                       // keys visible to the tile's last row
+  const int nkt = (n_keys + kKeys - 1) / kKeys;
+  const int unmasked_keys = s_b + first_t + 1;               // keys visible to every row of the tile
   // Q tile: 128 rows x 128 d in the cache dtype, 128-byte swizzled (rows past the chunk are zero)
   for (int i = tid; i < kRows * (kDh / 8); i += kThreads) {
     const int r = i / (kDh / 8), c = i % (kDh / 8);
@@ -391,8 +394,7 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
   const size_t smem = prefill_smem<Tc>();
   cudaError_t e = ensure_smem_limit<prefill_tc_kernel<Tc>>(smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.n_units * a.H_kv, kThreads, smem, st>>>(a, p, *tk, *tv);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(p.n_units * a.H_kv), dim3(kThreads), smem, st, a, p, *tk, *tv);
 }
 
 static_assert(prefill_smem<__half>() > 114 * 1024 && prefill_smem<__nv_bfloat16>() > 114 * 1024,

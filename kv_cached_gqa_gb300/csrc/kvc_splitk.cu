@@ -188,14 +188,6 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int R = a.T * a.G;                              // query rows of this K/V head
   const int row0 = rt * RMAX;
   const int nrows = min(RMAX, R - row0);
-  const int s_b = a.lens[b] + a.delta - a.T;            // committed length = first query position
-  const int t_max = (row0 + nrows - 1) / a.G;
-  const int n_eff = s_b + t_max + 1;                    // keys visible to the tile's last row
-  const int chunk = (n_eff + nsplit - 1) / nsplit;      // near-equal splits of the unit's keys
-  const int k_begin = split * chunk;
-  const int k_end = min(k_begin + chunk, n_eff);
-  const int n_keys = k_end - k_begin;
-  const int nkt = (n_keys + C::TILE - 1) / C::TILE;
   const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
 
   if (tid == 0) {
@@ -206,6 +198,17 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     sm->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // from here on the lengths and the queries, which earlier kernels write, are read
+  pdl_wait();
+  pdl_trigger();
+  const int s_b = a.lens[b] + a.delta - a.T;            // committed length = first query position
+  const int t_max = (row0 + nrows - 1) / a.G;
+  const int n_eff = s_b + t_max + 1;                    // keys visible to the tile's last row
+  const int chunk = (n_eff + nsplit - 1) / nsplit;      // near-equal splits of the unit's keys
+  const int k_begin = split * chunk;
+  const int k_end = min(k_begin + chunk, n_eff);
+  const int n_keys = k_end - k_begin;
+  const int nkt = (n_keys + C::TILE - 1) / C::TILE;
   // queries of the tile, prescaled by log2(e) / sqrt(d_h): scores are in base-2 units
   const float qscale = kLog2e * rsqrtf(static_cast<float>(D));
   for (int i = tid; i < RMAX * D; i += kThreads) {
@@ -443,8 +446,7 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
   auto kern = splitk_kernel<Tc, D, RMAX>;
   cudaError_t e = ensure_smem_limit<splitk_kernel<Tc, D, RMAX>>(smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.n_items, kThreads, smem, st>>>(a, p, *tk, *tv);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(p.n_items), dim3(kThreads), smem, st, a, p, *tk, *tv);
 }
 
 template <typename Tc, int D>
