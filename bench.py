@@ -159,13 +159,17 @@ def cpu_sample_child(arg):
     import numpy as np
 
     import kvc_workloads
-    from oracle.kvc_oracle import OracleKVCache, gqa_cached_attention
+    from oracle.kvc_oracle import OracleKVCache, OraclePagedKVCache, gqa_cached_attention
     sp = kvc_workloads.spec(cfg["workload"])
     seqs = list(range(cfg["n_seq"]))
     caches, queries = [], []
     for b in seqs:
         s_b = int(sp.lengths[b])
-        c = OracleKVCache(1, 1, sp.H_kv, sp.d_h, s_b + sp.T, sp.dtype)
+        if sp.block:
+            c = OraclePagedKVCache(1, 1, sp.H_kv, sp.d_h, s_b + sp.T, sp.block,
+                                   -(-(s_b + sp.T) // sp.block), sp.dtype)
+        else:
+            c = OracleKVCache(1, 1, sp.H_kv, sp.d_h, s_b + sp.T, sp.dtype)
         if s_b:
             kk = np.stack([sp.host_prefill_rows(0, b, h, s_b)[0] for h in range(sp.H_kv)])[None]
             vv = np.stack([sp.host_prefill_rows(0, b, h, s_b)[1] for h in range(sp.H_kv)])[None]
@@ -257,6 +261,9 @@ def workload_config(sp, note=None):
          "s_b": {"min": int(np.min(sp.lengths)), "mean": float(np.mean(sp.lengths)),
                  "max": int(np.max(sp.lengths))},
          "l2": "no flush: K/V read per layer is larger than the 129 MB L2"}
+    if sp.block:
+        c["paged"] = {"block": sp.block, "n_blocks": sp.B * (-(-sp.max_len // sp.block)),
+                      "layout": "prefilled one block per sequence in turn: a sequence's blocks lie B apart"}
     if note:
         c["note"] = note
     return c

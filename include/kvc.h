@@ -77,6 +77,45 @@ int kvc_create(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len, kv
 int kvc_create_external(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len,
                         kvc_dtype dtype, void* k_store_dev, void* v_store_dev, void* stream);
 
+/*
+ * kvc_create_paged — a cache whose rows live in a pool of fixed-size blocks mapped by a per-sequence
+ * block table, instead of one max_len-long slab per sequence.
+ * Defined by: "KV cache decoding", "Batching caches of different lengths" (the cache in fixed-size
+ * blocks with a table from each request to its blocks; a sequence takes a new block only when it grows
+ * into it and frees its blocks when it ends); "Generation and the KV Cache", "Static versus growing"
+ * (the positions a preallocated cache reserves are what a paged cache recovers); "KV cache,
+ * incremental decode, ...", Key Takeaways and §2.5 (a float16 paged cache stores what the contiguous
+ * one stores and compares with it exactly).
+ * Layout: K and V pools, each [L, n_blocks, H_kv, block_size, d_h] in `dtype`; a block table
+ * [B, ceil(max_len / block_size)] of int32 (device copy owned by the library, host mirror readable with
+ * kvc_block_table). Position p of sequence b is row p % block_size of physical block
+ * table[b][p / block_size], the same block in every layer; -1 marks a logical block with none.
+ * Allocation: kvc_append maps, lowest-numbered free block first (sequences in order, then logical
+ * blocks in order), every block the layer's new fill reaches and the sequence does not hold yet
+ * (one small table-edit launch before the append when any is needed). kvc_truncate and
+ * kvc_truncate_ragged return every block wholly past the new length to the pool (truncate to 0 frees
+ * a sequence's blocks when it ends). A partly filled last block stays with its sequence.
+ * Every other call (append, commit, positions, attention, the no-alloc variant, status) works on a
+ * paged handle with the same arguments, results and errors, and gqa_cached_attn returns exactly what
+ * it returns for a contiguous cache holding the same rows. kvc_nbytes is the pool capacity
+ * 2 * L * n_blocks * H_kv * block_size * d_h * itemsize; kvc_layer_ptrs gives a layer's pool
+ * [n_blocks, H_kv, block_size, d_h].
+ * k_pool_dev, v_pool_dev: both NULL (the library allocates and zeroes the pools) or both caller-owned,
+ * 256-byte aligned and zeroed, kept alive until kvc_destroy.
+ * Limits: those of kvc_create, block_size a power of two in [16, 2^20], n_blocks >= 1,
+ * L * n_blocks * H_kv < 2^31. Errors: KVC_E_INVAL; KVC_E_NOMEM. kvc_append returns KVC_E_CAPACITY,
+ * changing nothing, when the pool has too few free blocks for it.
+ */
+int kvc_create_paged(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len, int block_size,
+                     int n_blocks, kvc_dtype dtype, void* k_pool_dev, void* v_pool_dev, void* stream);
+
+/*
+ * kvc_block_table — copy a paged cache's block table (host mirror, the state after every call enqueued
+ * so far) into table_host[B * ceil(max_len / block_size)] and the number of free pool blocks into
+ * *n_free_host; either pointer may be NULL. KVC_E_INVAL for a contiguous cache.
+ */
+int kvc_block_table(kvc_handle h, int32_t* table_host, int32_t* n_free_host);
+
 /* kvc_destroy — synchronise the device, free everything the library allocated. NULL is a no-op. */
 int kvc_destroy(kvc_handle h);
 

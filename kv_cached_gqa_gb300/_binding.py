@@ -26,6 +26,9 @@ SIGNATURES = {
     "kvc_create": (_c_int, [ctypes.POINTER(_vp), _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "kvc_create_external": (_c_int, [ctypes.POINTER(_vp), _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                      _vp, _vp, _vp]),
+    "kvc_create_paged": (_c_int, [ctypes.POINTER(_vp), _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                  _c_int, _vp, _vp, _vp]),
+    "kvc_block_table": (_c_int, [_vp, _i32p, _i32p]),
     "kvc_destroy": (_c_int, [_vp]),
     "kvc_append": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _vp]),
     "kvc_commit": (_c_int, [_vp, _vp]),
@@ -138,6 +141,25 @@ class Cache:
             pass
 
 
+class PagedCache(Cache):
+    """A paged KV cache handle over torch-allocated pools, each [L, n_blocks, H_kv, block_size, d_h]."""
+
+    def __init__(self, L, B, H_kv, d_h, max_len, block_size, n_blocks, dtype, device="cuda", stream=None):
+        torch = _torch()
+        self.L, self.B, self.H_kv, self.d_h, self.max_len = L, B, H_kv, d_h, max_len
+        self.block_size, self.n_blocks = block_size, n_blocks
+        self.max_blocks = -(-max_len // block_size)
+        self.dtype = dtype if isinstance(dtype, int) else dtype_code(dtype)
+        shape = (L, n_blocks, H_kv, block_size, d_h)
+        self.k = torch.zeros(shape, dtype=torch_dtype(self.dtype), device=device)
+        self.v = torch.zeros(shape, dtype=torch_dtype(self.dtype), device=device)
+        h = ctypes.c_void_p()
+        self.h = None
+        _check(load().kvc_create_paged(ctypes.byref(h), L, B, H_kv, d_h, max_len, block_size, n_blocks,
+                                       self.dtype, self.k.data_ptr(), self.v.data_ptr(), _stream(stream)))
+        self.h = h
+
+
 def kvc_create(L, B, H_kv, d_h, max_len, dtype, stream=None) -> Cache:
     return Cache(L, B, H_kv, d_h, max_len, dtype, stream=stream)
 
@@ -149,6 +171,20 @@ def kvc_append(c: Cache, layer: int, k_new, v_new, stream=None):
         raise ValueError("k_new shape does not match the cache")
     _check(load().kvc_append(c.h, layer, _ptr(k_new), _ptr(v_new), dtype_code(k_new.dtype),
                              int(k_new.shape[2]), _stream(stream)), c.h)
+
+
+def kvc_create_paged(L, B, H_kv, d_h, max_len, block_size, n_blocks, dtype, stream=None) -> PagedCache:
+    return PagedCache(L, B, H_kv, d_h, max_len, block_size, n_blocks, dtype, stream=stream)
+
+
+def kvc_block_table(c: PagedCache):
+    """The block table as B lists of ceil(max_len / block_size) physical blocks (-1 = none), and the
+    number of free pool blocks."""
+    tab = (ctypes.c_int32 * (c.B * c.max_blocks))()
+    n_free = ctypes.c_int32()
+    _check(load().kvc_block_table(c.h, tab, ctypes.byref(n_free)), c.h)
+    flat = [int(x) for x in tab]
+    return [flat[b * c.max_blocks:(b + 1) * c.max_blocks] for b in range(c.B)], int(n_free.value)
 
 
 def kvc_commit(c: Cache, stream=None):

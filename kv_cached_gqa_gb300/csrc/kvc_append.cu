@@ -7,6 +7,10 @@
 // coalesced, vectorised stores with no read-modify-write. The write position comes from the
 // device's committed lengths, so the kernel stays correct when replayed from a captured graph.
 //
+// Paged store: the row's physical block comes from the sequence's block table (pool layout
+// [L, n_blocks, H, block, D]); the table edits that allocate blocks are one small launch before the
+// append, in stream order.
+//
 // Lengths: commit adds T to every committed length, truncate overwrites them; both are one tiny
 // kernel so the device copy changes in stream order with the rest of the forward.
 #include <cuda_bf16.h>
@@ -76,7 +80,18 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   const int bh = static_cast<int>(row / a.T);
   const int b = bh / a.H, h = bh % a.H;
   const int pos = a.lens[b] + a.delta + t;
-  const long long dst_row = ((static_cast<long long>(a.layer) * a.B + b) * a.H + h) * a.max_len + pos;
+  long long dst_row;
+  if (a.pg.table == nullptr) {
+    dst_row = ((static_cast<long long>(a.layer) * a.B + b) * a.H + h) * a.max_len + pos;
+  } else {
+    // paged: the row's block comes from the sequence's table (the host allocated it before this
+    // launch); a missing block, which the host never lets happen, drops the write instead of
+    // writing outside the pool
+    const int blk = a.pg.table[static_cast<long long>(b) * a.pg.max_blocks + (pos >> a.pg.block_shift)];
+    if (blk < 0 || blk >= a.pg.n_blocks) return;
+    dst_row = (((static_cast<long long>(a.layer) * a.pg.n_blocks + blk) * a.H + h) << a.pg.block_shift) +
+              (pos & ((1 << a.pg.block_shift) - 1));
+  }
   Tc* dst = static_cast<Tc*>(is_v ? a.v_store : a.k_store) + dst_row * a.D + grp * N;
   const long long src_off = row * a.D + grp * N;
   uint4 out;
@@ -101,6 +116,13 @@ __global__ void lens_add_kernel(int32_t* lens, int B, int delta) {
   dev::pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < B) lens[i] += delta;
+}
+
+__global__ void table_edits_kernel(int32_t* table, const __grid_constant__ TableEdits e) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < e.n) table[e.slot[i]] = e.value[i];
 }
 
 struct LensValues {
@@ -142,6 +164,11 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
     case KVC_BF16: return run_append<__nv_bfloat16>(a, st);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_table_edits(int32_t* table, const TableEdits& e, cudaStream_t st) {
+  if (e.n <= 0) return cudaSuccess;
+  return launch_pdl(table_edits_kernel, dim3((e.n + 255) / 256), dim3(256), 0, st, table, e);
 }
 
 cudaError_t launch_lens_add(int32_t* lens, int B, int delta, cudaStream_t st) {

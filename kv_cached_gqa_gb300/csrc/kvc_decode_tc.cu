@@ -123,7 +123,6 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int rt = plan.unit_b[unit] % plan.n_rowtiles;
   const int row0 = rt * NR;
   const int nrows = min(NR, a.T * a.G - row0);
-  const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
 
   // ---- set-up: TMEM, barriers, Q^T, zeroed P^T ------------------------------------------------
   if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&ctl->tmem));
@@ -147,7 +146,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   pdl_trigger();
   const int s_b = a.lens[b] + a.delta - a.T;
   const int n_eff = s_b + (row0 + nrows - 1) / a.G + 1;
-  const int chunk = (n_eff + nsplit - 1) / nsplit;      // near-equal splits of the unit's keys
+  const int chunk = split_chunk(n_eff, nsplit, kTK);    // near-equal, whole-tile splits of the unit's keys
   const int k_begin = split * chunk;
   const int k_end = min(k_begin + chunk, n_eff);
   const int nkt = (k_end - k_begin + kTK - 1) / kTK;
@@ -171,28 +170,31 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   volatile int* abort_flag = &ctl->abort;
 
   if (warp == 0) {
-    // ---------------------------------- TMA producer --------------------------------------------
+    // ---------------------------------- TMA producer (whole warp) -------------------------------
     if (lane == 0) {
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      int issued = 0;
-      for (int i = 0; i < 2 * nkt; ++i) {
-        const int st = i % kStages;
-        if (!mbar_wait(smem_u32(&ctl->empty[st]), ((i / kStages) & 1) ^ 1, abort_flag)) break;
-        const bool isv = i >= nkt;
-        const int y = k_begin + (isv ? i - nkt : i) * kTK;
-        const uint32_t full = smem_u32(&ctl->full[st]);
-        mbar_expect_tx(full, kTileBytes);
-        const uint32_t dst = s_stage + st * kTileBytes;
-#pragma unroll
-        for (int bx = 0; bx < Lo::kBoxes; ++bx)
-          tma_load_3d(dst + bx * kBoxBytes, isv ? &tv : &tk, 64 * bx, y, plane, full);
-        issued = i + 1;
+    }
+    int issued = 0;
+    for (int i = 0; i < 2 * nkt; ++i) {
+      const int st = i % kStages;
+      const bool isv = i >= nkt;
+      const int y = k_begin + (isv ? i - nkt : i) * kTK;
+      const TilePiece pc = tile_piece<kTK>(a, b, kvh, y, lane);   // a block-table read overlaps the wait
+      const uint32_t full = smem_u32(&ctl->full[st]);
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(smem_u32(&ctl->empty[st]), ((i / kStages) & 1) ^ 1, abort_flag);
+        if (ok) mbar_expect_tx(full, kTileBytes);
       }
-      // drain: the last copy issued into each stage has landed before the CTA can exit
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      issue_piece<kTK, Lo::kBoxes, 128, 64>(pc, isv ? &tv : &tk, s_stage + st * kTileBytes, full, lane);
+      issued = i + 1;
+    }
+    // drain: the last copy issued into each stage has landed before the CTA can exit
+    if (lane == 0)
       for (int i = max(0, issued - kStages); i < issued; ++i)
         mbar_drain(smem_u32(&ctl->full[i % kStages]), (i / kStages) & 1);
-    }
   } else if (warp == 1) {
     // ---------------------------------- MMA issuer ----------------------------------------------
     if (lane == 0) {

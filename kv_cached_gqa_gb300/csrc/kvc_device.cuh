@@ -76,6 +76,57 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<unsigned long long>(map)) : "memory");
 }
+// ---- K/V tile addressing -------------------------------------------------------------------------
+// Tensor-map coordinates (row, plane) of key `key` of K/V head kvh of sequence b. A contiguous store
+// has one plane per (layer, b, kvh) and row = key. A paged pool has one plane per (layer, physical
+// block, kvh) and row = key mod block, the block read from the sequence's table. A logical block with
+// no physical block (past the table, or -1) maps to row `block` of a valid plane: past the map's row
+// extent, where TMA writes zeros instead of reading memory.
+__device__ __forceinline__ void kv_coords(const AttnArgs& a, int b, int kvh, int key, int* row, int* plane) {
+  if (a.pg.table == nullptr) {
+    *row = key;
+    *plane = (a.layer * a.B + b) * a.H_kv + kvh;
+    return;
+  }
+  const int idx = key >> a.pg.block_shift;
+  const int phys = idx < a.pg.max_blocks ? a.pg.table[b * a.pg.max_blocks + idx] : -1;
+  const bool have = phys >= 0 && phys < a.pg.n_blocks;
+  *row = have ? (key & ((1 << a.pg.block_shift) - 1)) : (1 << a.pg.block_shift);
+  *plane = (a.layer * a.pg.n_blocks + (have ? phys : 0)) * a.H_kv + kvh;
+}
+
+// One lane's share of a K/V tile load. A tile is keys [y, y + kRows) of one K or V head, stored as
+// kBoxes boxes of kRows rows x kSpan bytes one after another. A contiguous store loads each box with
+// one TMA (lane 0). A paged pool whose blocks are shorter than the tile loads it in pieces of one
+// block: lane j issues piece j of every box, at row offset j * rows. The 128- and 64-byte swizzle
+// patterns repeat every 8 rows and blocks hold at least 16, so the pieces land exactly where one
+// whole-tile box would put them.
+struct TilePiece {
+  int row, plane, rows;
+  bool on;
+};
+template <int kRows>
+__device__ __forceinline__ TilePiece tile_piece(const AttnArgs& a, int b, int kvh, int y, int lane) {
+  TilePiece p;
+  p.rows = (a.pg.table != nullptr && (1 << a.pg.block_shift) < kRows) ? (1 << a.pg.block_shift) : kRows;
+  p.on = lane * p.rows < kRows;
+  p.row = 0;
+  p.plane = 0;
+  if (p.on) kv_coords(a, b, kvh, y + lane * p.rows, &p.row, &p.plane);
+  return p;
+}
+// Issue the piece (after the stage's barrier has been armed for the whole tile's bytes). kInner is
+// the element count of one box row, the x step between boxes.
+template <int kRows, int kBoxes, int kSpan, int kInner>
+__device__ __forceinline__ void issue_piece(const TilePiece& p, const CUtensorMap* map, uint32_t dst,
+                                            uint32_t bar, int lane) {
+  if (!p.on) return;
+#pragma unroll
+  for (int bx = 0; bx < kBoxes; ++bx)
+    tma_load_3d(dst + static_cast<uint32_t>((bx * kRows + lane * p.rows) * kSpan), map, bx * kInner, p.row,
+                p.plane, bar);
+}
+
 // generic-proxy shared-memory writes become visible to the async proxy (TMA, tensor cores)
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

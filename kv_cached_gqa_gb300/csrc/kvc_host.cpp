@@ -78,19 +78,28 @@ int init_device_state(kvc_handle h, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaMemsetAsync(h->d_status, 0, sizeof(int), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->d_counters, 0, sizeof(int) * kvc::kMaxUnits * h->H, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync");
+  if (h->paged) {                                   // every logical block starts unmapped (-1)
+    const size_t tb = sizeof(int32_t) * h->table.size();
+    e = cudaMalloc(&h->d_table, tb);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(block table)");
+    e = cudaMemsetAsync(h->d_table, 0xFF, tb, st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync(block table)");
+  }
   int rows = 0;
   kvc::splitk_shape(h->dtype, h->D, 1, &rows, &h->split_tile_keys);
   std::string err;
-  const long long planes = static_cast<long long>(h->L) * h->B * h->H;
-  if (!kvc::encode_store_map(&h->tmap_k_split, h->k, h->dtype, h->D, h->max_len, planes,
-                             h->split_tile_keys, &err) ||
-      !kvc::encode_store_map(&h->tmap_v_split, h->v, h->dtype, h->D, h->max_len, planes,
-                             h->split_tile_keys, &err))
+  const kvc::Paging pg = kvc_paging(h);
+  const long long planes = static_cast<long long>(h->L) * (h->paged ? h->n_blocks : h->B) * h->H;
+  const int plane_rows = h->paged ? h->block : h->max_len;
+  const int split_box = kvc::paged_box_rows(pg, h->split_tile_keys);
+  if (!kvc::encode_store_map(&h->tmap_k_split, h->k, h->dtype, h->D, plane_rows, planes, split_box, &err) ||
+      !kvc::encode_store_map(&h->tmap_v_split, h->v, h->dtype, h->D, plane_rows, planes, split_box, &err))
     return fail(h, KVC_E_CUDA, "%s", err.c_str());
   int tc_rows = 0, tc_tile = 0, tc_tiles = 0;
   if (kvc::decode_tc_shape(h->dtype, h->D, 1, &tc_rows, &tc_tile, &tc_tiles)) {
-    if (!kvc::encode_store_map(&h->tmap_k_tc, h->k, h->dtype, h->D, h->max_len, planes, tc_tile, &err) ||
-        !kvc::encode_store_map(&h->tmap_v_tc, h->v, h->dtype, h->D, h->max_len, planes, tc_tile, &err))
+    const int tc_box = kvc::paged_box_rows(pg, tc_tile);
+    if (!kvc::encode_store_map(&h->tmap_k_tc, h->k, h->dtype, h->D, plane_rows, planes, tc_box, &err) ||
+        !kvc::encode_store_map(&h->tmap_v_tc, h->v, h->dtype, h->D, plane_rows, planes, tc_box, &err))
       return fail(h, KVC_E_CUDA, "%s", err.c_str());
     h->has_tc = true;
   }
@@ -108,6 +117,7 @@ void release(kvc_handle h) {
   cudaFree(h->d_status);
   cudaFree(h->work);
   cudaFree(h->d_counters);
+  cudaFree(h->d_table);
   delete h;
 }
 
@@ -132,8 +142,73 @@ kvc_handle new_handle(int L, int B, int H_kv, int d_h, int max_len, kvc_dtype dt
   return h;
 }
 
+// Bytes of one of the two stores (K or V): [L, B, H, max_len, D], or the pool [L, n_blocks, H, block, D].
 size_t store_bytes(kvc_handle h) {
-  return static_cast<size_t>(h->L) * h->B * h->H * h->max_len * h->D * kvc::itemsize(h->dtype);
+  const size_t per_layer = h->paged ? static_cast<size_t>(h->n_blocks) * h->block : static_cast<size_t>(h->B) * h->max_len;
+  return static_cast<size_t>(h->L) * per_layer * h->H * h->D * kvc::itemsize(h->dtype);
+}
+
+// ---- paged pool bookkeeping ------------------------------------------------------------------------
+// Free blocks live in a min-heap, so the lowest-numbered free block is always handed out first; a
+// sequence's logical blocks 0 .. held-1 are mapped. Allocation happens at append, for the blocks the
+// layer's new fill reaches; truncate returns every block wholly past the new length.
+int blocks_for(kvc_handle h, long long rows) { return static_cast<int>((rows + h->block - 1) >> h->block_shift); }
+
+int pop_free(kvc_handle h) {
+  std::pop_heap(h->free_heap.begin(), h->free_heap.end(), std::greater<int32_t>());
+  const int v = h->free_heap.back();
+  h->free_heap.pop_back();
+  return v;
+}
+
+void push_free(kvc_handle h, int v) {
+  h->free_heap.push_back(v);
+  std::push_heap(h->free_heap.begin(), h->free_heap.end(), std::greater<int32_t>());
+}
+
+// Enqueue table edits (slot, value) in launches of at most kMaxTableEdits.
+cudaError_t send_edits(kvc_handle h, const std::vector<std::pair<int32_t, int32_t>>& edits, cudaStream_t st) {
+  static thread_local kvc::TableEdits e;    // 8 KB: keep it off the stack
+  for (size_t i = 0; i < edits.size(); i += kvc::kMaxTableEdits) {
+    e.n = static_cast<int>(std::min<size_t>(kvc::kMaxTableEdits, edits.size() - i));
+    for (int j = 0; j < e.n; ++j) {
+      e.slot[j] = edits[i + j].first;
+      e.value[j] = edits[i + j].second;
+    }
+    const cudaError_t r = kvc::launch_table_edits(h->d_table, e, st);
+    if (r != cudaSuccess) return r;
+    h->launches += 1;
+  }
+  return cudaSuccess;
+}
+
+// Map the blocks that `layer`'s fill reaches after T more rows. All or nothing: on error no block is
+// taken and the host table is unchanged.
+int paged_grow(kvc_handle h, int layer, int T, cudaStream_t st) {
+  long long need = 0;
+  for (int b = 0; b < h->B; ++b) {
+    const int nb = blocks_for(h, static_cast<long long>(h->fill[static_cast<size_t>(layer) * h->B + b]) + T);
+    if (nb > h->held[b]) need += nb - h->held[b];
+  }
+  if (need == 0) return KVC_OK;
+  if (need > static_cast<long long>(h->free_heap.size()))
+    return fail(h, KVC_E_CAPACITY, "block pool exhausted: the append needs %lld more blocks of %d positions, "
+                "%zu of %d are free", need, h->block, h->free_heap.size(), h->n_blocks);
+  std::vector<std::pair<int32_t, int32_t>>& edits = h->edit_scratch;
+  edits.clear();
+  for (int b = 0; b < h->B; ++b) {
+    const int nb = blocks_for(h, static_cast<long long>(h->fill[static_cast<size_t>(layer) * h->B + b]) + T);
+    for (int i = h->held[b]; i < nb; ++i) edits.push_back({b * h->max_blocks + i, pop_free(h)});
+  }
+  const cudaError_t e = send_edits(h, edits, st);
+  if (e != cudaSuccess) {
+    for (const auto& ed : edits) push_free(h, ed.second);
+    return cuda_fail(h, e, "block table launch");
+  }
+  for (const auto& ed : edits) h->table[ed.first] = ed.second;
+  for (int b = 0; b < h->B; ++b)
+    h->held[b] = std::max(h->held[b], blocks_for(h, static_cast<long long>(h->fill[static_cast<size_t>(layer) * h->B + b]) + T));
+  return KVC_OK;
 }
 
 // Uniform difference between one layer's fills and the committed lengths.
@@ -251,12 +326,13 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
   if (h->split_keys_override <= 0) w = std::max<long long>(w, 4LL * tile);
   w = std::max(1LL, w);
   for (int u = 0; u < n_units; ++u) {
-    long long ns = std::max(1LL, (n_eff[u] + w / 2) / w);
-    while ((n_eff[u] + ns - 1) / ns > cmax) ++ns;
-    const long long chunk = (n_eff[u] + ns - 1) / ns;
-    ns = (n_eff[u] + chunk - 1) / chunk;                    // same chunk, no empty trailing split
-    order[u] = {static_cast<int>(chunk), u};
-    nsplit[u] = static_cast<int>(ns);
+    const int n = static_cast<int>(n_eff[u]);
+    int ns = static_cast<int>(std::max(1LL, (n_eff[u] + w / 2) / w));
+    while (kvc::split_chunk(n, ns, tile) > cmax) ++ns;
+    const int chunk = kvc::split_chunk(n, ns, tile);        // whole tiles, as the kernels recompute it
+    ns = (n + chunk - 1) / chunk;                           // same chunk, no empty trailing split
+    order[u] = {chunk, u};
+    nsplit[u] = ns;
   }
   std::stable_sort(order.begin(), order.end(), longest_first);
   long long items = 0;
@@ -353,6 +429,69 @@ int kvc_create_external(kvc_handle* out, int L, int B, int H_kv, int d_h, int ma
   return KVC_OK;
 }
 
+int kvc_create_paged(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len, int block_size,
+                     int n_blocks, kvc_dtype dtype, void* k_pool, void* v_pool, void* stream) {
+  if (!out) return fail(nullptr, KVC_E_INVAL, "null output handle");
+  *out = nullptr;
+  int rc = check_sizes(L, B, H_kv, d_h, max_len, dtype);
+  if (rc) return rc;
+  if (block_size < 16 || block_size > (1 << 20) || (block_size & (block_size - 1)))
+    return fail(nullptr, KVC_E_INVAL, "block_size=%d must be a power of two in [16, 2^20]", block_size);
+  if (n_blocks < 1) return fail(nullptr, KVC_E_INVAL, "n_blocks=%d must be positive", n_blocks);
+  const long long max_blocks = (static_cast<long long>(max_len) + block_size - 1) / block_size;
+  if (static_cast<long long>(L) * n_blocks * H_kv >= (1LL << 31) || static_cast<long long>(B) * max_blocks >= (1LL << 31))
+    return fail(nullptr, KVC_E_INVAL, "pool or block table too large for 32-bit tile coordinates");
+  if ((k_pool == nullptr) != (v_pool == nullptr))
+    return fail(nullptr, KVC_E_INVAL, "pass both pool pointers or neither");
+  if (k_pool && (!aligned(k_pool, 256) || !aligned(v_pool, 256)))
+    return fail(nullptr, KVC_E_INVAL, "pool pointers must be 256-byte aligned");
+  kvc_handle h = new_handle(L, B, H_kv, d_h, max_len, dtype);
+  if (!h) return fail(nullptr, KVC_E_NOMEM, "host allocation failed");
+  h->paged = true;
+  h->block = block_size;
+  h->block_shift = __builtin_ctz(static_cast<unsigned>(block_size));
+  h->n_blocks = n_blocks;
+  h->max_blocks = static_cast<int>(max_blocks);
+  h->table.assign(static_cast<size_t>(B) * h->max_blocks, -1);
+  h->held.assign(B, 0);
+  h->free_heap.resize(n_blocks);
+  for (int i = 0; i < n_blocks; ++i) h->free_heap[i] = i;   // ascending order is already a min-heap
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = store_bytes(h);
+  if (k_pool) {
+    h->k = k_pool;
+    h->v = v_pool;
+  } else {
+    h->owns_store = true;
+    cudaError_t e = cudaMalloc(&h->k, bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&h->v, bytes);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->k, 0, bytes, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->v, 0, bytes, st);
+    if (e != cudaSuccess) {
+      rc = fail(nullptr, KVC_E_NOMEM, "pool allocation of 2 x %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+      cudaGetLastError();
+      release(h);
+      return rc;
+    }
+  }
+  rc = init_device_state(h, st);
+  if (rc) {
+    g_err = h->err;
+    release(h);
+    return rc;
+  }
+  *out = h;
+  return KVC_OK;
+}
+
+int kvc_block_table(kvc_handle h, int32_t* table_host, int32_t* n_free_host) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (!h->paged) return fail(h, KVC_E_INVAL, "not a paged cache");
+  if (table_host) memcpy(table_host, h->table.data(), sizeof(int32_t) * h->table.size());
+  if (n_free_host) *n_free_host = static_cast<int32_t>(h->free_heap.size());
+  return KVC_OK;
+}
+
 int kvc_destroy(kvc_handle h) {
   release(h);
   return KVC_OK;
@@ -376,10 +515,15 @@ int kvc_append(kvc_handle h, int layer, const void* k_new, const void* v_new, kv
     if (end > h->max_len)
       return fail(h, KVC_E_CAPACITY, "sequence %d: %lld positions exceed max_len=%d", b, end, h->max_len);
   }
+  if (h->paged) {
+    rc = paged_grow(h, layer, T, static_cast<cudaStream_t>(stream));
+    if (rc) return rc;
+  }
   kvc::AppendArgs a{};
   a.k_store = h->k; a.v_store = h->v; a.k_new = k_new; a.v_new = v_new; a.lens = h->d_lens;
   a.layer = layer; a.B = h->B; a.H = h->H; a.D = h->D; a.T = T; a.max_len = h->max_len;
   a.delta = delta; a.cache_dtype = h->dtype; a.in_dtype = in_dtype;
+  a.pg = kvc_paging(h);
   cudaError_t e = kvc::launch_append(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "append launch");
   h->launches += 1;
@@ -414,9 +558,21 @@ int kvc_truncate_ragged(kvc_handle h, const int32_t* n, void* stream) {
     if (n[b] > h->lens[b])
       return fail(h, KVC_E_STATE, "sequence %d: truncate to %d beyond committed length %d", b, n[b], h->lens[b]);
   }
-  cudaError_t e = kvc::launch_lens_set(h->d_lens, h->B, n, static_cast<cudaStream_t>(stream));
+  std::vector<std::pair<int32_t, int32_t>>& edits = h->edit_scratch;
+  edits.clear();
+  if (h->paged)                                       // blocks wholly past the new length go back
+    for (int b = 0; b < h->B; ++b)
+      for (int i = blocks_for(h, n[b]); i < h->held[b]; ++i) edits.push_back({b * h->max_blocks + i, -1});
+  cudaError_t e = send_edits(h, edits, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = kvc::launch_lens_set(h->d_lens, h->B, n, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "truncate launch");
   h->launches += 1;
+  for (const auto& ed : edits) {
+    push_free(h, h->table[ed.first]);
+    h->table[ed.first] = -1;
+  }
+  if (h->paged)
+    for (int b = 0; b < h->B; ++b) h->held[b] = std::min(h->held[b], blocks_for(h, n[b]));
   for (int b = 0; b < h->B; ++b) {
     h->lens[b] = n[b];
     for (int l = 0; l < h->L; ++l) h->fill[static_cast<size_t>(l) * h->B + b] = n[b];
@@ -455,7 +611,7 @@ size_t kvc_nbytes(kvc_handle h) { return h ? 2 * store_bytes(h) : 0; }
 int kvc_layer_ptrs(kvc_handle h, int layer, void** k, void** v) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
   if (layer < 0 || layer >= h->L || !k || !v) return fail(h, KVC_E_INVAL, "bad layer or null output");
-  const size_t off = static_cast<size_t>(layer) * h->B * h->H * h->max_len * h->D * kvc::itemsize(h->dtype);
+  const size_t off = store_bytes(h) / h->L * layer;
   *k = static_cast<char*>(h->k) + off;
   *v = static_cast<char*>(h->v) + off;
   return KVC_OK;
@@ -509,6 +665,7 @@ int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, i
   a.lens = h->d_lens; a.status = h->d_status;
   a.layer = layer; a.B = h->B; a.H_kv = h->H; a.H_q = H_q; a.G = G; a.T = T; a.D = h->D;
   a.max_len = h->max_len; a.delta = T; a.cache_dtype = h->dtype;
+  a.pg = kvc_paging(h);
   cudaError_t e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
   h->launches += 1;

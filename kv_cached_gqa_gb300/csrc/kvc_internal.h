@@ -23,6 +23,23 @@ inline int itemsize(kvc_dtype t) { return t == KVC_F32 ? 4 : 2; }
 // Device status word values written by kernels whose bounded waits give up.
 constexpr int kStatusTimeout = 1;
 
+// Where a store keeps its rows. A contiguous store is [L, B, H, max_len, D]. A paged store is a
+// pool of fixed-size blocks, [L, n_blocks, H, block, D], and a block table [B, max_blocks] that maps
+// each sequence's logical block i (positions [i * block, (i + 1) * block)) to a physical block, the
+// same one in every layer; -1 marks a logical block that holds no physical block.
+struct Paging {
+  const int32_t* table = nullptr;   // device block table; nullptr for a contiguous store
+  int max_blocks = 0;               // table row width = ceil(max_len / block)
+  int block_shift = 0;              // log2(block)
+  int n_blocks = 0;                 // physical blocks in the pool
+};
+
+// Tile row split of a paged store: keys per TMA box (a tile of `tile` keys takes tile / box_rows
+// boxes per 128-byte column when blocks are shorter than the tile).
+inline int paged_box_rows(const Paging& pg, int tile) {
+  return pg.table ? (tile < (1 << pg.block_shift) ? tile : (1 << pg.block_shift)) : tile;
+}
+
 // ------------------------------------------------------------------------------------------------
 // Append: writes a [B, H, T, D] chunk at row lens[b] + delta + t of each (layer, b, h).
 // ------------------------------------------------------------------------------------------------
@@ -35,8 +52,18 @@ struct AppendArgs {
   int layer, B, H, D, T, max_len;
   int delta;                // this layer's fill minus the committed length (uniform over b)
   kvc_dtype cache_dtype, in_dtype;
+  Paging pg;                // paged store: rows go through the block table
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
+
+// Block-table edits: table[slot[i]] = value[i], applied in one launch before the call that needs them.
+constexpr int kMaxTableEdits = 1024;
+struct TableEdits {
+  int n;
+  int32_t slot[kMaxTableEdits];
+  int32_t value[kMaxTableEdits];
+};
+cudaError_t launch_table_edits(int32_t* table, const TableEdits& e, cudaStream_t st);
 
 // lens[b] += delta for all b
 cudaError_t launch_lens_add(int32_t* lens, int B, int delta, cudaStream_t st);
@@ -71,6 +98,7 @@ struct AttnArgs {
   int layer, B, H_kv, H_q, G, T, D, max_len;
   int delta;                // fill - committed for this layer (== T when the chunk was appended)
   kvc_dtype cache_dtype;
+  Paging pg;                // paged store: tiles are gathered through the block table
 };
 // Workspace floats the plan needs (0 when no unit splits).
 size_t splitk_workspace_floats(const SplitPlan& p, int D);
@@ -103,9 +131,21 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
 cudaError_t launch_attention(const AttnPlan& ap, const AttnArgs& a, const SplitPlan& p, kvc_handle h,
                              cudaStream_t st);
 
-// Tensor map over a store viewed as [L*B*H, max_len, D] with boxes of (swizzle span, box_rows, 1).
-bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max_len,
+// Tensor map over a store viewed as [planes, rows, D] with boxes of (swizzle span, box_rows, 1):
+// planes = L*B*H and rows = max_len for a contiguous store, planes = L*n_blocks*H and rows = block
+// for a paged pool.
+bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int rows,
                       long long planes, int box_rows, std::string* err);
+
+// Keys per split when a unit's n keys are cut into nsplit splits (split i covers [i * chunk, (i + 1) *
+// chunk) clipped to n): the near-equal share rounded up to whole tiles, so every split starts on a
+// tile boundary and a paged tile never straddles two blocks at an odd offset. If nsplit = ceil(n /
+// chunk) for a chunk computed this way, recomputing the chunk from nsplit gives it back, so the host
+// planner and the kernels agree and no split is empty.
+__host__ __device__ inline int split_chunk(int n, int nsplit, int tile) {
+  const int share = (n + nsplit - 1) / nsplit;
+  return (share + tile - 1) / tile * tile;
+}
 
 // Launch with programmatic stream serialization: the kernel may be scheduled before its stream
 // predecessor finishes and orders itself with griddepcontrol.wait (see kvc_device.cuh).
@@ -147,6 +187,14 @@ struct kvc_cache {
   int L = 0, B = 0, H = 0, D = 0, max_len = 0;
   kvc_dtype dtype = KVC_F32;
   bool owns_store = false;
+  // paged store: pool blocks, device table and its host mirror, and the free list
+  bool paged = false;
+  int block = 0, block_shift = 0, n_blocks = 0, max_blocks = 0;
+  int32_t* d_table = nullptr;     // [B * max_blocks]
+  std::vector<int32_t> table;     // host mirror
+  std::vector<int32_t> held;      // blocks each sequence holds (logical blocks 0 .. held-1)
+  std::vector<int32_t> free_heap; // free physical blocks, a min-heap: the lowest is handed out first
+  std::vector<std::pair<int32_t, int32_t>> edit_scratch;   // (slot, value) table edits of one call
   void* k = nullptr;
   void* v = nullptr;
   int32_t* d_lens = nullptr;      // committed lengths on the device
@@ -169,3 +217,15 @@ struct kvc_cache {
   int device = 0;
   std::string err;
 };
+
+// The store addressing the kernels of a handle use.
+inline kvc::Paging kvc_paging(const kvc_cache* h) {
+  kvc::Paging pg;
+  if (h->paged) {
+    pg.table = h->d_table;
+    pg.max_blocks = h->max_blocks;
+    pg.block_shift = h->block_shift;
+    pg.n_blocks = h->n_blocks;
+  }
+  return pg;
+}

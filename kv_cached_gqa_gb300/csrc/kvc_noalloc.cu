@@ -127,6 +127,7 @@ extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_
   a.lens = h->d_lens; a.status = h->d_status;
   a.layer = layer; a.B = h->B; a.H_kv = h->H; a.H_q = H_q; a.G = G; a.T = T; a.D = h->D;
   a.max_len = h->max_len; a.delta = T; a.cache_dtype = h->dtype;
+  a.pg = kvc_paging(h);
   e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return set_err(h, KVC_E_CUDA, "attention launch: %s", cudaGetErrorString(e));
   h->launches += 1;

@@ -147,7 +147,6 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int rt = plan.unit_b[unit] % plan.n_rowtiles;
   const int row0 = rt * kRows;
   const int nrows = min(kRows, a.T * a.G - row0);
-  const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
 
   // ---- set-up ------------------------------------------------------------------------------------
   if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&ctl->tmem));
@@ -200,26 +199,28 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   volatile int* abort_flag = &ctl->abort;
 
   if (warp == 0) {
-    // ---------------------------------- TMA producer: K0, V0, K1, V1, ... ---------------------------
+    // ---------------------------------- TMA producer (whole warp): K0, V0, K1, V1, ... -------------
     if (lane == 0) {
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      int issued = 0;
-      for (int i = 0; i < 2 * nkt; ++i) {
-        const int st = i % kStages;
-        if (!mbar_wait(smem_u32(&ctl->empty[st]), ((i / kStages) & 1) ^ 1, abort_flag)) break;
-        const uint32_t full = smem_u32(&ctl->full[st]);
-        mbar_expect_tx(full, kTile);
-        const uint32_t dst = s_ring + st * kTile;
-        const CUtensorMap* map = (i & 1) ? &tv : &tk;
-        const int y = (i >> 1) * kKeys;
-        tma_load_3d(dst, map, 0, y, plane, full);
-        tma_load_3d(dst + kBox, map, 64, y, plane, full);
-        issued = i + 1;
+    }
+    int issued = 0;
+    for (int i = 0; i < 2 * nkt; ++i) {
+      const int st = i % kStages;
+      const TilePiece pc = tile_piece<kKeys>(a, b, kvh, (i >> 1) * kKeys, lane);
+      const uint32_t full = smem_u32(&ctl->full[st]);
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(smem_u32(&ctl->empty[st]), ((i / kStages) & 1) ^ 1, abort_flag);
+        if (ok) mbar_expect_tx(full, kTile);
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      issue_piece<kKeys, 2, 128, 64>(pc, (i & 1) ? &tv : &tk, s_ring + st * kTile, full, lane);
+      issued = i + 1;
+    }
+    if (lane == 0)
       for (int i = max(0, issued - kStages); i < issued; ++i)
         mbar_drain(smem_u32(&ctl->full[i % kStages]), (i / kStages) & 1);
-    }
   } else if (warp == 1) {
     // ---------------------------------- MMA issuer ------------------------------------------------
     if (lane == 0) {

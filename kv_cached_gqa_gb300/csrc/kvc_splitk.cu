@@ -188,7 +188,6 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int R = a.T * a.G;                              // query rows of this K/V head
   const int row0 = rt * RMAX;
   const int nrows = min(RMAX, R - row0);
-  const int plane = (a.layer * a.B + b) * a.H_kv + kvh;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -204,7 +203,7 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int s_b = a.lens[b] + a.delta - a.T;            // committed length = first query position
   const int t_max = (row0 + nrows - 1) / a.G;
   const int n_eff = s_b + t_max + 1;                    // keys visible to the tile's last row
-  const int chunk = (n_eff + nsplit - 1) / nsplit;      // near-equal splits of the unit's keys
+  const int chunk = split_chunk(n_eff, nsplit, C::TILE);  // near-equal, whole-tile splits of the unit's keys
   const int k_begin = split * chunk;
   const int k_end = min(k_begin + chunk, n_eff);
   const int n_keys = k_end - k_begin;
@@ -228,21 +227,24 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   if (warp == kConsumerWarps) {
     // ---------------------------------- producer ------------------------------------------
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<unsigned long long>(&tk)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<unsigned long long>(&tv)) : "memory");
-      for (int i = 0; i < 2 * nkt; ++i) {
-        const int st = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (!mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1, abort_flag)) break;
-        const bool isv = i >= nkt;
-        const int y = k_begin + (isv ? i - nkt : i) * C::TILE;
-        const uint32_t full = smem_u32(&sm->full[st]);
-        mbar_expect_tx(full, kTileBytes);
-        const uint32_t dst = smem_u32(tiles + st * kTileBytes);
-#pragma unroll
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          tma_load_3d(dst + bx * C::TILE * C::SW, isv ? &tv : &tk, bx * C::BOX_INNER, y, plane, full);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+    }
+    for (int i = 0; i < 2 * nkt; ++i) {
+      const int st = i % kStages;
+      const uint32_t ph = (i / kStages) & 1;
+      const bool isv = i >= nkt;
+      const int y = k_begin + (isv ? i - nkt : i) * C::TILE;
+      const TilePiece pc = tile_piece<C::TILE>(a, b, kvh, y, lane);   // a block-table read overlaps the wait
+      const uint32_t full = smem_u32(&sm->full[st]);
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1, abort_flag);
+        if (ok) mbar_expect_tx(full, kTileBytes);
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      issue_piece<C::TILE, C::NBOX, C::SW, C::BOX_INNER>(pc, isv ? &tv : &tk, smem_u32(tiles + st * kTileBytes), full,
+                                                       lane);
     }
     return;
   }

@@ -36,6 +36,7 @@ class WorkloadSpec:
     lengths: np.ndarray
     T: int = 1
     seed: int = 0
+    block: int = 0          # paged cache block (positions); 0 = contiguous cache
 
     @property
     def S0(self) -> int:
@@ -103,7 +104,7 @@ def spec(name: str, seed: int = 0) -> WorkloadSpec:
     else:
         lengths = np.full(w["B"], w["s"], dtype=np.int64)
     return WorkloadSpec(name, w["L"], w["B"], w["H_q"], w["H_kv"], w["d_h"], w["max_len"], w["dtype"],
-                        lengths, T=w["T"], seed=seed)
+                        lengths, T=w["T"], seed=seed, block=w.get("block", 0))
 
 
 class GpuWorkload:
@@ -113,7 +114,12 @@ class GpuWorkload:
         import torch
         from kv_cached_gqa_gb300 import _binding as kb
         self.torch, self.kb, self.spec, self.device = torch, kb, sp, device
-        self.cache = kb.Cache(sp.L, sp.B, sp.H_kv, sp.d_h, sp.max_len, DTYPE_CODE[sp.dtype], device=device)
+        if sp.block:
+            n_blocks = sp.B * (-(-sp.max_len // sp.block))
+            self.cache = kb.PagedCache(sp.L, sp.B, sp.H_kv, sp.d_h, sp.max_len, sp.block, n_blocks,
+                                       DTYPE_CODE[sp.dtype], device=device)
+        else:
+            self.cache = kb.Cache(sp.L, sp.B, sp.H_kv, sp.d_h, sp.max_len, DTYPE_CODE[sp.dtype], device=device)
 
     def __getattr__(self, name):                      # shape fields and host redraws of the spec
         return getattr(self.__dict__["spec"], name)
@@ -124,13 +130,22 @@ class GpuWorkload:
         return t
 
     def prefill(self):
-        """Append S0 rows to every layer, commit, then truncate each sequence to s_b."""
+        """Append S0 rows to every layer, commit, then truncate each sequence to s_b. A paged cache
+        takes the rows one block of positions per append, so layer 0's appends hand each sequence one
+        block in turn (the later layers reuse the same blocks) and a sequence's blocks end up B blocks
+        apart in the pool."""
         sp, kb = self.spec, self.kb
         shape = (sp.B, sp.H_kv, sp.S0, sp.d_h)
+        chunk = sp.block or sp.S0
         for layer in range(sp.L):
             k = self.draw(shape, stream_id(STREAM_K_PREFILL, layer))
             v = self.draw(shape, stream_id(STREAM_V_PREFILL, layer))
-            kb.kvc_append(self.cache, layer, k, v)
+            for c0 in range(0, sp.S0, chunk):
+                c1 = min(sp.S0, c0 + chunk)
+                if c0 == 0 and c1 == sp.S0:
+                    kb.kvc_append(self.cache, layer, k, v)
+                else:
+                    kb.kvc_append(self.cache, layer, k[:, :, c0:c1].contiguous(), v[:, :, c0:c1].contiguous())
             del k, v
         kb.kvc_commit(self.cache)
         kb.kvc_truncate_ragged(self.cache, [int(x) for x in sp.lengths])

@@ -21,13 +21,17 @@ It computes the plain definitions, in float64, one (sequence, head) at a time:
   order [0, 0, 1, 1] for 4 query and 2 K/V heads ("Heads, GQA and K/V cache",
   "Four queries, two sets of K/V");
 * the uncached full recompute that the cached path must equal ("KV cache
-  decoding", "Why the causal mask makes caching exact").
+  decoding", "Why the causal mask makes caching exact");
+* the paged cache: fixed-size blocks and a per-sequence block table ("KV cache decoding",
+  "Batching caches of different lengths").
 
 Readings where the pages are silent (each listed in the design doc):
 * rounding to float16/bfloat16 is round-to-nearest-even; NaN inputs are out of scope;
 * a query for a 16-bit cache is rounded to the cache dtype before use;
 * `commit` is explicit and requires every layer's fill to agree per sequence;
-* `truncate(n)` requires n <= the committed length and leaves stale rows in place.
+* `truncate(n)` requires n <= the committed length and leaves stale rows in place;
+* the paged cache hands out the lowest-numbered free block first and frees, on truncate, every
+  block wholly past the new length.
 
 Parity status: every function here is pinned by `tests/test_oracle_pins.py`.
 """
@@ -209,6 +213,142 @@ class OracleKVCache:
 
 
 # ----------------------------------------------------------------------------------------------
+# The paged cache ("KV cache decoding", "Batching caches of different lengths": the cache kept in
+# fixed-size blocks with a table from each request to its blocks, a new block taken only when the
+# sequence grows into it and its blocks freed when it ends; "KV cache, incremental decode, ...",
+# Key Takeaways and §2.5: a float16 paged cache stores what the contiguous one stores and compares
+# with it exactly).
+# ----------------------------------------------------------------------------------------------
+
+class OraclePagedKVCache:
+    """Block pool (L, n_blocks, H_kv, block, d_h) plus a block table (B, ceil(max_len / block)).
+
+    Position p of sequence b lives at row p % block of physical block table[b, p // block], the same
+    block in every layer. Readings where the pages leave the policy open:
+    * blocks are handed out lowest-numbered free block first, sequences in order, then logical
+      blocks in order, when an append's new fill reaches them;
+    * truncate returns every block wholly past the new length; a partly filled block stays;
+    * a pool too small for an append raises OverflowError, like the max_len check, changing nothing.
+    Lengths, commit and the errors are those of OracleKVCache.
+    """
+
+    def __init__(self, n_layers: int, batch: int, n_kv_heads: int, d_head: int, max_len: int,
+                 block: int, n_blocks: int, dtype: str = "f32"):
+        if dtype not in DTYPES:
+            raise ValueError(f"unknown dtype {dtype!r}")
+        if min(n_layers, batch, n_kv_heads, d_head, max_len, block, n_blocks) <= 0:
+            raise ValueError("all sizes must be positive")
+        self.L, self.B, self.H, self.d, self.max_len, self.dtype = (
+            n_layers, batch, n_kv_heads, d_head, max_len, dtype)
+        self.block, self.n_blocks = block, n_blocks
+        self.max_blocks = -(-max_len // block)
+        shape = (n_layers, n_blocks, n_kv_heads, block, d_head)
+        self.k = np.zeros(shape, dtype=storage_np_dtype(dtype))
+        self.v = np.zeros(shape, dtype=storage_np_dtype(dtype))
+        self.table = np.full((batch, self.max_blocks), -1, dtype=np.int64)
+        self.free = set(range(n_blocks))
+        self.fill = np.zeros((n_layers, batch), dtype=np.int64)
+        self.lens = np.zeros(batch, dtype=np.int64)
+
+    # -- blocks ----------------------------------------------------------------------------
+    def held(self, b: int) -> int:
+        """Logical blocks sequence b holds (they are always 0 .. held-1)."""
+        return int(np.sum(self.table[b] >= 0))
+
+    def blocks_for(self, n: int) -> int:
+        return -(-int(n) // self.block)
+
+    def take_block(self) -> int:
+        """Remove and return the lowest-numbered free block."""
+        blk = min(self.free)
+        self.free.remove(blk)
+        return blk
+
+    def where(self, b: int, p):
+        """(physical block, row) of position(s) p of sequence b."""
+        p = np.asarray(p)
+        return self.table[b, p // self.block], p % self.block
+
+    # -- lengths (as OracleKVCache) -------------------------------------------------------------
+    def seq_len(self, layer: int | None = None) -> np.ndarray:
+        if layer is None:
+            return self.fill.min(axis=0).copy()
+        return self.fill[layer].copy()
+
+    def committed(self) -> np.ndarray:
+        return self.lens.copy()
+
+    def positions(self, T: int) -> np.ndarray:
+        return self.lens[:, None] + np.arange(T)[None, :]
+
+    # -- writes ----------------------------------------------------------------------------
+    def append(self, layer: int, k_new, v_new):
+        """Write a [B, H_kv, T, d_h] chunk at each sequence's fill, taking blocks as it grows."""
+        if not 0 <= layer < self.L:
+            raise ValueError("layer out of range")
+        k_new = np.asarray(k_new)
+        v_new = np.asarray(v_new)
+        if k_new.ndim != 4 or k_new.shape != v_new.shape:
+            raise ValueError("k_new and v_new must both be [B, H_kv, T, d_h]")
+        B, H, T, d = k_new.shape
+        if (B, H, d) != (self.B, self.H, self.d):
+            raise ValueError("shape mismatch")
+        if np.any(self.fill[layer] + T > self.max_len):
+            raise OverflowError("append would exceed max_len")
+        need = [max(0, self.blocks_for(self.fill[layer, b] + T) - self.held(b)) for b in range(B)]
+        if sum(need) > len(self.free):
+            raise OverflowError("block pool exhausted")
+        for b in range(B):
+            for i in range(self.held(b), self.held(b) + need[b]):
+                self.table[b, i] = self.take_block()
+        kq = store_round(k_new, self.dtype)
+        vq = store_round(v_new, self.dtype)
+        for b in range(B):
+            blk, row = self.where(b, int(self.fill[layer, b]) + np.arange(T))
+            self.k[layer, blk, :, row] = kq[b].transpose(1, 0, 2)     # [T, H, d] rows
+            self.v[layer, blk, :, row] = vq[b].transpose(1, 0, 2)
+        self.fill[layer] += T
+        out = []
+        for b in range(B):
+            n = int(self.fill[layer, b])
+            ks = np.stack([self.stored_f64(layer, b, h, n)[0] for h in range(H)])
+            vs = np.stack([self.stored_f64(layer, b, h, n)[1] for h in range(H)])
+            out.append((ks, vs))
+        return out
+
+    def commit(self) -> None:
+        if np.any(self.fill != self.fill[0][None, :]):
+            raise RuntimeError("commit with unequal per-layer fills")
+        self.lens = self.fill[0].copy()
+
+    def truncate(self, n) -> None:
+        """Set every fill and committed length to n; blocks wholly past n go back to the pool."""
+        n = np.broadcast_to(np.asarray(n, dtype=np.int64), (self.B,)).copy()
+        if np.any(n < 0):
+            raise ValueError("negative length")
+        if np.any(n > self.lens):
+            raise RuntimeError("truncate beyond the committed length")
+        for b in range(self.B):
+            for i in range(self.blocks_for(n[b]), self.max_blocks):
+                if self.table[b, i] >= 0:
+                    self.free.add(int(self.table[b, i]))
+                    self.table[b, i] = -1
+        self.fill[:, :] = n[None, :]
+        self.lens = n
+
+    # -- sizes and reads -------------------------------------------------------------------
+    def nbytes(self) -> int:
+        """Pool capacity: 2 * L * n_blocks * H_kv * block * d_h * itemsize."""
+        return 2 * self.L * self.n_blocks * self.H * self.block * self.d * ITEMSIZE[self.dtype]
+
+    def stored_f64(self, layer: int, b: int, kvh: int, n: int):
+        """Float64 rows 0 .. n-1 of one (layer, sequence, K/V head), gathered through the table."""
+        blk, row = self.where(b, np.arange(n))
+        return (stored_to_f64(self.k[layer, blk, kvh, row], self.dtype),
+                stored_to_f64(self.v[layer, blk, kvh, row], self.dtype))
+
+
+# ----------------------------------------------------------------------------------------------
 # Attention
 # ----------------------------------------------------------------------------------------------
 
@@ -243,8 +383,8 @@ def query_as_f64(q, dtype: str) -> np.ndarray:
     return q.astype(np.float64)
 
 
-def gqa_cached_attention(cache: OracleKVCache, layer: int, q, T: int | None = None) -> np.ndarray:
-    """Attend a chunk's queries over every stored row of one layer.
+def gqa_cached_attention(cache, layer: int, q, T: int | None = None) -> np.ndarray:
+    """Attend a chunk's queries over every stored row of one layer (OracleKVCache or OraclePagedKVCache).
 
     q is [B, H_q, T, d_h]. The layer must already hold the chunk (fill = s_b + T, with s_b the
     committed length). Query head h of sequence b reads K/V head h // G, G = H_q / H_kv, and

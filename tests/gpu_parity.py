@@ -8,7 +8,7 @@ from __future__ import annotations
 import numpy as np
 
 import kvc_synth
-from oracle.kvc_oracle import OracleKVCache, gqa_cached_attention
+from oracle.kvc_oracle import OracleKVCache, OraclePagedKVCache, gqa_cached_attention
 
 DT = {"f32": 0, "f16": 1, "bf16": 2}
 FP32_ATOL = 1e-5        # float32 caches: absolute, every output element
@@ -31,15 +31,22 @@ def check_outputs(got: np.ndarray, want: np.ndarray, dtype: str, what: str = "")
 
 
 class Mirror:
-    """A GPU cache and an oracle cache driven by the same calls."""
+    """A GPU cache and an oracle cache driven by the same calls (paged when `block` is given: a pool of
+    `n_blocks` blocks, by default enough for every sequence at max_len)."""
 
-    def __init__(self, L, B, H_kv, d_h, max_len, dtype, seed=0):
+    def __init__(self, L, B, H_kv, d_h, max_len, dtype, seed=0, block=None, n_blocks=None):
         import torch
         from kv_cached_gqa_gb300 import _binding as kb
         self.torch, self.kb = torch, kb
         self.L, self.B, self.H, self.d, self.max_len, self.dtype, self.seed = L, B, H_kv, d_h, max_len, dtype, seed
-        self.gpu = kb.Cache(L, B, H_kv, d_h, max_len, DT[dtype])
-        self.ref = OracleKVCache(L, B, H_kv, d_h, max_len, dtype)
+        self.paged = block is not None
+        if self.paged:
+            n_blocks = n_blocks or B * (-(-max_len // block))
+            self.gpu = kb.PagedCache(L, B, H_kv, d_h, max_len, block, n_blocks, DT[dtype])
+            self.ref = OraclePagedKVCache(L, B, H_kv, d_h, max_len, block, n_blocks, dtype)
+        else:
+            self.gpu = kb.Cache(L, B, H_kv, d_h, max_len, DT[dtype])
+            self.ref = OracleKVCache(L, B, H_kv, d_h, max_len, dtype)
         self.n_draws = 0
 
     def draw(self, shape):
@@ -114,6 +121,10 @@ class Mirror:
             assert self.kb.kvc_seq_len(self.gpu, layer) == [int(x) for x in self.ref.seq_len(layer)]
         pos = self.kb.kvc_positions(self.gpu, 3).cpu().numpy()
         np.testing.assert_array_equal(pos, self.ref.positions(3))
+        if self.paged:
+            table, n_free = self.kb.kvc_block_table(self.gpu)
+            np.testing.assert_array_equal(np.array(table), self.ref.table)
+            assert n_free == len(self.ref.free)
 
     def close(self):
         self.gpu.close()

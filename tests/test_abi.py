@@ -33,7 +33,8 @@ def lib():
 def test_headers_declare_the_entry_points():
     names = declared_symbols()
     for n in ("kvc_create", "kvc_append", "kvc_commit", "kvc_truncate", "kvc_nbytes", "gqa_cached_attn",
-              "kvc_truncate_ragged", "kvc_seq_len", "kvc_positions", "kvc_layer_ptrs", "kvc_status"):
+              "kvc_truncate_ragged", "kvc_seq_len", "kvc_positions", "kvc_layer_ptrs", "kvc_status",
+              "kvc_create_paged", "kvc_block_table"):
         assert n in names
 
 
@@ -75,6 +76,17 @@ def test_host_validation_without_gpu(lib):
                lib.kvc_status(None, None), lib.kvc_set_split_keys(None, 0)):
         assert rc == -1
     assert "null handle" in _err(lib)
+    # paged: rejected before any CUDA call
+    assert lib.kvc_create_paged(ctypes.byref(h), 1, 1, 1, 64, 64, 24, 8, 1, None, None, None) == -1   # not 2^k
+    assert "power of two" in _err(lib)
+    assert lib.kvc_create_paged(ctypes.byref(h), 1, 1, 1, 64, 64, 8, 8, 1, None, None, None) == -1    # < 16
+    assert lib.kvc_create_paged(ctypes.byref(h), 1, 1, 1, 64, 64, 16, 0, 1, None, None, None) == -1   # no blocks
+    assert lib.kvc_create_paged(ctypes.byref(h), 1, 1, 1, 64, 64, 16, 8, 1, 256, None, None) == -1    # one pool
+    assert lib.kvc_create_paged(ctypes.byref(h), 1, 1, 1, 64, 64, 16, 8, 1, 16, 512, None) == -1      # misaligned
+    assert lib.kvc_create_paged(ctypes.byref(h), 1, 1, 1, 48, 64, 16, 8, 1, None, None, None) == -6   # d_h 48
+    assert lib.kvc_create_paged(None, 1, 1, 1, 64, 64, 16, 8, 1, None, None, None) == -1
+    assert h.value is None
+    assert lib.kvc_block_table(None, None, None) == -1
 
 
 def test_binding_fails_loudly_when_library_missing(monkeypatch, tmp_path):

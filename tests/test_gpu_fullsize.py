@@ -41,10 +41,15 @@ def _run_and_sample(wl, samples):
         want = gqa_cached_attention(ref, 0, qh[None])
         got = outs[layer][b, kvh * G:(kvh + 1) * G].cpu().numpy()[None]
         check_outputs(got, want, wl.dtype, f"layer {layer} b {b} kvh {kvh}")
-        stored = wl.cache.k[layer, b, kvh, :s_b + wl.T].view(view).cpu().numpy()
-        np.testing.assert_array_equal(stored, ref.k[0, 0, 0].view(stored.dtype))
-        stored = wl.cache.v[layer, b, kvh, :s_b + wl.T].view(view).cpu().numpy()
-        np.testing.assert_array_equal(stored, ref.v[0, 0, 0].view(stored.dtype))
+        for store, want_rows in ((wl.cache.k, ref.k[0, 0, 0]), (wl.cache.v, ref.v[0, 0, 0])):
+            if wl.block:                        # gather the sequence's rows through its block table
+                p = torch.arange(s_b + wl.T)
+                blk = torch.tensor(kb.kvc_block_table(wl.cache)[0][b])[p // wl.block]
+                stored = store[layer][blk.cuda(), kvh, (p % wl.block).cuda()]
+            else:
+                stored = store[layer, b, kvh, :s_b + wl.T]
+            stored = stored.contiguous().view(view).cpu().numpy()
+            np.testing.assert_array_equal(stored, want_rows.view(stored.dtype))
     assert kb.kvc_seq_len(wl.cache) == [int(x) + wl.T for x in wl.lengths]
     wl.close()
 
@@ -73,3 +78,11 @@ def test_llama3_8b_prefill_chunk_fp16_full_size():
     """Prefill chunk, fp16: H_q=32, H_kv=8, d_h=128, B=16, T=512 at s=1024."""
     _run_and_sample(kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-prefill-fp16")),
                     [(0, 0, 0), (31, 15, 7), (16, 4, 3)])
+
+
+def test_llama3_8b_decode_bf16_paged16_full_size():
+    """The Llama-3-8B-shaped ragged decode batch in a paged cache of 16-position blocks, each
+    sequence's blocks B apart in the pool."""
+    wl = kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-decode-bf16-paged16"))
+    lo, hi = int(np.argmin(wl.lengths)), int(np.argmax(wl.lengths))
+    _run_and_sample(wl, [(0, lo, 0), (31, hi, 7), (13, 17, 3)])

@@ -113,3 +113,39 @@ def test_bf16_truncation_instead_of_rounding_is_caught(monkeypatch):
 
     monkeypatch.setattr(pins, "store_round", truncating)
     _fails(pins.test_storage_rounding_golden, "bf16")
+
+
+# ---- the paged oracle ("KV cache decoding", "Batching caches of different lengths") ------------------
+from tests import test_oracle_paged as paged_pins
+
+
+def test_paged_rows_reversed_within_a_block_are_caught(monkeypatch):
+    """Rows stored from the end of each block: reads stay consistent, the layout does not."""
+    def where_reversed(self, b, p):
+        p = np.asarray(p)
+        return self.table[b, p // self.block], self.block - 1 - p % self.block
+
+    monkeypatch.setattr(ko.OraclePagedKVCache, "where", where_reversed)
+    _fails(paged_pins.test_paged_hand_example)
+
+
+def test_paged_truncate_that_frees_nothing_is_caught(monkeypatch):
+    """Blocks kept past the new length: the memory paging should recover stays taken."""
+    def truncate_keep_blocks(self, n):
+        n = np.broadcast_to(np.asarray(n, dtype=np.int64), (self.B,)).copy()
+        self.fill[:, :] = n[None, :]
+        self.lens = n
+
+    monkeypatch.setattr(ko.OraclePagedKVCache, "truncate", truncate_keep_blocks)
+    _fails(paged_pins.test_paged_holds_exactly_the_blocks_its_rows_reach, 4)
+
+
+def test_paged_highest_block_first_is_caught(monkeypatch):
+    """A different allocation order than the stated lowest-free-first reading."""
+    def take_highest(self):
+        blk = max(self.free)
+        self.free.remove(blk)
+        return blk
+
+    monkeypatch.setattr(ko.OraclePagedKVCache, "take_block", take_highest)
+    _fails(paged_pins.test_paged_allocation_order_by_hand)
