@@ -66,7 +66,7 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("kvc_decode_tc.cu", "kvc_splitk.cu", "kvc_device.cuh", "kvc_host.cpp")
+KERNEL_SOURCES = ("kvc_decode_tc.cu", "kvc_splitk.cu", "kvc_device.cuh", "kvc_host.cpp", "kvc_internal.h")
 
 
 def kernel_source_hash():
