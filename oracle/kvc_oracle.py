@@ -23,7 +23,10 @@ It computes the plain definitions, in float64, one (sequence, head) at a time:
 * the uncached full recompute that the cached path must equal ("KV cache
   decoding", "Why the causal mask makes caching exact");
 * the paged cache: fixed-size blocks and a per-sequence block table ("KV cache decoding",
-  "Batching caches of different lengths").
+  "Batching caches of different lengths");
+* rotary positions applied to the keys before they are stored and to the queries before they
+  attend ("KV cache decoding", "Position information with a cache"; the formula is the RoFormer
+  paper's, which the pages name but do not print).
 
 Readings where the pages are silent (each listed in the design doc):
 * rounding to float16/bfloat16 is round-to-nearest-even; NaN inputs are out of scope;
@@ -31,7 +34,9 @@ Readings where the pages are silent (each listed in the design doc):
 * `commit` is explicit and requires every layer's fill to agree per sequence;
 * `truncate(n)` requires n <= the committed length and leaves stale rows in place;
 * the paged cache hands out the lowest-numbered free block first and frees, on truncate, every
-  block wholly past the new length.
+  block wholly past the new length;
+* RoPE: theta_i = base^(-2i/d) with pairs (i, i + d/2) or (2i, 2i + 1); a rotated row is rounded to
+  float32 before the cache dtype.
 
 Parity status: every function here is pinned by `tests/test_oracle_pins.py`.
 """
@@ -346,6 +351,60 @@ class OraclePagedKVCache:
         blk, row = self.where(b, np.arange(n))
         return (stored_to_f64(self.k[layer, blk, kvh, row], self.dtype),
                 stored_to_f64(self.v[layer, blk, kvh, row], self.dtype))
+
+
+# ----------------------------------------------------------------------------------------------
+# Rotary positions ("KV cache decoding", "Position information with a cache": the query and the key
+# are rotated by an angle that depends on their absolute position, keys are stored already rotated
+# and the new query is rotated by its position, so the score depends only on the distance and cached
+# keys never change. The pages name RoPE without its formula; this is the published one, Su et al.,
+# "RoFormer: Enhanced Transformer with Rotary Position Embedding", eq. 34: pair i of a d-wide vector
+# turns by position * theta_i, theta_i = base^(-2i/d).)
+# ----------------------------------------------------------------------------------------------
+
+ROPE_STYLES = ("half", "interleaved")
+
+
+def rope_theta(d: int, base: float) -> np.ndarray:
+    """Angular frequency of each of the d/2 pairs: theta_i = base^(-2i/d), i = 0 .. d/2 - 1."""
+    return float(base) ** (-2.0 * np.arange(d // 2, dtype=np.float64) / d)
+
+
+def rope_pairs(d: int, style: str):
+    """Element indices (a_i, b_i) of the pairs that rotate together: (i, i + d/2) for "half" (the
+    Llama-family layout), (2i, 2i + 1) for "interleaved" (the RoFormer paper's layout)."""
+    i = np.arange(d // 2)
+    if style == "half":
+        return i, i + d // 2
+    if style == "interleaved":
+        return 2 * i, 2 * i + 1
+    raise ValueError(f"unknown RoPE style {style!r}")
+
+
+def apply_rope(x, positions, base: float, style: str) -> np.ndarray:
+    """Rotate the last axis of x [..., n, d] row by row, row j at absolute position positions[j],
+    in float64: (x_a, x_b) -> (x_a cos - x_b sin, x_b cos + x_a sin) with angle position * theta_i."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * rope_theta(d, base)[None, :]
+    c, sn = np.cos(ang), np.sin(ang)
+    a, b = rope_pairs(d, style)
+    out = x.copy()
+    out[..., a] = x[..., a] * c - x[..., b] * sn
+    out[..., b] = x[..., b] * c + x[..., a] * sn
+    return out
+
+
+def rope_chunk(x, starts, base: float, style: str) -> np.ndarray:
+    """A [B, H, T, d] chunk whose row t of sequence b sits at absolute position starts[b] + t,
+    rotated in float64 and rounded to float32 (what a fused append stores, before the cache dtype;
+    what a fused attention uses as its query)."""
+    x = np.asarray(x)
+    B, H, T, d = x.shape
+    out = np.empty(x.shape, dtype=np.float32)
+    for b in range(B):
+        out[b] = apply_rope(x[b], int(starts[b]) + np.arange(T), base, style).astype(np.float32)
+    return out
 
 
 # ----------------------------------------------------------------------------------------------

@@ -149,3 +149,34 @@ def test_paged_highest_block_first_is_caught(monkeypatch):
 
     monkeypatch.setattr(ko.OraclePagedKVCache, "take_block", take_highest)
     _fails(paged_pins.test_paged_allocation_order_by_hand)
+
+
+# ---- rotary positions ("KV cache decoding", "Position information with a cache") ---------------------
+from tests import test_oracle_rope as rope_pins
+
+
+def test_rope_at_position_zero_is_caught(monkeypatch):
+    """The pages' classic bug: the new token rotated as if it sat at position 0."""
+    orig = ko.rope_chunk
+
+    def rope_from_zero(x, starts, base, style):
+        return orig(x, [0] * len(starts), base, style)
+
+    monkeypatch.setattr(rope_pins, "rope_chunk", rope_from_zero)
+    _fails(rope_pins.test_rope_chunk_positions_follow_each_sequence)
+
+
+def test_rope_turning_the_wrong_way_is_caught(monkeypatch):
+    orig = ko.apply_rope
+
+    def backwards(x, positions, base, style):
+        return orig(x, -np.asarray(positions, dtype=np.float64), base, style)
+
+    monkeypatch.setattr(rope_pins, "apply_rope", backwards)
+    _fails(rope_pins.test_two_dims_turn_by_the_position_in_radians, "half")
+
+
+def test_rope_frequency_off_by_two_is_caught(monkeypatch):
+    """theta_i = base^(-i/d) instead of base^(-2i/d)."""
+    monkeypatch.setattr(ko, "rope_theta", lambda d, base: float(base) ** (-np.arange(d // 2) / d))
+    _fails(rope_pins.test_pair_frequencies_form_a_geometric_series, "half")
