@@ -159,8 +159,11 @@ def cpu_sample_child(arg):
     import numpy as np
 
     import kvc_workloads
-    from oracle.kvc_oracle import OracleKVCache, OraclePagedKVCache, gqa_cached_attention
+    from oracle.kvc_oracle import OracleKVCache, OraclePagedKVCache, gqa_cached_attention, rope_chunk
     sp = kvc_workloads.spec(cfg["workload"])
+
+    def rot(x, start):                 # the workload's rotary positions, if it has them
+        return rope_chunk(x, [start], sp.rope_base, sp.rope_style) if sp.rope_base else x
     seqs = list(range(cfg["n_seq"]))
     caches, queries = [], []
     for b in seqs:
@@ -173,13 +176,13 @@ def cpu_sample_child(arg):
         if s_b:
             kk = np.stack([sp.host_prefill_rows(0, b, h, s_b)[0] for h in range(sp.H_kv)])[None]
             vv = np.stack([sp.host_prefill_rows(0, b, h, s_b)[1] for h in range(sp.H_kv)])[None]
-            c.append(0, kk, vv)
+            c.append(0, rot(kk, 0), vv)
             c.commit()
         kn = np.stack([sp.host_step_rows(0, 0, b, h)[0] for h in range(sp.H_kv)])[None]
         vn = np.stack([sp.host_step_rows(0, 0, b, h)[1] for h in range(sp.H_kv)])[None]
-        c.append(0, kn, vn)
+        c.append(0, rot(kn, s_b), vn)
         caches.append(c)
-        queries.append(sp.host_queries(0, 0, b, range(sp.H_q))[None])
+        queries.append(rot(sp.host_queries(0, 0, b, range(sp.H_q))[None], s_b))
     bytes_per_pass = sp.attn_bytes(seqs)
     t_end = time.perf_counter() + cfg["seconds"]
     passes, elapsed = 0, 0.0
@@ -261,6 +264,9 @@ def workload_config(sp, note=None):
          "s_b": {"min": int(np.min(sp.lengths)), "mean": float(np.mean(sp.lengths)),
                  "max": int(np.max(sp.lengths))},
          "l2": "no flush: K/V read per layer is larger than the 129 MB L2"}
+    if sp.rope_base:
+        c["rope"] = {"base": sp.rope_base, "style": sp.rope_style,
+                     "fused": "keys rotated in the append kernel, queries in the attention prologue"}
     if sp.block:
         c["paged"] = {"block": sp.block, "n_blocks": sp.B * (-(-sp.max_len // sp.block)),
                       "layout": "prefilled one block per sequence in turn: a sequence's blocks lie B apart"}
@@ -296,10 +302,10 @@ def run_ours(args):
 
     def step(ev=None):
         for layer, (q, k, v) in enumerate(inputs):
-            kb.kvc_append(wl.cache, layer, k, v)
+            wl.append(layer, k, v)
             if ev is not None:
                 ev[layer][0].record(stream)
-            kb.gqa_cached_attn(wl.cache, q, layer, out=outs[layer])
+            wl.attend(q, layer, out=outs[layer])
             if ev is not None:
                 ev[layer][1].record(stream)
         kb.kvc_commit(wl.cache)
@@ -384,8 +390,8 @@ def run_ours(args):
                 for d_, h_ in zip(dev_in[layer], host_in[layer]):
                     d_.copy_(h_, non_blocking=True)
                 q, k, v = dev_in[layer]
-                kb.kvc_append(wl.cache, layer, k, v)
-                kb.gqa_cached_attn(wl.cache, q, layer, out=outs[layer])
+                wl.append(layer, k, v)
+                wl.attend(q, layer, out=outs[layer])
                 host_out[layer].copy_(outs[layer], non_blocking=True)
             kb.kvc_commit(wl.cache)
             kb.kvc_truncate_ragged(wl.cache, lengths)

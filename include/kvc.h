@@ -51,6 +51,12 @@ enum {
   KVC_E_NOMEM = -7           /* device or host allocation failed */
 };
 
+/* Rotary-position pair layouts (kvc_set_rope). */
+typedef enum {
+  KVC_ROPE_HALF = 0,        /* element i turns with element i + d_h/2 (the Llama-family layout) */
+  KVC_ROPE_INTERLEAVED = 1  /* element 2i turns with element 2i + 1 (the RoFormer paper's layout) */
+} kvc_rope_style;
+
 /* Pass as `s` to gqa_cached_attn to use each sequence's own committed length (ragged batches). */
 #define KVC_COMMITTED (-1)
 /* Largest batch a handle accepts. */
@@ -135,6 +141,28 @@ int kvc_append(kvc_handle h, int layer, const void* k_new_dev, const void* v_new
                kvc_dtype in_dtype, int T, void* stream);
 
 /*
+ * kvc_set_rope — give the handle rotary positions: build on the device, once, the table of
+ * (cos, sin)(p * theta_i) for every position p < max_len and pair i < d_h/2, theta_i = base^(-2i/d_h),
+ * computed in float64 and stored as float32 pairs (max_len * d_h/2 * 8 bytes, owned by the handle).
+ * Calling it again rebuilds the table for the new base and style (stream-ordered).
+ * Defined by: "KV cache decoding", "Position information with a cache" (query and key rotated by an angle
+ * of their absolute position; keys stored already rotated; the new query rotated by its position; the
+ * score then depends only on the distance). The pages name RoPE without printing it; the formula is
+ * Su et al., "RoFormer", eq. 34.
+ * Errors: KVC_E_INVAL (base not in (1, 1e12], unknown style), KVC_E_NOMEM.
+ */
+int kvc_set_rope(kvc_handle h, double base, kvc_rope_style style, void* stream);
+
+/*
+ * kvc_append_rope — kvc_append with the keys rotated inside the append: row t of sequence b is turned
+ * by its absolute position (the position it is written at, s_b + t for a forward's chunk) in float32,
+ * then rounded to the cache dtype; values are stored as given. k_new_dev holds the keys BEFORE RoPE.
+ * Arguments, layout and errors are kvc_append's, plus KVC_E_STATE when kvc_set_rope was not called.
+ */
+int kvc_append_rope(kvc_handle h, int layer, const void* k_new_dev, const void* v_new_dev,
+                    kvc_dtype in_dtype, int T, void* stream);
+
+/*
  * kvc_commit — advance every committed length s_b to its fill, once per forward after the last
  * layer ("KV cache, incremental decode, ...", §2.3: the length advances only after the last layer;
  * "KV cache decoding", step 7).
@@ -193,6 +221,16 @@ int kvc_layer_ptrs(kvc_handle h, int layer, void** k_dev, void** v_dev);
  */
 int gqa_cached_attn(kvc_handle h, const void* q_dev, kvc_dtype q_dtype, int layer, int s, int T,
                     int H_q, float* out_dev, void* stream);
+
+/*
+ * gqa_cached_attn_rope — gqa_cached_attn with the queries rotated in the attention kernel's prologue:
+ * query row t of sequence b is turned by its absolute position s_b + t in float32 (then, for a 16-bit
+ * cache, rounded to the cache dtype) before it attends. q_dev holds the queries BEFORE RoPE; the cache
+ * must hold keys stored rotated (kvc_append_rope). Arguments, layout and errors are gqa_cached_attn's,
+ * plus KVC_E_STATE when kvc_set_rope was not called.
+ */
+int gqa_cached_attn_rope(kvc_handle h, const void* q_dev, kvc_dtype q_dtype, int layer, int s, int T,
+                         int H_q, float* out_dev, void* stream);
 
 /*
  * kvc_status — synchronise `stream` and report device-side failures: KVC_E_DEVICE_TIMEOUT if a

@@ -14,6 +14,8 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 _lib = None
 
 KVC_F32, KVC_F16, KVC_BF16 = 0, 1, 2
+KVC_ROPE_HALF, KVC_ROPE_INTERLEAVED = 0, 1
+ROPE_STYLE = {"half": KVC_ROPE_HALF, "interleaved": KVC_ROPE_INTERLEAVED}
 KVC_COMMITTED = -1
 KVC_MAX_BATCH = 1024
 ERRORS = {0: "KVC_OK", -1: "KVC_E_INVAL", -2: "KVC_E_CAPACITY", -3: "KVC_E_STATE", -4: "KVC_E_CUDA",
@@ -31,6 +33,8 @@ SIGNATURES = {
     "kvc_block_table": (_c_int, [_vp, _i32p, _i32p]),
     "kvc_destroy": (_c_int, [_vp]),
     "kvc_append": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _vp]),
+    "kvc_append_rope": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _vp]),
+    "kvc_set_rope": (_c_int, [_vp, ctypes.c_double, _c_int, _vp]),
     "kvc_commit": (_c_int, [_vp, _vp]),
     "kvc_truncate": (_c_int, [_vp, _c_int, _vp]),
     "kvc_truncate_ragged": (_c_int, [_vp, _i32p, _vp]),
@@ -39,6 +43,7 @@ SIGNATURES = {
     "kvc_nbytes": (_sz, [_vp]),
     "kvc_layer_ptrs": (_c_int, [_vp, _c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp)]),
     "gqa_cached_attn": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
+    "gqa_cached_attn_rope": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
     "gqa_cached_attn_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
     "kvc_status": (_c_int, [_vp, _vp]),
     "kvc_last_error": (_c_int, [_vp, ctypes.c_char_p, _sz]),
@@ -187,6 +192,22 @@ def kvc_block_table(c: PagedCache):
     return [flat[b * c.max_blocks:(b + 1) * c.max_blocks] for b in range(c.B)], int(n_free.value)
 
 
+def kvc_set_rope(c: Cache, base: float, style="half", stream=None):
+    """Build the handle's rotary table (theta_i = base^(-2i/d_h)); style "half" or "interleaved"."""
+    code = ROPE_STYLE[style] if isinstance(style, str) else int(style)
+    _check(load().kvc_set_rope(c.h, float(base), code, _stream(stream)), c.h)
+
+
+def kvc_append_rope(c: Cache, layer: int, k_new, v_new, stream=None):
+    """kvc_append with the keys (given before RoPE) rotated by their positions inside the append."""
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype or k_new.dim() != 4:
+        raise ValueError("k_new and v_new must both be [B, H_kv, T, d_h] of one dtype")
+    if tuple(k_new.shape[:2]) != (c.B, c.H_kv) or k_new.shape[3] != c.d_h:
+        raise ValueError("k_new shape does not match the cache")
+    _check(load().kvc_append_rope(c.h, layer, _ptr(k_new), _ptr(v_new), dtype_code(k_new.dtype),
+                                  int(k_new.shape[2]), _stream(stream)), c.h)
+
+
 def kvc_commit(c: Cache, stream=None):
     _check(load().kvc_commit(c.h, _stream(stream)), c.h)
 
@@ -232,6 +253,18 @@ def gqa_cached_attn(c: Cache, q, layer: int, s: int = KVC_COMMITTED, out=None, s
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     _check(load().gqa_cached_attn(c.h, _ptr(q), dtype_code(q.dtype), layer, s, int(q.shape[2]),
                                   int(q.shape[1]), _ptr(out), _stream(stream)), c.h)
+    return out
+
+
+def gqa_cached_attn_rope(c: Cache, q, layer: int, s: int = KVC_COMMITTED, out=None, stream=None):
+    """gqa_cached_attn with the queries (given before RoPE) rotated by their positions s_b + t."""
+    torch = _torch()
+    if q.dim() != 4 or q.shape[0] != c.B or q.shape[3] != c.d_h:
+        raise ValueError("q must be [B, H_q, T, d_h]")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _check(load().gqa_cached_attn_rope(c.h, _ptr(q), dtype_code(q.dtype), layer, s, int(q.shape[2]),
+                                       int(q.shape[1]), _ptr(out), _stream(stream)), c.h)
     return out
 
 

@@ -7,6 +7,10 @@
 // coalesced, vectorised stores with no read-modify-write. The write position comes from the
 // device's committed lengths, so the kernel stays correct when replayed from a captured graph.
 //
+// Rotary positions (fused RoPE): a key row is rotated by its absolute position, the position it is
+// written at, in float32 from a float64-built cos/sin table, and then rounded; V rows are stored as
+// given. The table is [max_len, D/2] pairs of (cos, sin), built once per handle.
+//
 // Paged store: the row's physical block comes from the sequence's block table (pool layout
 // [L, n_blocks, H, block, D]); the table edits that allocate blocks are one small launch before the
 // append, in stream order.
@@ -61,6 +65,24 @@ struct Pack<__nv_bfloat16> {
   }
 };
 
+// N consecutive input elements (one output group) as float32: float32 input, or the cache dtype widened.
+template <typename Tc, bool kF32In>
+__device__ __forceinline__ void load_group(const void* src, long long off, float* x) {
+  constexpr int N = Pack<Tc>::N;
+  if constexpr (kF32In) {
+    const float* p = static_cast<const float*>(src) + off;
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const float4 f = *reinterpret_cast<const float4*>(p + i);
+      x[i] = f.x; x[i + 1] = f.y; x[i + 2] = f.z; x[i + 3] = f.w;
+    }
+  } else {
+    const Tc* p = static_cast<const Tc*>(src) + off;
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = dev::to_f32<Tc>(p[i]);
+  }
+}
+
 // One thread per 16-byte output group; grid covers 2 (K, V) x B x H x T x D / N groups.
 template <typename Tc, bool kF32In>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
@@ -94,19 +116,35 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   }
   Tc* dst = static_cast<Tc*>(is_v ? a.v_store : a.k_store) + dst_row * a.D + grp * N;
   const long long src_off = row * a.D + grp * N;
+  const void* src = is_v ? a.v_new : a.k_new;
   uint4 out;
-  if constexpr (kF32In) {
-    const float* src = static_cast<const float*>(is_v ? a.v_new : a.k_new) + src_off;
-    float x[N];
+  if (!is_v && a.rope.table != nullptr) {
+    // RoPE: rotate the key row by its absolute position (its write position) in float32, then round.
+    // The partners of this group's elements are the group D/2 away (style 0) or its own neighbours.
+    float x[N], y[N];
+    load_group<Tc, kF32In>(src, src_off, x);
+    const int e0 = grp * N;
+    if (a.rope.style == 0) {
+      load_group<Tc, kF32In>(src, src_off + (e0 < a.D / 2 ? a.D / 2 : -(a.D / 2)), y);
+    } else {
 #pragma unroll
-    for (int i = 0; i < N; i += 4) {
-      const float4 f = *reinterpret_cast<const float4*>(src + i);
-      x[i] = f.x; x[i + 1] = f.y; x[i + 2] = f.z; x[i + 3] = f.w;
+      for (int i = 0; i < N; ++i) y[i] = x[i ^ 1];
+    }
+    const float2* cs = a.rope.table + static_cast<long long>(pos) * (a.D >> 1);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      int pair;
+      bool second;
+      dev::rope_partner(e0 + i, a.D, a.rope.style, &pair, &second);
+      x[i] = dev::rope_rotate(x[i], y[i], cs[pair], second);
     }
     out = Pack<Tc>::from_f32(x);
+  } else if constexpr (kF32In) {
+    float x[N];
+    load_group<Tc, true>(src, src_off, x);
+    out = Pack<Tc>::from_f32(x);
   } else {
-    const Tc* src = static_cast<const Tc*>(is_v ? a.v_new : a.k_new) + src_off;
-    out = *reinterpret_cast<const uint4*>(src);
+    out = *reinterpret_cast<const uint4*>(static_cast<const Tc*>(src) + src_off);
   }
   *reinterpret_cast<uint4*>(dst) = out;
 }
@@ -123,6 +161,17 @@ __global__ void table_edits_kernel(int32_t* table, const __grid_constant__ Table
   dev::pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < e.n) table[e.slot[i]] = e.value[i];
+}
+
+__global__ void rope_table_kernel(float2* table, int max_len, int half, const __grid_constant__ RopeTheta th) {
+  dev::pdl_wait();
+  dev::pdl_trigger();
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long long>(max_len) * half) return;
+  const int p = static_cast<int>(i / half), j = static_cast<int>(i % half);
+  double sn, c;
+  sincos(static_cast<double>(p) * th.theta[j], &sn, &c);     // the angle in float64, then rounded
+  table[i] = make_float2(static_cast<float>(c), static_cast<float>(sn));
 }
 
 struct LensValues {
@@ -164,6 +213,12 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
     case KVC_BF16: return run_append<__nv_bfloat16>(a, st);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_rope_table(float2* table, int max_len, int D, const RopeTheta& th, cudaStream_t st) {
+  const long long n = static_cast<long long>(max_len) * (D / 2);
+  return launch_pdl(rope_table_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, st, table,
+                    max_len, D / 2, th);
 }
 
 cudaError_t launch_table_edits(int32_t* table, const TableEdits& e, cudaStream_t st) {

@@ -155,7 +155,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     float x = 0.f;
     if (r < nrows) {
       const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-      x = load_query<Tc>(a.q, a.q_dtype, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d);
+      x = load_query_rot<Tc>(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh, d, s_b + t);
     }
     *reinterpret_cast<Tc*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tc>(x);
   }

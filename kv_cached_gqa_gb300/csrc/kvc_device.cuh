@@ -225,5 +225,45 @@ __device__ __forceinline__ float load_query(const void* q, kvc_dtype qt, long lo
   return to_f32<Tc>(static_cast<const Tc*>(q)[i]);
 }
 
+// ---- rotary positions ----------------------------------------------------------------------------
+// Element e of a D-wide row turns with one partner: (e, e + D/2) for style 0, (e, e ^ 1) for style 1.
+// Returns the partner, the pair index (the column of the cos/sin table) and whether e is the pair's
+// second element: the first becomes x cos - y sin, the second x cos + y sin (y = the partner).
+__device__ __forceinline__ int rope_partner(int e, int D, int style, int* pair, bool* second) {
+  if (style == 0) {
+    const int h = D >> 1;
+    *second = e >= h;
+    *pair = *second ? e - h : e;
+    return *second ? e - h : e + h;
+  }
+  *second = (e & 1) != 0;
+  *pair = e >> 1;
+  return e ^ 1;
+}
+__device__ __forceinline__ float rope_rotate(float x, float y, float2 cs, bool second) {
+  return second ? fmaf(x, cs.x, y * cs.y) : fmaf(x, cs.x, -(y * cs.y));
+}
+
+// A query element as given (float32, or the cache dtype widened), before any rounding.
+template <typename Tc>
+__device__ __forceinline__ float raw_query(const void* q, kvc_dtype qt, long long i) {
+  if (qt == KVC_F32) return static_cast<const float*>(q)[i];
+  return to_f32<Tc>(static_cast<const Tc*>(q)[i]);
+}
+
+// Element e of the query row starting at element `row`, as the attention uses it: rotated to
+// absolute position `pos` when the call applies RoPE, then (16-bit caches) rounded to the cache dtype.
+template <typename Tc>
+__device__ __forceinline__ float load_query_rot(const AttnArgs& a, long long row, int e, int pos) {
+  if (a.rope.table == nullptr) return load_query<Tc>(a.q, a.q_dtype, row + e);
+  int pair;
+  bool second;
+  const int pe = rope_partner(e, a.D, a.rope.style, &pair, &second);
+  float r = rope_rotate(raw_query<Tc>(a.q, a.q_dtype, row + e), raw_query<Tc>(a.q, a.q_dtype, row + pe),
+                        a.rope.table[static_cast<long long>(pos) * (a.D >> 1) + pair], second);
+  if constexpr (sizeof(Tc) == 2) r = to_f32<Tc>(from_f32<Tc>(r));
+  return r;
+}
+
 }  // namespace dev
 }  // namespace kvc

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -118,6 +119,7 @@ void release(kvc_handle h) {
   cudaFree(h->work);
   cudaFree(h->d_counters);
   cudaFree(h->d_table);
+  cudaFree(h->d_rope);
   delete h;
 }
 
@@ -302,9 +304,17 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
   auto longest_first = [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; };
   out->kernel = kind;
   out->rows_per_tile = rpt;
-  if (kind == AttnKernel::PrefillTC) {                      // one CTA per (unit, K/V head), longest first
+  if (kind == AttnKernel::PrefillTC) {
+    // one CTA per (unit, K/V head). Longest sequences first, and a sequence's row tiles together
+    // (longest tile first): the CTAs resident at any time then share a few sequences' K/V, which
+    // stays in L2 instead of being re-read from HBM by each row tile
     for (int u = 0; u < n_units; ++u) order[u] = {static_cast<int>(std::min<long long>(n_eff[u], 1 << 30)), u};
-    std::stable_sort(order.begin(), order.end(), longest_first);
+    std::stable_sort(order.begin(), order.end(), [&](const std::pair<int, int>& x, const std::pair<int, int>& y) {
+      const int bx = x.second / n_rt, by = y.second / n_rt;
+      if (h->lens[bx] != h->lens[by]) return h->lens[bx] > h->lens[by];
+      if (bx != by) return bx < by;
+      return x.first > y.first;
+    });
     for (int i = 0; i < n_units; ++i) plan->unit_b[i] = order[i].second;
     plan->n_items = n_units * h->H;
     plan->split_keys = n_units ? order[0].first : 0;
@@ -497,9 +507,10 @@ int kvc_destroy(kvc_handle h) {
   return KVC_OK;
 }
 
-int kvc_append(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
-               int T, void* stream) {
+static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
+                       int T, bool rope, void* stream) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (rope && !h->d_rope) return fail(h, KVC_E_STATE, "no rotary table: call kvc_set_rope first");
   if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
   if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
   if (!k_new || !v_new) return fail(h, KVC_E_INVAL, "null k_new/v_new");
@@ -524,10 +535,46 @@ int kvc_append(kvc_handle h, int layer, const void* k_new, const void* v_new, kv
   a.layer = layer; a.B = h->B; a.H = h->H; a.D = h->D; a.T = T; a.max_len = h->max_len;
   a.delta = delta; a.cache_dtype = h->dtype; a.in_dtype = in_dtype;
   a.pg = kvc_paging(h);
+  if (rope) {
+    a.rope.table = h->d_rope;
+    a.rope.style = h->rope_style;
+  }
   cudaError_t e = kvc::launch_append(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "append launch");
   h->launches += 1;
   for (int b = 0; b < h->B; ++b) h->fill[static_cast<size_t>(layer) * h->B + b] += T;
+  return KVC_OK;
+}
+
+int kvc_append(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
+               int T, void* stream) {
+  return append_impl(h, layer, k_new, v_new, in_dtype, T, false, stream);
+}
+
+int kvc_append_rope(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
+                    int T, void* stream) {
+  return append_impl(h, layer, k_new, v_new, in_dtype, T, true, stream);
+}
+
+int kvc_set_rope(kvc_handle h, double base, kvc_rope_style style, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (!(base > 1.0) || base > 1e12) return fail(h, KVC_E_INVAL, "RoPE base %g must be in (1, 1e12]", base);
+  if (style != KVC_ROPE_HALF && style != KVC_ROPE_INTERLEAVED) return fail(h, KVC_E_INVAL, "RoPE style %d", style);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!h->d_rope) {
+    const size_t bytes = sizeof(float2) * static_cast<size_t>(h->max_len) * (h->D / 2);
+    cudaError_t e = cudaMalloc(&h->d_rope, bytes);
+    if (e != cudaSuccess) {
+      h->d_rope = nullptr;
+      return fail(h, KVC_E_NOMEM, "rotary table (%zu bytes): %s", bytes, cudaGetErrorString(e));
+    }
+  }
+  static thread_local kvc::RopeTheta th;
+  for (int i = 0; i < h->D / 2; ++i) th.theta[i] = std::pow(base, -2.0 * i / h->D);
+  cudaError_t e = kvc::launch_rope_table(h->d_rope, h->max_len, h->D, th, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "rotary table launch");
+  h->launches += 1;
+  h->rope_style = style;
   return KVC_OK;
 }
 
@@ -617,9 +664,10 @@ int kvc_layer_ptrs(kvc_handle h, int layer, void** k, void** v) {
   return KVC_OK;
 }
 
-int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
-                    float* out, void* stream) {
+static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
+                     float* out, bool rope, void* stream) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (rope && !h->d_rope) return fail(h, KVC_E_STATE, "no rotary table: call kvc_set_rope first");
   if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
   if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
   if (!q || !out) return fail(h, KVC_E_INVAL, "null q/out");
@@ -666,10 +714,24 @@ int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, i
   a.layer = layer; a.B = h->B; a.H_kv = h->H; a.H_q = H_q; a.G = G; a.T = T; a.D = h->D;
   a.max_len = h->max_len; a.delta = T; a.cache_dtype = h->dtype;
   a.pg = kvc_paging(h);
+  if (rope) {
+    a.rope.table = h->d_rope;
+    a.rope.style = h->rope_style;
+  }
   cudaError_t e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
   h->launches += 1;
   return KVC_OK;
+}
+
+int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
+                    float* out, void* stream) {
+  return attn_impl(h, q, q_dtype, layer, s, T, H_q, out, false, stream);
+}
+
+int gqa_cached_attn_rope(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
+                         float* out, void* stream) {
+  return attn_impl(h, q, q_dtype, layer, s, T, H_q, out, true, stream);
 }
 
 int kvc_status(kvc_handle h, void* stream) {

@@ -34,6 +34,19 @@ struct Paging {
   int n_blocks = 0;                 // physical blocks in the pool
 };
 
+// Rotary positions applied inside the kernels: table[p * (D / 2) + i] = (cos, sin)(p * theta_i), built
+// once per handle in float64 and rounded to float32; style 0 rotates pairs (i, i + D/2), style 1 pairs
+// (2i, 2i + 1).
+struct Rope {
+  const float2* table = nullptr;    // nullptr: no rotation
+  int style = 0;
+};
+constexpr int kMaxRopePairs = 64;   // d_h <= 128
+struct RopeTheta {
+  double theta[kMaxRopePairs];      // base^(-2i/D), computed on the host
+};
+cudaError_t launch_rope_table(float2* table, int max_len, int D, const RopeTheta& th, cudaStream_t st);
+
 // Tile row split of a paged store: keys per TMA box (a tile of `tile` keys takes tile / box_rows
 // boxes per 128-byte column when blocks are shorter than the tile).
 inline int paged_box_rows(const Paging& pg, int tile) {
@@ -53,6 +66,7 @@ struct AppendArgs {
   int delta;                // this layer's fill minus the committed length (uniform over b)
   kvc_dtype cache_dtype, in_dtype;
   Paging pg;                // paged store: rows go through the block table
+  Rope rope;                // rotate K rows by their positions before storing them (V untouched)
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 
@@ -99,6 +113,7 @@ struct AttnArgs {
   int delta;                // fill - committed for this layer (== T when the chunk was appended)
   kvc_dtype cache_dtype;
   Paging pg;                // paged store: tiles are gathered through the block table
+  Rope rope;                // rotate each query row by its position s_b + t before attending
 };
 // Workspace floats the plan needs (0 when no unit splits).
 size_t splitk_workspace_floats(const SplitPlan& p, int D);
@@ -195,6 +210,9 @@ struct kvc_cache {
   std::vector<int32_t> held;      // blocks each sequence holds (logical blocks 0 .. held-1)
   std::vector<int32_t> free_heap; // free physical blocks, a min-heap: the lowest is handed out first
   std::vector<std::pair<int32_t, int32_t>> edit_scratch;   // (slot, value) table edits of one call
+  // rotary positions (kvc_set_rope): cos/sin table [max_len, D / 2] on the device
+  float2* d_rope = nullptr;
+  int rope_style = -1;
   void* k = nullptr;
   void* v = nullptr;
   int32_t* d_lens = nullptr;      // committed lengths on the device

@@ -181,7 +181,12 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     if (r < nrows) {
       const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
       const long long base = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + c * 8;
-      if (a.q_dtype == KVC_F32) {
+      if (a.rope.table != nullptr) {          // rotated to position s_b + t, element by element
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = load_query_rot<Tc>(a, base - c * 8, c * 8 + j, s_b + t);
+        w = make_uint4(pack2<Tc>(x[0], x[1]), pack2<Tc>(x[2], x[3]), pack2<Tc>(x[4], x[5]), pack2<Tc>(x[6], x[7]));
+      } else if (a.q_dtype == KVC_F32) {
         const float4 x0 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + base);
         const float4 x1 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + base + 4);
         w = make_uint4(pack2<Tc>(x0.x, x0.y), pack2<Tc>(x0.z, x0.w), pack2<Tc>(x1.x, x1.y), pack2<Tc>(x1.z, x1.w));

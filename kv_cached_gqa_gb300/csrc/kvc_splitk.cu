@@ -215,8 +215,8 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     float x = 0.f;
     if (r < nrows) {
       const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-      const long long qi = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + e;
-      x = load_query<Tc>(a.q, a.q_dtype, qi) * qscale;
+      const long long qrow = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D;
+      x = load_query_rot<Tc>(a, qrow, e, s_b + t) * qscale;
     }
     qs[r * C::QSTRIDE + e + (e / C::DPART) * 4] = x;
   }

@@ -37,6 +37,8 @@ class WorkloadSpec:
     T: int = 1
     seed: int = 0
     block: int = 0          # paged cache block (positions); 0 = contiguous cache
+    rope_base: float = 0.0  # fused rotary positions (kvc_append_rope / gqa_cached_attn_rope); 0 = none
+    rope_style: str = "half"
 
     @property
     def S0(self) -> int:
@@ -104,7 +106,8 @@ def spec(name: str, seed: int = 0) -> WorkloadSpec:
     else:
         lengths = np.full(w["B"], w["s"], dtype=np.int64)
     return WorkloadSpec(name, w["L"], w["B"], w["H_q"], w["H_kv"], w["d_h"], w["max_len"], w["dtype"],
-                        lengths, T=w["T"], seed=seed, block=w.get("block", 0))
+                        lengths, T=w["T"], seed=seed, block=w.get("block", 0),
+                        rope_base=w.get("rope_base", 0.0), rope_style=w.get("rope_style", "half"))
 
 
 class GpuWorkload:
@@ -120,6 +123,17 @@ class GpuWorkload:
                                        DTYPE_CODE[sp.dtype], device=device)
         else:
             self.cache = kb.Cache(sp.L, sp.B, sp.H_kv, sp.d_h, sp.max_len, DTYPE_CODE[sp.dtype], device=device)
+        if sp.rope_base:
+            kb.kvc_set_rope(self.cache, sp.rope_base, sp.rope_style)
+
+    def append(self, layer, k, v):
+        """The workload's append: kvc_append, or kvc_append_rope when it rotates keys."""
+        (self.kb.kvc_append_rope if self.spec.rope_base else self.kb.kvc_append)(self.cache, layer, k, v)
+
+    def attend(self, q, layer, out=None):
+        """The workload's attention: gqa_cached_attn, or gqa_cached_attn_rope when it rotates queries."""
+        fn = self.kb.gqa_cached_attn_rope if self.spec.rope_base else self.kb.gqa_cached_attn
+        return fn(self.cache, q, layer, out=out)
 
     def __getattr__(self, name):                      # shape fields and host redraws of the spec
         return getattr(self.__dict__["spec"], name)
@@ -143,9 +157,9 @@ class GpuWorkload:
             for c0 in range(0, sp.S0, chunk):
                 c1 = min(sp.S0, c0 + chunk)
                 if c0 == 0 and c1 == sp.S0:
-                    kb.kvc_append(self.cache, layer, k, v)
+                    self.append(layer, k, v)
                 else:
-                    kb.kvc_append(self.cache, layer, k[:, :, c0:c1].contiguous(), v[:, :, c0:c1].contiguous())
+                    self.append(layer, k[:, :, c0:c1].contiguous(), v[:, :, c0:c1].contiguous())
             del k, v
         kb.kvc_commit(self.cache)
         kb.kvc_truncate_ragged(self.cache, [int(x) for x in sp.lengths])

@@ -8,7 +8,8 @@ from __future__ import annotations
 import numpy as np
 
 import kvc_synth
-from oracle.kvc_oracle import OracleKVCache, OraclePagedKVCache, gqa_cached_attention
+from oracle.kvc_oracle import (OracleKVCache, OraclePagedKVCache, gqa_cached_attention, rope_chunk,
+                               store_round, stored_to_f64)
 
 DT = {"f32": 0, "f16": 1, "bf16": 2}
 FP32_ATOL = 1e-5        # float32 caches: absolute, every output element
@@ -30,11 +31,41 @@ def check_outputs(got: np.ndarray, want: np.ndarray, dtype: str, what: str = "")
     return rel
 
 
+def check_rotated_store(got_bits, want_bits, dtype):
+    """Keys rotated on the GPU (float32 arithmetic from float32 cos/sin) against the oracle's float64
+    rotation rounded to float32, then to the cache dtype. The float32 rotation of a pair (x, y) is off
+    by at most about 4 * 2^-24 * (|x| + |y|), i.e. 2^-21 of the row's largest magnitude m; each side
+    then rounds once to the cache dtype. So |got - want| <= ulp(want) + 2^-21 m for 16-bit caches
+    (where x cos and y sin nearly cancel, the result is small and that is many of its own ulps) and
+    2^-20 m for float32 caches; most elements must agree exactly."""
+    if dtype == "f32":
+        g = got_bits.view(np.float32).astype(np.float64)
+        w = want_bits.view(np.float32).astype(np.float64)
+        m = np.abs(w).max(axis=-1, keepdims=True)
+        assert np.all(np.abs(g - w) <= 2.0 ** -20 * m), "rotated float32 keys differ"
+        return
+    npdt = np.float16 if dtype == "f16" else None
+    if npdt is not None:
+        g = got_bits.view(np.float16).astype(np.float64)
+        w = want_bits.view(np.float16).astype(np.float64)
+        ulp = np.spacing(np.abs(want_bits.view(np.float16))).astype(np.float64)
+    else:
+        g = (got_bits.astype(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        w = (want_bits.astype(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ulp = np.spacing(np.abs(w).astype(np.float32)).astype(np.float64) * 2.0 ** 16
+    m = np.abs(w).max(axis=-1, keepdims=True)
+    err = np.abs(g - w)
+    bound = ulp + 2.0 ** -21 * m
+    assert np.all(err <= bound), f"rotated keys off by {float((err / bound).max()):.2f} x the bound"
+    frac = np.count_nonzero(err) / err.size
+    assert frac < 5e-3, f"{frac:.2e} of rotated keys differ from the oracle"
+
+
 class Mirror:
     """A GPU cache and an oracle cache driven by the same calls (paged when `block` is given: a pool of
     `n_blocks` blocks, by default enough for every sequence at max_len)."""
 
-    def __init__(self, L, B, H_kv, d_h, max_len, dtype, seed=0, block=None, n_blocks=None):
+    def __init__(self, L, B, H_kv, d_h, max_len, dtype, seed=0, block=None, n_blocks=None, rope=None):
         import torch
         from kv_cached_gqa_gb300 import _binding as kb
         self.torch, self.kb = torch, kb
@@ -48,6 +79,9 @@ class Mirror:
             self.gpu = kb.Cache(L, B, H_kv, d_h, max_len, DT[dtype])
             self.ref = OracleKVCache(L, B, H_kv, d_h, max_len, dtype)
         self.n_draws = 0
+        self.rope = rope                      # (base, style): keys and queries rotated by position
+        if rope is not None:
+            kb.kvc_set_rope(self.gpu, rope[0], rope[1])
 
     def draw(self, shape):
         self.n_draws += 1
@@ -60,22 +94,35 @@ class Mirror:
     def append(self, layer, T, in_dtype="f32"):
         k = self.draw((self.B, self.H, T, self.d))
         v = self.draw((self.B, self.H, T, self.d))
-        self.ref.append(layer, k, v)
+        if self.rope is not None:
+            # the oracle rotates the values the GPU receives (rounded first if given in 16 bits)
+            k_in = k if in_dtype == "f32" else stored_to_f64(store_round(k, in_dtype), in_dtype).astype(np.float32)
+            self.ref.append(layer, rope_chunk(k_in, self.ref.seq_len(layer), *self.rope), v)
+        else:
+            self.ref.append(layer, k, v)
         if in_dtype == "f32":
             kd, vd = self.dev(k), self.dev(v)
         else:
             # input already in the cache dtype: hand the oracle's own rounding of it to both sides
             tdt = self.kb.torch_dtype(DT[in_dtype])
             kd, vd = self.dev(k).to(tdt), self.dev(v).to(tdt)
-        self.kb.kvc_append(self.gpu, layer, kd, vd)
+        if self.rope is not None:
+            self.kb.kvc_append_rope(self.gpu, layer, kd, vd)
+        else:
+            self.kb.kvc_append(self.gpu, layer, kd, vd)
 
     def attend(self, layer, H_q, T, q_in="f32", split_keys=0):
         q = self.draw((self.B, H_q, T, self.d))
-        want = gqa_cached_attention(self.ref, layer, q)
+        if self.rope is not None:
+            q_in_vals = q if q_in == "f32" else stored_to_f64(store_round(q, q_in), q_in).astype(np.float32)
+            want = gqa_cached_attention(self.ref, layer, rope_chunk(q_in_vals, self.ref.committed(), *self.rope))
+        else:
+            want = gqa_cached_attention(self.ref, layer, q)
         qd = self.dev(q) if q_in == "f32" else self.dev(q).to(self.kb.torch_dtype(DT[q_in]))
         if split_keys:
             self.kb.kvc_set_split_keys(self.gpu, split_keys)
-        got = self.kb.gqa_cached_attn(self.gpu, qd, layer).cpu().numpy()
+        attn = self.kb.gqa_cached_attn_rope if self.rope is not None else self.kb.gqa_cached_attn
+        got = attn(self.gpu, qd, layer).cpu().numpy()
         if split_keys:
             self.kb.kvc_set_split_keys(self.gpu, 0)
         return got, want
@@ -114,7 +161,10 @@ class Mirror:
 
     def check_state(self):
         (gk, gv), (rk, rv) = self.store_bits()
-        np.testing.assert_array_equal(gk, rk)
+        if self.rope is None:
+            np.testing.assert_array_equal(gk, rk)
+        else:
+            check_rotated_store(gk, rk, self.dtype)
         np.testing.assert_array_equal(gv, rv)
         assert self.kb.kvc_seq_len(self.gpu, -1) == [int(x) for x in self.ref.committed()]
         for layer in range(self.L):

@@ -34,7 +34,7 @@ def test_headers_declare_the_entry_points():
     names = declared_symbols()
     for n in ("kvc_create", "kvc_append", "kvc_commit", "kvc_truncate", "kvc_nbytes", "gqa_cached_attn",
               "kvc_truncate_ragged", "kvc_seq_len", "kvc_positions", "kvc_layer_ptrs", "kvc_status",
-              "kvc_create_paged", "kvc_block_table"):
+              "kvc_create_paged", "kvc_block_table", "kvc_set_rope", "kvc_append_rope", "gqa_cached_attn_rope"):
         assert n in names
 
 
@@ -87,6 +87,9 @@ def test_host_validation_without_gpu(lib):
     assert lib.kvc_create_paged(None, 1, 1, 1, 64, 64, 16, 8, 1, None, None, None) == -1
     assert h.value is None
     assert lib.kvc_block_table(None, None, None) == -1
+    assert lib.kvc_set_rope(None, 10000.0, 0, None) == -1
+    assert lib.kvc_append_rope(None, 0, None, None, 0, 1, None) == -1
+    assert lib.gqa_cached_attn_rope(None, None, 0, 0, -1, 1, 1, None, None) == -1
 
 
 def test_binding_fails_loudly_when_library_missing(monkeypatch, tmp_path):

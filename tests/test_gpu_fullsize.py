@@ -8,8 +8,8 @@ import numpy as np
 import pytest
 
 import kvc_workloads
-from oracle.kvc_oracle import OracleKVCache, gqa_cached_attention
-from tests.gpu_parity import check_outputs
+from oracle.kvc_oracle import OracleKVCache, gqa_cached_attention, rope_chunk
+from tests.gpu_parity import check_outputs, check_rotated_store
 
 pytestmark = pytest.mark.gpu
 
@@ -21,8 +21,8 @@ def _run_and_sample(wl, samples):
     inputs = wl.step_inputs(0)
     outs = []
     for layer, (q, k, v) in enumerate(inputs):
-        kb.kvc_append(wl.cache, layer, k, v)
-        outs.append(kb.gqa_cached_attn(wl.cache, q, layer))
+        wl.append(layer, k, v)
+        outs.append(wl.attend(q, layer))
     kb.kvc_commit(wl.cache)
     kb.kvc_status(wl.cache)
     G = wl.H_q // wl.H_kv
@@ -30,14 +30,16 @@ def _run_and_sample(wl, samples):
     for layer, b, kvh in samples:
         s_b = int(wl.lengths[b])
         ref = OracleKVCache(1, 1, 1, wl.d_h, s_b + wl.T, wl.dtype)
+        rot = (lambda x, start: rope_chunk(x, [start], wl.rope_base, wl.rope_style)) if wl.rope_base else \
+            (lambda x, start: x)
         if s_b:
             kp, vp = wl.host_prefill_rows(layer, b, kvh, s_b)
-            ref.append(0, kp[None, None], vp[None, None])
+            ref.append(0, rot(kp[None, None], 0), vp[None, None])
             ref.commit()
         kn, vn = wl.host_step_rows(layer, 0, b, kvh)
-        ref.append(0, kn[None, None], vn[None, None])
+        ref.append(0, rot(kn[None, None], s_b), vn[None, None])
         heads = list(range(kvh * G, (kvh + 1) * G))
-        qh = wl.host_queries(layer, 0, b, heads)
+        qh = rot(wl.host_queries(layer, 0, b, heads)[None], s_b)[0]
         want = gqa_cached_attention(ref, 0, qh[None])
         got = outs[layer][b, kvh * G:(kvh + 1) * G].cpu().numpy()[None]
         check_outputs(got, want, wl.dtype, f"layer {layer} b {b} kvh {kvh}")
@@ -49,7 +51,10 @@ def _run_and_sample(wl, samples):
             else:
                 stored = store[layer, b, kvh, :s_b + wl.T]
             stored = stored.contiguous().view(view).cpu().numpy()
-            np.testing.assert_array_equal(stored, want_rows.view(stored.dtype))
+            if wl.rope_base and store is wl.cache.k:
+                check_rotated_store(stored, want_rows.view(stored.dtype), wl.dtype)
+            else:
+                np.testing.assert_array_equal(stored, want_rows.view(stored.dtype))
     assert kb.kvc_seq_len(wl.cache) == [int(x) + wl.T for x in wl.lengths]
     wl.close()
 
@@ -86,3 +91,11 @@ def test_llama3_8b_decode_bf16_paged16_full_size():
     wl = kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-decode-bf16-paged16"))
     lo, hi = int(np.argmin(wl.lengths)), int(np.argmax(wl.lengths))
     _run_and_sample(wl, [(0, lo, 0), (31, hi, 7), (13, 17, 3)])
+
+
+def test_llama3_8b_decode_bf16_rope_full_size():
+    """The ragged decode batch with fused RoPE (base 500000, rotate-half): keys rotated in the append,
+    queries in the attention prologue."""
+    wl = kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-decode-bf16-rope"))
+    lo, hi = int(np.argmin(wl.lengths)), int(np.argmax(wl.lengths))
+    _run_and_sample(wl, [(0, lo, 0), (31, hi, 7), (9, 30, 4)])
