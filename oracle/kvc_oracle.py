@@ -36,7 +36,9 @@ Readings where the pages are silent (each listed in the design doc):
 * the paged cache hands out the lowest-numbered free block first and frees, on truncate, every
   block wholly past the new length;
 * RoPE: theta_i = base^(-2i/d) with pairs (i, i + d/2) or (2i, 2i + 1); a rotated row is rounded to
-  float32 before the cache dtype.
+  float32 before the cache dtype;
+* fp8 caches store E4M3 codes of x / scale (one K and one V scale per layer; round to nearest even,
+  saturating at 448); a query meets an fp8 cache rounded to float16.
 
 Parity status: every function here is pinned by `tests/test_oracle_pins.py`.
 """
@@ -44,8 +46,9 @@ from __future__ import annotations
 
 import numpy as np
 
-DTYPES = ("f32", "f16", "bf16", "f64")
-ITEMSIZE = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8}
+DTYPES = ("f32", "f16", "bf16", "f64", "e4m3")
+ITEMSIZE = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8, "e4m3": 1}
+E4M3_MAX = 448.0
 
 
 # ----------------------------------------------------------------------------------------------
@@ -53,17 +56,50 @@ ITEMSIZE = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8}
 # converted on the way in and the stored values are what every later read returns).
 # ----------------------------------------------------------------------------------------------
 
+def e4m3_encode(x) -> np.ndarray:
+    """float32 values -> FP8 E4M3 codes (uint8): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits,
+    subnormals below 2^-6 in steps of 2^-9, no infinities, largest finite 448. Round to nearest even on
+    the value grid, then saturate to +-448 (NaN inputs are out of scope)."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    neg = np.signbit(x)
+    a = np.abs(x)
+    _, ex = np.frexp(a)                             # a = m * 2^ex, m in [0.5, 1): binade exponent ex - 1
+    e = np.maximum(ex - 1, -6)                      # below 2^-6 the grid is the subnormal one
+    quantum = np.ldexp(1.0, e - 3)                  # 3 mantissa bits
+    r = np.minimum(np.rint(a / quantum) * quantum, E4M3_MAX)   # a / quantum is exact: a power of two
+    # encode the (now representable) magnitude
+    _, rex = np.frexp(r)
+    normal = r >= 2.0 ** -6
+    exp_field = np.where(normal, rex - 1 + 7, 0)
+    man = np.where(normal, np.rint((r / np.ldexp(1.0, rex - 1) - 1.0) * 8), np.rint(r / 2.0 ** -9))
+    code = (exp_field.astype(np.int64) << 3) | man.astype(np.int64)
+    return (code | (neg.astype(np.int64) << 7)).astype(np.uint8)
+
+
+def e4m3_decode(c) -> np.ndarray:
+    """FP8 E4M3 codes -> float64 values (codes 0x7F / 0xFF are NaN)."""
+    c = np.asarray(c, dtype=np.uint8).astype(np.int64)
+    exp_field = (c >> 3) & 15
+    man = c & 7
+    mag = np.where(exp_field == 0, man * 2.0 ** -9, (1.0 + man / 8.0) * np.ldexp(1.0, exp_field - 7))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return np.where(c & 0x80, -mag, mag)
+
+
 def store_round(x, dtype: str) -> np.ndarray:
     """Convert float32 input values to the cache's stored representation.
 
     f32 -> float32 copy; f16 -> IEEE half (NumPy's astype, round to nearest even);
     bf16 -> uint16 bit patterns, rounding float32 to its top 16 bits to nearest even;
-    f64 -> float64 (the NumPy default store of the "KV cache decoding" listing).
+    e4m3 -> uint8 FP8 E4M3 codes (round to nearest even, saturating; a cache's scale is applied by
+    the caller); f64 -> float64 (the NumPy default store of the "KV cache decoding" listing).
     """
     x = np.asarray(x)
     if dtype == "f64":
         return x.astype(np.float64)
     x = x.astype(np.float32)
+    if dtype == "e4m3":
+        return e4m3_encode(x)
     if dtype == "f32":
         return x.copy()
     if dtype == "f16":
@@ -77,14 +113,16 @@ def store_round(x, dtype: str) -> np.ndarray:
 
 
 def stored_to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact float64 value of stored elements."""
+    """Exact float64 value of stored elements (an fp8 cache's scale is applied by the caller)."""
+    if dtype == "e4m3":
+        return e4m3_decode(a)
     if dtype == "bf16":
         return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     return a.astype(np.float64)
 
 
 def storage_np_dtype(dtype: str):
-    return {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "f64": np.float64}[dtype]
+    return {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "f64": np.float64, "e4m3": np.uint8}[dtype]
 
 
 # ----------------------------------------------------------------------------------------------
@@ -107,6 +145,33 @@ def kv_bytes(layers: int, heads: int, head_dim: int, seq_len: int, batch: int = 
     "What is cached, what is not, and what it costs"; "Heads, GQA and K/V cache", "Memory and the
     window limit"; "Generation and the KV Cache", "Memory")."""
     return 2 * layers * heads * head_dim * seq_len * batch * bytes_per_value
+
+
+# ----------------------------------------------------------------------------------------------
+# FP8 storage. The pages name cache quantisation as a decode lever ("KV cache decoding", "What is
+# cached, what is not, and what it costs") but give no format. Reading: E4M3 codes with one scale per
+# layer for K and one for V, stored = e4m3(x / scale) (float32 division, round to nearest even,
+# saturating), read back as code * scale.
+# ----------------------------------------------------------------------------------------------
+
+def set_fp8_scales(cache, k_scale, v_scale) -> None:
+    """Per-layer K and V scales of an fp8 cache, fixed while it holds no rows."""
+    if cache.dtype != "e4m3":
+        raise ValueError("scales belong to fp8 caches")
+    if np.any(cache.fill != 0):
+        raise RuntimeError("scales change only while the cache is empty")
+    k = np.broadcast_to(np.asarray(k_scale, dtype=np.float32), (cache.L,)).copy()
+    v = np.broadcast_to(np.asarray(v_scale, dtype=np.float32), (cache.L,)).copy()
+    if not (np.all(np.isfinite(k)) and np.all(k > 0) and np.all(np.isfinite(v)) and np.all(v > 0)):
+        raise ValueError("scales must be positive and finite")
+    cache.k_scale, cache.v_scale = k, v
+
+
+def quantize_rows(x, dtype: str, scale) -> np.ndarray:
+    """Stored form of float32 rows: store_round, after dividing by the layer's scale for fp8."""
+    if dtype == "e4m3":
+        return store_round(np.asarray(x, dtype=np.float32) / np.float32(scale), dtype)
+    return store_round(x, dtype)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -134,6 +199,8 @@ class OracleKVCache:
         self.v = np.zeros(shape, dtype=storage_np_dtype(dtype))
         self.fill = np.zeros((n_layers, batch), dtype=np.int64)   # per-layer fill counts
         self.lens = np.zeros(batch, dtype=np.int64)               # committed lengths s_b
+        self.k_scale = np.ones(n_layers, dtype=np.float32)        # fp8 caches: stored = e4m3(x / scale)
+        self.v_scale = np.ones(n_layers, dtype=np.float32)
 
     # -- lengths ---------------------------------------------------------------------------
     def seq_len(self, layer: int | None = None) -> np.ndarray:
@@ -172,16 +239,23 @@ class OracleKVCache:
             raise ValueError("shape mismatch")
         if np.any(self.fill[layer] + T > self.max_len):
             raise OverflowError("append would exceed max_len")
-        kq = store_round(k_new, self.dtype)      # copies: the caller may reuse its buffers
-        vq = store_round(v_new, self.dtype)
+        kq = quantize_rows(k_new, self.dtype, self.k_scale[layer])   # copies: the caller may reuse its buffers
+        vq = quantize_rows(v_new, self.dtype, self.v_scale[layer])
         for b in range(B):
             f = int(self.fill[layer, b])
             self.k[layer, b, :, f:f + T] = kq[b]
             self.v[layer, b, :, f:f + T] = vq[b]
         self.fill[layer] += T
-        return [(stored_to_f64(self.k[layer, b, :, :self.fill[layer, b]], self.dtype),
-                 stored_to_f64(self.v[layer, b, :, :self.fill[layer, b]], self.dtype))
+        return [(self._read(layer, self.k[layer, b, :, :self.fill[layer, b]], True),
+                 self._read(layer, self.v[layer, b, :, :self.fill[layer, b]], False))
                 for b in range(B)]
+
+    def _read(self, layer, stored, is_k):
+        """Float64 values of stored elements of one layer (times the layer's scale for fp8)."""
+        x = stored_to_f64(stored, self.dtype)
+        if self.dtype == "e4m3":
+            x = x * float(self.k_scale[layer] if is_k else self.v_scale[layer])
+        return x
 
     def commit(self) -> None:
         """Advance every committed length to its fill, once per forward after the last layer."""
@@ -213,8 +287,8 @@ class OracleKVCache:
 
     def stored_f64(self, layer: int, b: int, kvh: int, n: int):
         """Float64 view of the first n stored rows of one (layer, sequence, K/V head)."""
-        return (stored_to_f64(self.k[layer, b, kvh, :n], self.dtype),
-                stored_to_f64(self.v[layer, b, kvh, :n], self.dtype))
+        return (self._read(layer, self.k[layer, b, kvh, :n], True),
+                self._read(layer, self.v[layer, b, kvh, :n], False))
 
 
 # ----------------------------------------------------------------------------------------------
@@ -254,6 +328,8 @@ class OraclePagedKVCache:
         self.free = set(range(n_blocks))
         self.fill = np.zeros((n_layers, batch), dtype=np.int64)
         self.lens = np.zeros(batch, dtype=np.int64)
+        self.k_scale = np.ones(n_layers, dtype=np.float32)
+        self.v_scale = np.ones(n_layers, dtype=np.float32)
 
     # -- blocks ----------------------------------------------------------------------------
     def held(self, b: int) -> int:
@@ -306,8 +382,8 @@ class OraclePagedKVCache:
         for b in range(B):
             for i in range(self.held(b), self.held(b) + need[b]):
                 self.table[b, i] = self.take_block()
-        kq = store_round(k_new, self.dtype)
-        vq = store_round(v_new, self.dtype)
+        kq = quantize_rows(k_new, self.dtype, self.k_scale[layer])
+        vq = quantize_rows(v_new, self.dtype, self.v_scale[layer])
         for b in range(B):
             blk, row = self.where(b, int(self.fill[layer, b]) + np.arange(T))
             self.k[layer, blk, :, row] = kq[b].transpose(1, 0, 2)     # [T, H, d] rows
@@ -349,8 +425,10 @@ class OraclePagedKVCache:
     def stored_f64(self, layer: int, b: int, kvh: int, n: int):
         """Float64 rows 0 .. n-1 of one (layer, sequence, K/V head), gathered through the table."""
         blk, row = self.where(b, np.arange(n))
-        return (stored_to_f64(self.k[layer, blk, kvh, row], self.dtype),
-                stored_to_f64(self.v[layer, blk, kvh, row], self.dtype))
+        return (self._read(layer, self.k[layer, blk, kvh, row], True),
+                self._read(layer, self.v[layer, blk, kvh, row], False))
+
+    _read = OracleKVCache._read
 
 
 # ----------------------------------------------------------------------------------------------
@@ -433,8 +511,11 @@ def attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_offset: int) -> np.nda
 
 
 def query_as_f64(q, dtype: str) -> np.ndarray:
-    """A float32 query rounded to the cache dtype (16-bit caches), as float64."""
+    """A float32 query rounded to the cache dtype (16-bit caches) or to float16 (fp8 caches, whose
+    values float16 holds exactly), as float64."""
     q = np.asarray(q)
+    if dtype == "e4m3":
+        return q.astype(np.float32).astype(np.float16).astype(np.float64)
     if dtype in ("f16", "bf16"):
         return stored_to_f64(store_round(q, dtype), dtype)
     if dtype == "f32":

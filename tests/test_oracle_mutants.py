@@ -180,3 +180,43 @@ def test_rope_frequency_off_by_two_is_caught(monkeypatch):
     """theta_i = base^(-i/d) instead of base^(-2i/d)."""
     monkeypatch.setattr(ko, "rope_theta", lambda d, base: float(base) ** (-np.arange(d // 2) / d))
     _fails(rope_pins.test_pair_frequencies_form_a_geometric_series, "half")
+
+
+# ---- fp8 storage (E4M3 with per-layer scales) ---------------------------------------------------------
+from tests import test_oracle_fp8 as fp8_pins
+
+
+def test_e4m3_truncating_instead_of_rounding_is_caught(monkeypatch):
+    def truncating(x):
+        x = np.asarray(x, dtype=np.float32).astype(np.float64)
+        a = np.abs(x)
+        _, ex = np.frexp(a)
+        q = np.ldexp(1.0, np.maximum(ex - 1, -6) - 3)
+        return ko.e4m3_encode((np.sign(x) * np.minimum(np.floor(a / q) * q, 448.0)).astype(np.float32))
+
+    monkeypatch.setattr(fp8_pins, "e4m3_encode", truncating)
+    _fails(fp8_pins.test_encode_matches_torch_in_range, 1.0)
+
+
+def test_e4m3_without_saturation_is_caught(monkeypatch):
+    orig = ko.e4m3_encode
+
+    def wrapping(x):
+        x = np.asarray(x, dtype=np.float32)
+        out = orig(x)
+        return np.where(np.abs(x) > 448, np.uint8(0x7F) | (out & 0x80), out).astype(np.uint8)   # NaN code
+
+    monkeypatch.setattr(fp8_pins, "e4m3_encode", wrapping)
+    _fails(fp8_pins.test_hand_worked_codes)
+
+
+def test_fp8_scale_multiplied_instead_of_divided_is_caught(monkeypatch):
+    orig = ko.quantize_rows
+
+    def multiplied(x, dtype, scale):
+        if dtype == "e4m3":
+            return ko.store_round(np.asarray(x, dtype=np.float32) * np.float32(scale), dtype)
+        return orig(x, dtype, scale)
+
+    monkeypatch.setattr(ko, "quantize_rows", multiplied)
+    _fails(fp8_pins.test_fp8_cache_stores_codes_of_x_over_scale, ko.OracleKVCache)
