@@ -35,8 +35,11 @@ extern "C" {
 
 typedef struct kvc_cache* kvc_handle;
 
-/* Storage / input element types. */
-typedef enum { KVC_F32 = 0, KVC_F16 = 1, KVC_BF16 = 2 } kvc_dtype;
+/* Storage / input element types. KVC_FP8_E4M3 is a cache (storage) type only: FP8 E4M3 codes (bias 7,
+ * no infinities, largest finite 448) of x / scale, with one scale per layer for K and one for V
+ * (kvc_set_kv_scales, default 1). Inputs to an fp8 cache may be F32, F16 or BF16; its queries F32 or
+ * F16 (the attention uses them in float16, which holds every E4M3 value exactly). */
+typedef enum { KVC_F32 = 0, KVC_F16 = 1, KVC_BF16 = 2, KVC_FP8_E4M3 = 3 } kvc_dtype;
 
 /* Return codes. */
 enum {
@@ -70,7 +73,8 @@ typedef enum {
  * batch_size, max_len): k, v of shape (L, B, H, max_len, d_head)"); "KV cache decoding",
  * KVCache listing (np.zeros: unfilled slots are zero).
  * The library owns the store (cudaMalloc) and frees it in kvc_destroy. All lengths start at 0.
- * Limits: 1 <= B <= KVC_MAX_BATCH, d_h in {32, 64, 128}, L*B*H_kv < 2^31, max_len < 2^31 - 256.
+ * Limits: 1 <= B <= KVC_MAX_BATCH, d_h in {32, 64, 128} ({64, 128} for KVC_FP8_E4M3), L*B*H_kv < 2^31,
+ * max_len < 2^30.
  */
 int kvc_create(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len, kvc_dtype dtype,
                void* stream);
@@ -161,6 +165,18 @@ int kvc_set_rope(kvc_handle h, double base, kvc_rope_style style, void* stream);
  */
 int kvc_append_rope(kvc_handle h, int layer, const void* k_new_dev, const void* v_new_dev,
                     kvc_dtype in_dtype, int T, void* stream);
+
+/*
+ * kvc_set_kv_scales — per-layer scales of an fp8 cache: k_scale_host[L] and v_scale_host[L] (host
+ * memory, copied), positive and finite. A row x of layer l is stored as E4M3(x / scale_l) (float32
+ * division, round to nearest even, saturating at +-448) and read as code * scale_l.
+ * Defined by: "KV cache decoding", "What is cached, what is not, and what it costs" (cache quantisation
+ * as a lever for decode's memory traffic). The pages give no format; E4M3 with per-layer scales is the
+ * reading used here.
+ * Errors: KVC_E_INVAL (not an fp8 cache, null, a scale <= 0 or not finite); KVC_E_STATE (any layer
+ * already holds rows: scales are fixed while the cache holds data).
+ */
+int kvc_set_kv_scales(kvc_handle h, const float* k_scale_host, const float* v_scale_host);
 
 /*
  * kvc_commit — advance every committed length s_b to its fill, once per forward after the last

@@ -13,7 +13,7 @@ import os
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkvc.so")
 _lib = None
 
-KVC_F32, KVC_F16, KVC_BF16 = 0, 1, 2
+KVC_F32, KVC_F16, KVC_BF16, KVC_FP8_E4M3 = 0, 1, 2, 3
 KVC_ROPE_HALF, KVC_ROPE_INTERLEAVED = 0, 1
 ROPE_STYLE = {"half": KVC_ROPE_HALF, "interleaved": KVC_ROPE_INTERLEAVED}
 KVC_COMMITTED = -1
@@ -35,6 +35,7 @@ SIGNATURES = {
     "kvc_append": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _vp]),
     "kvc_append_rope": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _vp]),
     "kvc_set_rope": (_c_int, [_vp, ctypes.c_double, _c_int, _vp]),
+    "kvc_set_kv_scales": (_c_int, [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     "kvc_commit": (_c_int, [_vp, _vp]),
     "kvc_truncate": (_c_int, [_vp, _c_int, _vp]),
     "kvc_truncate_ragged": (_c_int, [_vp, _i32p, _vp]),
@@ -99,12 +100,14 @@ def _torch():
 
 def dtype_code(t) -> int:
     torch = _torch()
-    return {torch.float32: KVC_F32, torch.float16: KVC_F16, torch.bfloat16: KVC_BF16}[t]
+    return {torch.float32: KVC_F32, torch.float16: KVC_F16, torch.bfloat16: KVC_BF16,
+            torch.float8_e4m3fn: KVC_FP8_E4M3}[t]
 
 
 def torch_dtype(code: int):
     torch = _torch()
-    return {KVC_F32: torch.float32, KVC_F16: torch.float16, KVC_BF16: torch.bfloat16}[code]
+    return {KVC_F32: torch.float32, KVC_F16: torch.float16, KVC_BF16: torch.bfloat16,
+            KVC_FP8_E4M3: torch.float8_e4m3fn}[code]
 
 
 def _stream(stream):
@@ -206,6 +209,14 @@ def kvc_append_rope(c: Cache, layer: int, k_new, v_new, stream=None):
         raise ValueError("k_new shape does not match the cache")
     _check(load().kvc_append_rope(c.h, layer, _ptr(k_new), _ptr(v_new), dtype_code(k_new.dtype),
                                   int(k_new.shape[2]), _stream(stream)), c.h)
+
+
+def kvc_set_kv_scales(c: Cache, k_scale, v_scale):
+    """Per-layer scales of an fp8 cache (sequences of L floats, or one float for every layer)."""
+    def arr(x):
+        vals = [float(x)] * c.L if isinstance(x, (int, float)) else [float(y) for y in x]
+        return (ctypes.c_float * c.L)(*vals)
+    _check(load().kvc_set_kv_scales(c.h, arr(k_scale), arr(v_scale)), c.h)
 
 
 def kvc_commit(c: Cache, stream=None):

@@ -19,6 +19,9 @@
 // kernel so the device copy changes in stream order with the rest of the forward.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <type_traits>
 
 #include "kvc_device.cuh"
 #include "kvc_internal.h"
@@ -65,30 +68,47 @@ struct Pack<__nv_bfloat16> {
   }
 };
 
-// N consecutive input elements (one output group) as float32: float32 input, or the cache dtype widened.
-template <typename Tc, bool kF32In>
+template <>
+struct Pack<dev::fp8> {
+  static constexpr int N = 16;
+  // x already divided by the layer's scale: round to nearest even, saturate to +-448
+  __device__ static uint4 from_f32(const float* x) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i], x[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i + 2], x[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
+      w[i] = (lo & 0xffffu) | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// n consecutive input elements as float32 (float32 input, or a 16-bit input widened exactly).
+template <typename Tin, int n>
 __device__ __forceinline__ void load_group(const void* src, long long off, float* x) {
-  constexpr int N = Pack<Tc>::N;
-  if constexpr (kF32In) {
+  if constexpr (std::is_same<Tin, float>::value) {
     const float* p = static_cast<const float*>(src) + off;
 #pragma unroll
-    for (int i = 0; i < N; i += 4) {
+    for (int i = 0; i < n; i += 4) {
       const float4 f = *reinterpret_cast<const float4*>(p + i);
       x[i] = f.x; x[i + 1] = f.y; x[i + 2] = f.z; x[i + 3] = f.w;
     }
   } else {
-    const Tc* p = static_cast<const Tc*>(src) + off;
+    const Tin* p = static_cast<const Tin*>(src) + off;
 #pragma unroll
-    for (int i = 0; i < N; ++i) x[i] = dev::to_f32<Tc>(p[i]);
+    for (int i = 0; i < n; ++i) x[i] = dev::to_f32<Tin>(p[i]);
   }
 }
 
-// One thread per 16-byte output group; grid covers 2 (K, V) x B x H x T x D / N groups.
-template <typename Tc, bool kF32In>
+// One thread per 16-byte output group; grid covers 2 (K, V) x B x H x T x D / N groups. Tc is the
+// storage type, Tin the input type (float32, the storage type itself, or a 16-bit type for fp8).
+template <typename Tc, typename Tin>
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   dev::pdl_wait();
   dev::pdl_trigger();
   constexpr int N = Pack<Tc>::N;
+  constexpr bool kFp8 = std::is_same<Tc, dev::fp8>::value;
   const int groups_per_row = a.D / N;
   const long long rows = static_cast<long long>(a.B) * a.H * a.T;
   const long long per_tensor = rows * groups_per_row;
@@ -117,34 +137,39 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   Tc* dst = static_cast<Tc*>(is_v ? a.v_store : a.k_store) + dst_row * a.D + grp * N;
   const long long src_off = row * a.D + grp * N;
   const void* src = is_v ? a.v_new : a.k_new;
+  const bool rotate = !is_v && a.rope.table != nullptr;
   uint4 out;
-  if (!is_v && a.rope.table != nullptr) {
-    // RoPE: rotate the key row by its absolute position (its write position) in float32, then round.
-    // The partners of this group's elements are the group D/2 away (style 0) or its own neighbours.
-    float x[N], y[N];
-    load_group<Tc, kF32In>(src, src_off, x);
-    const int e0 = grp * N;
-    if (a.rope.style == 0) {
-      load_group<Tc, kF32In>(src, src_off + (e0 < a.D / 2 ? a.D / 2 : -(a.D / 2)), y);
-    } else {
-#pragma unroll
-      for (int i = 0; i < N; ++i) y[i] = x[i ^ 1];
-    }
-    const float2* cs = a.rope.table + static_cast<long long>(pos) * (a.D >> 1);
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      int pair;
-      bool second;
-      dev::rope_partner(e0 + i, a.D, a.rope.style, &pair, &second);
-      x[i] = dev::rope_rotate(x[i], y[i], cs[pair], second);
-    }
-    out = Pack<Tc>::from_f32(x);
-  } else if constexpr (kF32In) {
-    float x[N];
-    load_group<Tc, true>(src, src_off, x);
-    out = Pack<Tc>::from_f32(x);
+  if (std::is_same<Tc, Tin>::value && !rotate) {
+    out = *reinterpret_cast<const uint4*>(static_cast<const Tc*>(src) + src_off);   // same type: a copy
   } else {
-    out = *reinterpret_cast<const uint4*>(static_cast<const Tc*>(src) + src_off);
+    float x[N];
+    load_group<Tin, N>(src, src_off, x);
+    if (rotate) {
+      // RoPE: turn the key row by its absolute position (its write position) in float32. The
+      // partners of this group's elements are the group D/2 away (style 0) or its own neighbours.
+      float y[N];
+      const int e0 = grp * N;
+      if (a.rope.style == 0) {
+        load_group<Tin, N>(src, src_off + (e0 < a.D / 2 ? a.D / 2 : -(a.D / 2)), y);
+      } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) y[i] = x[i ^ 1];
+      }
+      const float2* cs = a.rope.table + static_cast<long long>(pos) * (a.D >> 1);
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        int pair;
+        bool second;
+        dev::rope_partner(e0 + i, a.D, a.rope.style, &pair, &second);
+        x[i] = dev::rope_rotate(x[i], y[i], cs[pair], second);
+      }
+    }
+    if constexpr (kFp8) {
+      const float sc = is_v ? a.v_scale : a.k_scale;
+#pragma unroll
+      for (int i = 0; i < N; ++i) x[i] = __fdiv_rn(x[i], sc);
+    }
+    out = Pack<Tc>::from_f32(x);
   }
   *reinterpret_cast<uint4*>(dst) = out;
 }
@@ -192,25 +217,39 @@ __global__ void positions_kernel(const int32_t* lens, int B, int T, int32_t* out
   if (i < static_cast<long long>(B) * T) out[i] = lens[i / T] + static_cast<int>(i % T);
 }
 
-template <typename Tc>
+template <typename Tc, typename Tin>
 cudaError_t run_append(const AppendArgs& a, cudaStream_t st) {
   constexpr int N = Pack<Tc>::N;
   const long long total = 2LL * a.B * a.H * a.T * (a.D / N);
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
-  if (a.in_dtype == KVC_F32)
-    return launch_pdl(append_kernel<Tc, true>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, a);
-  else
-    return launch_pdl(append_kernel<Tc, false>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, a);
+  return launch_pdl(append_kernel<Tc, Tin>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, a);
+}
+
+template <typename Tc>
+cudaError_t run_append_in(const AppendArgs& a, cudaStream_t st) {
+  switch (a.in_dtype) {
+    case KVC_F32: return run_append<Tc, float>(a, st);
+    case KVC_F16:
+      if constexpr (std::is_same<Tc, __half>::value || std::is_same<Tc, dev::fp8>::value) return run_append<Tc, __half>(a, st);
+      break;
+    case KVC_BF16:
+      if constexpr (std::is_same<Tc, __nv_bfloat16>::value || std::is_same<Tc, dev::fp8>::value)
+        return run_append<Tc, __nv_bfloat16>(a, st);
+      break;
+    default: break;
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
   switch (a.cache_dtype) {
-    case KVC_F32: return run_append<float>(a, st);
-    case KVC_F16: return run_append<__half>(a, st);
-    case KVC_BF16: return run_append<__nv_bfloat16>(a, st);
+    case KVC_F32: return run_append_in<float>(a, st);
+    case KVC_F16: return run_append_in<__half>(a, st);
+    case KVC_BF16: return run_append_in<__nv_bfloat16>(a, st);
+    case KVC_FP8_E4M3: return run_append_in<dev::fp8>(a, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cstdint>
 #include <type_traits>
@@ -214,15 +215,28 @@ template <> __device__ __forceinline__ float from_f32<float>(float x) { return x
 template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-// A query element as the attention uses it: an F32 query meets a 16-bit cache rounded to it.
+// FP8 E4M3 storage: codes widened exactly to half, then to float (the scale is applied separately).
+using fp8 = __nv_fp8_e4m3;
+template <> __device__ __forceinline__ float to_f32<fp8>(fp8 x) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw(x.__x, __NV_E4M3)));
+}
+
+// The type a query is used in: the cache dtype for float32 and 16-bit caches, float16 for fp8 caches
+// (which float16 holds exactly).
+template <typename Tc> struct QueryOf { using T = Tc; };
+template <> struct QueryOf<fp8> { using T = __half; };
+
+// A query element as the attention uses it: an F32 query meets a 16-bit (or fp8) cache rounded to its
+// query type; a query given in that type is used as is.
 template <typename Tc>
 __device__ __forceinline__ float load_query(const void* q, kvc_dtype qt, long long i) {
+  using Q = typename QueryOf<Tc>::T;
   if (qt == KVC_F32) {
     const float x = static_cast<const float*>(q)[i];
-    if constexpr (sizeof(Tc) == 2) return to_f32<Tc>(from_f32<Tc>(x));
+    if constexpr (sizeof(Q) == 2) return to_f32<Q>(from_f32<Q>(x));
     return x;
   }
-  return to_f32<Tc>(static_cast<const Tc*>(q)[i]);
+  return to_f32<Q>(static_cast<const Q*>(q)[i]);
 }
 
 // ---- rotary positions ----------------------------------------------------------------------------
@@ -247,8 +261,9 @@ __device__ __forceinline__ float rope_rotate(float x, float y, float2 cs, bool s
 // A query element as given (float32, or the cache dtype widened), before any rounding.
 template <typename Tc>
 __device__ __forceinline__ float raw_query(const void* q, kvc_dtype qt, long long i) {
+  using Q = typename QueryOf<Tc>::T;
   if (qt == KVC_F32) return static_cast<const float*>(q)[i];
-  return to_f32<Tc>(static_cast<const Tc*>(q)[i]);
+  return to_f32<Q>(static_cast<const Q*>(q)[i]);
 }
 
 // Element e of the query row starting at element `row`, as the attention uses it: rotated to
@@ -261,7 +276,8 @@ __device__ __forceinline__ float load_query_rot(const AttnArgs& a, long long row
   const int pe = rope_partner(e, a.D, a.rope.style, &pair, &second);
   float r = rope_rotate(raw_query<Tc>(a.q, a.q_dtype, row + e), raw_query<Tc>(a.q, a.q_dtype, row + pe),
                         a.rope.table[static_cast<long long>(pos) * (a.D >> 1) + pair], second);
-  if constexpr (sizeof(Tc) == 2) r = to_f32<Tc>(from_f32<Tc>(r));
+  using Q = typename QueryOf<Tc>::T;
+  if constexpr (sizeof(Q) == 2) r = to_f32<Q>(from_f32<Q>(r));
   return r;
 }
 

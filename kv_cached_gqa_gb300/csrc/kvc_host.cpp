@@ -40,7 +40,7 @@ int cuda_fail(kvc_handle h, cudaError_t e, const char* what) {
   return fail(h, KVC_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-bool valid_dtype(int t) { return t == KVC_F32 || t == KVC_F16 || t == KVC_BF16; }
+bool valid_dtype(int t) { return t == KVC_F32 || t == KVC_F16 || t == KVC_BF16 || t == KVC_FP8_E4M3; }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -130,6 +130,8 @@ int check_sizes(int L, int B, int H_kv, int d_h, int max_len, int dtype) {
   if (B > KVC_MAX_BATCH) return fail(nullptr, KVC_E_INVAL, "B=%d exceeds KVC_MAX_BATCH", B);
   if (d_h != 32 && d_h != 64 && d_h != 128)
     return fail(nullptr, KVC_E_UNSUPPORTED, "d_h=%d: kernels exist for 32, 64 and 128", d_h);
+  if (dtype == KVC_FP8_E4M3 && d_h == 32)
+    return fail(nullptr, KVC_E_UNSUPPORTED, "fp8 caches need d_h 64 or 128 (rows of at least 64 bytes)");
   if (static_cast<long long>(L) * B * H_kv >= (1LL << 31) || max_len >= (1 << 30))
     return fail(nullptr, KVC_E_INVAL, "cache too large for 32-bit tile coordinates");
   return KVC_OK;
@@ -141,6 +143,8 @@ kvc_handle new_handle(int L, int B, int H_kv, int d_h, int max_len, kvc_dtype dt
   h->L = L; h->B = B; h->H = H_kv; h->D = d_h; h->max_len = max_len; h->dtype = dtype;
   h->fill.assign(static_cast<size_t>(L) * B, 0);
   h->lens.assign(B, 0);
+  h->k_scale.assign(L, 1.f);
+  h->v_scale.assign(L, 1.f);
   return h;
 }
 
@@ -236,7 +240,8 @@ bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max
   const int span = row_bytes >= 128 ? 128 : 64;
   const CUtensorMapDataType ty = dt == KVC_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : dt == KVC_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+                                 : dt == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_UINT8;   // fp8 codes
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(max_len),
                               static_cast<cuuint64_t>(planes)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
@@ -514,8 +519,8 @@ static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v
   if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
   if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
   if (!k_new || !v_new) return fail(h, KVC_E_INVAL, "null k_new/v_new");
-  if (!valid_dtype(in_dtype) || (in_dtype != KVC_F32 && in_dtype != h->dtype))
-    return fail(h, KVC_E_INVAL, "input dtype %d must be F32 or the cache dtype", in_dtype);
+  if (!kvc::input_dtype_ok(h->dtype, in_dtype))
+    return fail(h, KVC_E_INVAL, "input dtype %d: F32 or the cache dtype (F32, F16 or BF16 for an fp8 cache)", in_dtype);
   if (!aligned(k_new, 16) || !aligned(v_new, 16))
     return fail(h, KVC_E_INVAL, "k_new/v_new must be 16-byte aligned");
   int delta = 0;
@@ -539,6 +544,8 @@ static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v
     a.rope.table = h->d_rope;
     a.rope.style = h->rope_style;
   }
+  a.k_scale = h->k_scale[layer];
+  a.v_scale = h->v_scale[layer];
   cudaError_t e = kvc::launch_append(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "append launch");
   h->launches += 1;
@@ -575,6 +582,22 @@ int kvc_set_rope(kvc_handle h, double base, kvc_rope_style style, void* stream) 
   if (e != cudaSuccess) return cuda_fail(h, e, "rotary table launch");
   h->launches += 1;
   h->rope_style = style;
+  return KVC_OK;
+}
+
+int kvc_set_kv_scales(kvc_handle h, const float* k_scale, const float* v_scale) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (h->dtype != KVC_FP8_E4M3) return fail(h, KVC_E_INVAL, "scales belong to fp8 caches");
+  if (!k_scale || !v_scale) return fail(h, KVC_E_INVAL, "null scales");
+  for (int l = 0; l < h->L; ++l)
+    if (!(k_scale[l] > 0.f) || !(v_scale[l] > 0.f) || !std::isfinite(k_scale[l]) || !std::isfinite(v_scale[l]))
+      return fail(h, KVC_E_INVAL, "layer %d: scales must be positive and finite", l);
+  for (int32_t f : h->fill)
+    if (f != 0) return fail(h, KVC_E_STATE, "scales are fixed while the cache holds rows");
+  for (int l = 0; l < h->L; ++l) {
+    h->k_scale[l] = k_scale[l];
+    h->v_scale[l] = v_scale[l];
+  }
   return KVC_OK;
 }
 
@@ -672,8 +695,8 @@ static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, 
   if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
   if (!q || !out) return fail(h, KVC_E_INVAL, "null q/out");
   if (H_q < 1 || H_q % h->H) return fail(h, KVC_E_INVAL, "H_q=%d must be a positive multiple of H_kv=%d", H_q, h->H);
-  if (!valid_dtype(q_dtype) || (q_dtype != KVC_F32 && q_dtype != h->dtype))
-    return fail(h, KVC_E_INVAL, "query dtype %d must be F32 or the cache dtype", q_dtype);
+  if (!kvc::query_dtype_ok(h->dtype, q_dtype))
+    return fail(h, KVC_E_INVAL, "query dtype %d: F32 or the cache dtype (F16 for an fp8 cache)", q_dtype);
   if (!aligned(q, 16) || !aligned(out, 16)) return fail(h, KVC_E_INVAL, "q/out must be 16-byte aligned");
   if (s < KVC_COMMITTED) return fail(h, KVC_E_INVAL, "s=%d", s);
   for (int b = 0; b < h->B; ++b) {
@@ -718,6 +741,8 @@ static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, 
     a.rope.table = h->d_rope;
     a.rope.style = h->rope_style;
   }
+  a.k_scale = h->k_scale[layer];
+  a.v_scale = h->v_scale[layer];
   cudaError_t e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
   h->launches += 1;

@@ -18,7 +18,20 @@ constexpr int kMaxBatch = KVC_MAX_BATCH;
 // parameters, so this bounds their size (2 * 4 * kMaxUnits bytes).
 constexpr int kMaxUnits = 2048;
 
-inline int itemsize(kvc_dtype t) { return t == KVC_F32 ? 4 : 2; }
+inline int itemsize(kvc_dtype t) { return t == KVC_F32 ? 4 : t == KVC_FP8_E4M3 ? 1 : 2; }
+// Element types an append may hand to a cache of type `cache`: float32 or the cache dtype; an fp8
+// cache takes float32, float16 or bfloat16 rows.
+inline bool input_dtype_ok(kvc_dtype cache, int in) {
+  if (in == KVC_F32) return true;
+  if (cache == KVC_FP8_E4M3) return in == KVC_F16 || in == KVC_BF16;
+  return in == cache && in != KVC_FP8_E4M3;
+}
+// Element types a query may have: float32 or the type the attention uses it in (the cache dtype;
+// float16 for an fp8 cache).
+inline bool query_dtype_ok(kvc_dtype cache, int q) {
+  if (q == KVC_F32) return true;
+  return cache == KVC_FP8_E4M3 ? q == KVC_F16 : (q == cache && q != KVC_FP8_E4M3);
+}
 
 // Device status word values written by kernels whose bounded waits give up.
 constexpr int kStatusTimeout = 1;
@@ -67,6 +80,8 @@ struct AppendArgs {
   kvc_dtype cache_dtype, in_dtype;
   Paging pg;                // paged store: rows go through the block table
   Rope rope;                // rotate K rows by their positions before storing them (V untouched)
+  float k_scale = 1.f;      // fp8 caches: stored code = e4m3(x / scale)
+  float v_scale = 1.f;
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 
@@ -114,6 +129,8 @@ struct AttnArgs {
   kvc_dtype cache_dtype;
   Paging pg;                // paged store: tiles are gathered through the block table
   Rope rope;                // rotate each query row by its position s_b + t before attending
+  float k_scale = 1.f;      // fp8 caches: scores use code * k_scale, outputs code * v_scale
+  float v_scale = 1.f;
 };
 // Workspace floats the plan needs (0 when no unit splits).
 size_t splitk_workspace_floats(const SplitPlan& p, int D);
@@ -213,6 +230,8 @@ struct kvc_cache {
   // rotary positions (kvc_set_rope): cos/sin table [max_len, D / 2] on the device
   float2* d_rope = nullptr;
   int rope_style = -1;
+  // fp8 caches: per-layer scales (stored code = e4m3(x / scale)), 1 until kvc_set_kv_scales
+  std::vector<float> k_scale, v_scale;
   void* k = nullptr;
   void* v = nullptr;
   int32_t* d_lens = nullptr;      // committed lengths on the device

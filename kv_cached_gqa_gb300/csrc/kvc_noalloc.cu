@@ -80,8 +80,8 @@ extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_
   if (T < 1) return set_err(h, KVC_E_INVAL, "T=%d must be >= 1", T);
   if (!q || !out) return set_err(h, KVC_E_INVAL, "null q/out");
   if (H_q < 1 || H_q % h->H) return set_err(h, KVC_E_INVAL, "H_q=%d must be a positive multiple of H_kv=%d", H_q, h->H);
-  if ((q_dtype != KVC_F32 && q_dtype != KVC_F16 && q_dtype != KVC_BF16) || (q_dtype != KVC_F32 && q_dtype != h->dtype))
-    return set_err(h, KVC_E_INVAL, "query dtype %d must be F32 or the cache dtype", q_dtype);
+  if (!kvc::query_dtype_ok(h->dtype, q_dtype))
+    return set_err(h, KVC_E_INVAL, "query dtype %d: F32 or the cache dtype (F16 for an fp8 cache)", q_dtype);
   if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
     return set_err(h, KVC_E_INVAL, "q/out must be 16-byte aligned");
   if (s < KVC_COMMITTED) return set_err(h, KVC_E_INVAL, "s=%d", s);
@@ -128,6 +128,8 @@ extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_
   a.layer = layer; a.B = h->B; a.H_kv = h->H; a.H_q = H_q; a.G = G; a.T = T; a.D = h->D;
   a.max_len = h->max_len; a.delta = T; a.cache_dtype = h->dtype;
   a.pg = kvc_paging(h);
+  a.k_scale = h->k_scale[layer];
+  a.v_scale = h->v_scale[layer];
   e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return set_err(h, KVC_E_CUDA, "attention launch: %s", cudaGetErrorString(e));
   h->launches += 1;

@@ -26,6 +26,7 @@
 // the CTA skips its remaining work instead of hanging.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <type_traits>
 
@@ -105,6 +106,15 @@ template <> __device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4&
     f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
 }
+template <> __device__ __forceinline__ void unpack16<fp8>(const uint4& r, float* f) {   // 16 E4M3 codes
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 lo = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] & 0xffffu), __NV_E4M3)));
+    const float2 hi = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3)));
+    f[4 * i] = lo.x; f[4 * i + 1] = lo.y; f[4 * i + 2] = hi.x; f[4 * i + 3] = hi.y;
+  }
+}
 template <> __device__ __forceinline__ void unpack16<__half>(const uint4& r, float* f) {
   const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
@@ -122,7 +132,15 @@ __device__ __forceinline__ void load_v(const unsigned char* tile, int key, int l
   constexpr int BYTES = C::EPL * C::E;                  // bytes per lane: 2, 4, 8 or 16
   const int byte0 = lane * BYTES;
   const unsigned char* p = tile + tile_off<C>(key, byte0 >> 4) + (byte0 & 15);
-  if constexpr (BYTES == 16) {
+  if constexpr (sizeof(Tc) == 1) {                     // fp8: 2 or 4 codes
+#pragma unroll
+    for (int i = 0; i < BYTES; i += 2) {
+      const float2 x = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(
+          *reinterpret_cast<const __nv_fp8x2_storage_t*>(p + i), __NV_E4M3)));
+      v[i] = x.x;
+      v[i + 1] = x.y;
+    }
+  } else if constexpr (BYTES == 16) {
     unpack16<Tc>(*reinterpret_cast<const uint4*>(p), v);
   } else if constexpr (BYTES == 8) {
     const uint2 r = *reinterpret_cast<const uint2*>(p);
@@ -209,7 +227,7 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int n_keys = k_end - k_begin;
   const int nkt = (n_keys + C::TILE - 1) / C::TILE;
   // queries of the tile, prescaled by log2(e) / sqrt(d_h): scores are in base-2 units
-  const float qscale = kLog2e * rsqrtf(static_cast<float>(D));
+  const float qscale = kLog2e * rsqrtf(static_cast<float>(D)) * a.k_scale;   // k_scale: fp8 codes -> keys
   for (int i = tid; i < RMAX * D; i += kThreads) {
     const int r = i / D, e = i % D;
     float x = 0.f;
@@ -394,7 +412,7 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     if (aborted) continue;
     if (nsplit == 1) {
       const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-      a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / sm->l[r];
+      a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / sm->l[r] * a.v_scale;
     } else {
       a.part_o[(item_row0 + r) * D + d] = o;
       if (d == 0) {
@@ -430,7 +448,7 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       m = mn;
     }
     const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-    if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / l;
+    if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / l * a.v_scale;
   }
   if (tid == 0) *counter = 0;
 }
@@ -466,7 +484,9 @@ template <typename Tc>
 cudaError_t run_d(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, const CUtensorMap* tv,
                   cudaStream_t st) {
   switch (a.D) {
-    case 32: return run_rows<Tc, 32>(a, p, tk, tv, st);
+    case 32:
+      if constexpr (sizeof(Tc) > 1) return run_rows<Tc, 32>(a, p, tk, tv, st);   // fp8 rows need >= 64 B
+      return cudaErrorInvalidValue;
     case 64: return run_rows<Tc, 64>(a, p, tk, tv, st);
     case 128: return run_rows<Tc, 128>(a, p, tk, tv, st);
   }
@@ -477,6 +497,7 @@ cudaError_t run_d(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, 
 
 bool splitk_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys) {
   if (D != 32 && D != 64 && D != 128) return false;
+  if (dt == KVC_FP8_E4M3 && D == 32) return false;
   *rows_per_tile = rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
   *tile_keys = kTileBytes / (D * itemsize(dt));
   return true;
@@ -492,6 +513,7 @@ cudaError_t launch_splitk(const AttnArgs& a, const SplitPlan& p, const CUtensorM
     case KVC_F32: return run_d<float>(a, p, tk, tv, st);
     case KVC_F16: return run_d<__half>(a, p, tk, tv, st);
     case KVC_BF16: return run_d<__nv_bfloat16>(a, p, tk, tv, st);
+    case KVC_FP8_E4M3: return run_d<fp8>(a, p, tk, tv, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -9,9 +9,10 @@ import numpy as np
 
 import kvc_synth
 from oracle.kvc_oracle import (OracleKVCache, OraclePagedKVCache, gqa_cached_attention, rope_chunk,
-                               store_round, stored_to_f64)
+                               set_fp8_scales, store_round, stored_to_f64)
 
-DT = {"f32": 0, "f16": 1, "bf16": 2}
+DT = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
+QUERY_DT = {"f32": "f32", "f16": "f16", "bf16": "bf16", "e4m3": "f16"}   # the type a query is used in
 FP32_ATOL = 1e-5        # float32 caches: absolute, every output element
 REL_16 = 2e-3           # 16-bit caches: max |o - r| / max |r| over each (b, query head)
 
@@ -44,6 +45,16 @@ def check_rotated_store(got_bits, want_bits, dtype):
         m = np.abs(w).max(axis=-1, keepdims=True)
         assert np.all(np.abs(g - w) <= 2.0 ** -20 * m), "rotated float32 keys differ"
         return
+    if dtype == "e4m3":                      # codes: compare in code space (the scale cancels)
+        from oracle.kvc_oracle import e4m3_decode
+        g, w = e4m3_decode(got_bits.view(np.uint8)), e4m3_decode(want_bits.view(np.uint8))
+        _, ex = np.frexp(np.abs(w))
+        ulp = np.ldexp(1.0, np.maximum(ex - 1, -6) - 3)
+        m = np.abs(w).max(axis=-1, keepdims=True)
+        err = np.abs(g - w)
+        assert np.all(err <= ulp + 2.0 ** -21 * m), "rotated fp8 keys off by more than one grid step"
+        assert np.count_nonzero(err) / err.size < 5e-3
+        return
     npdt = np.float16 if dtype == "f16" else None
     if npdt is not None:
         g = got_bits.view(np.float16).astype(np.float64)
@@ -65,7 +76,8 @@ class Mirror:
     """A GPU cache and an oracle cache driven by the same calls (paged when `block` is given: a pool of
     `n_blocks` blocks, by default enough for every sequence at max_len)."""
 
-    def __init__(self, L, B, H_kv, d_h, max_len, dtype, seed=0, block=None, n_blocks=None, rope=None):
+    def __init__(self, L, B, H_kv, d_h, max_len, dtype, seed=0, block=None, n_blocks=None, rope=None,
+                 scales=None):
         import torch
         from kv_cached_gqa_gb300 import _binding as kb
         self.torch, self.kb = torch, kb
@@ -82,6 +94,9 @@ class Mirror:
         self.rope = rope                      # (base, style): keys and queries rotated by position
         if rope is not None:
             kb.kvc_set_rope(self.gpu, rope[0], rope[1])
+        if scales is not None:                # fp8: (k_scale, v_scale) per layer
+            set_fp8_scales(self.ref, *scales)
+            kb.kvc_set_kv_scales(self.gpu, self.ref.k_scale, self.ref.v_scale)
 
     def draw(self, shape):
         self.n_draws += 1
@@ -94,12 +109,13 @@ class Mirror:
     def append(self, layer, T, in_dtype="f32"):
         k = self.draw((self.B, self.H, T, self.d))
         v = self.draw((self.B, self.H, T, self.d))
+        # the oracle stores what the GPU receives: the float32 draws, or their 16-bit rounding
+        def given(x):
+            return x if in_dtype == "f32" else stored_to_f64(store_round(x, in_dtype), in_dtype).astype(np.float32)
+        k_in = given(k)
         if self.rope is not None:
-            # the oracle rotates the values the GPU receives (rounded first if given in 16 bits)
-            k_in = k if in_dtype == "f32" else stored_to_f64(store_round(k, in_dtype), in_dtype).astype(np.float32)
-            self.ref.append(layer, rope_chunk(k_in, self.ref.seq_len(layer), *self.rope), v)
-        else:
-            self.ref.append(layer, k, v)
+            k_in = rope_chunk(k_in, self.ref.seq_len(layer), *self.rope)
+        self.ref.append(layer, k_in, given(v))
         if in_dtype == "f32":
             kd, vd = self.dev(k), self.dev(v)
         else:
@@ -152,11 +168,12 @@ class Mirror:
     def store_bits(self):
         """GPU store as raw bits and the oracle store as raw bits (same dtype/shape)."""
         torch = self.torch
-        view = torch.int32 if self.dtype == "f32" else torch.int16
+        view, npview = {"f32": (torch.int32, np.int32), "e4m3": (torch.uint8, np.uint8)}.get(
+            self.dtype, (torch.int16, np.int16))
         gk = self.gpu.k.view(view).cpu().numpy()
         gv = self.gpu.v.view(view).cpu().numpy()
-        rk = self.ref.k.view(np.int32 if self.dtype == "f32" else np.int16)
-        rv = self.ref.v.view(np.int32 if self.dtype == "f32" else np.int16)
+        rk = self.ref.k.view(npview)
+        rv = self.ref.v.view(npview)
         return (gk, gv), (rk, rv)
 
     def check_state(self):
