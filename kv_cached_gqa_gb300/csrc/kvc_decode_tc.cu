@@ -22,6 +22,8 @@
 // A unit with several splits writes (m, l, o) partials; the CTA that finishes its last split
 // merges them (log-sum-exp) while they are in L2. Every wait is bounded (~1 s): a wait that gives
 // up sets the device status word and the CTA skips the rest of its work, frees its TMEM and exits.
+#include <type_traits>
+
 #include "kvc_device.cuh"
 #include "kvc_internal.h"
 
@@ -37,28 +39,38 @@ constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kMergeSplits = 31;            // splits merged through shared memory (else a running merge)
 
-// Shared memory per CTA stays under ~110 KB so that two CTAs share an SM: the K/V ring holds 96 KB
-// (3 tiles of 32 KB for d_h = 128, 6 of 16 KB for d_h = 64), plus Q^T and one P^T buffer (hi, lo).
-template <int NR, int DH>
+// Shared memory per CTA stays under ~110 KB so that two CTAs share an SM. 16-bit caches: the K/V ring
+// holds 96 KB (3 tiles of 32 KB for d_h = 128, 6 of 16 KB for d_h = 64), plus Q^T and one P^T buffer
+// (hi, lo). fp8 caches (d_h = 128): a 2-stage ring of 16 KB fp8 tiles, plus two 32 KB float16 tiles the
+// softmax warps widen the fp8 tiles into, alternately (the MMAs read those), so that one tile is
+// widened while the MMAs work on the other.
+template <int NR, int DH, bool F8>
 struct Layout {
-  static constexpr int kBoxes = DH / 64;                        // 64-element boxes per key row
-  static constexpr int kTileBytes = kBoxes * kBoxBytes;         // a tile's K (or V) rows
-  static constexpr int kStages = 96 * 1024 / kTileBytes;
+  static constexpr int kBoxes = DH / 64;                        // 64-element boxes per key row (MMA view)
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;         // a tile's K (or V) rows in 16 bits
+  static constexpr int kStageBytes = F8 ? kTK * DH : kTileBytes;   // what TMA brings per tile
+  static constexpr int kLoadBoxes = F8 ? DH / 128 : kBoxes;     // 128-byte column boxes TMA loads
+  static constexpr int kLoadInner = F8 ? 128 : 64;              // elements per loaded box row
+  static constexpr int kStages = F8 ? 2 : 96 * 1024 / kTileBytes;
+  static constexpr int kConvBufs = F8 ? 2 : 0;
   static constexpr int kPBufs = 1;
   static constexpr int kQBytes = NR * DH * 2;                   // Q^T: atoms of NR rows x 128 B
   static constexpr int kPBytes = NR * 256;                      // one P^T operand (hi or lo): 128 keys
   static constexpr int kStageOff = 0;
-  static constexpr int kQOff = kStages * kTileBytes;
+  static constexpr int kConvOff = kStages * kStageBytes;        // fp8: the widened tile
+  static constexpr int kQOff = kConvOff + kConvBufs * kTileBytes;
   static constexpr int kPOff = kQOff + kQBytes;                 // kPBufs buffers x (hi, lo)
   static constexpr int kCtlOff = kPOff + 2 * kPBufs * kPBytes;
   static constexpr int kSTiles = (kTmemCols - NR) / NR;         // S^T tiles that fit beside O^T
 };
 
-template <int NR, int DH>
+template <int NR, int DH, bool F8>
 struct __align__(8) Ctl {
-  unsigned long long full[Layout<NR, DH>::kStages], empty[Layout<NR, DH>::kStages];
-  unsigned long long p_full[Layout<NR, DH>::kPBufs], p_empty[Layout<NR, DH>::kPBufs];
-  unsigned long long s_ready[Layout<NR, DH>::kSTiles];         // one per K tile, used once
+  using Lo = Layout<NR, DH, F8>;
+  unsigned long long full[Lo::kStages], empty[Lo::kStages];
+  unsigned long long p_full[Lo::kPBufs], p_empty[Lo::kPBufs];
+  unsigned long long s_ready[Lo::kSTiles];                     // one per K tile, used once
+  unsigned long long k_conv[2];                                // fp8: a K tile widened into buffer c
   unsigned long long o_full, done;
   uint32_t tmem;
   int abort, last;
@@ -68,13 +80,37 @@ struct __align__(8) Ctl {
 
 // Dynamic shared memory per CTA. At least 80 KB, so that no more than two CTAs are ever resident on
 // an SM: each holds 256 of the SM's 512 TMEM columns, and a third could wait forever on tcgen05.alloc.
-template <int NR, int DH>
+template <int NR, int DH, bool F8>
 constexpr size_t smem_bytes() {
-  return (1024 + Layout<NR, DH>::kCtlOff + sizeof(Ctl<NR, DH>)) > 80 * 1024
-             ? (1024 + Layout<NR, DH>::kCtlOff + sizeof(Ctl<NR, DH>)) : 80 * 1024;
+  return (1024 + Layout<NR, DH, F8>::kCtlOff + sizeof(Ctl<NR, DH, F8>)) > 80 * 1024
+             ? (1024 + Layout<NR, DH, F8>::kCtlOff + sizeof(Ctl<NR, DH, F8>)) : 80 * 1024;
 }
 static_assert(3 * 80 * 1024 > 228 * 1024, "three CTAs must not fit on one SM");
-static_assert((2 * 16 * kMergeSplits + 16) * 4 <= 2 * Layout<16, 64>::kPBytes, "merge scratch fits the P buffer");
+static_assert(2 * smem_bytes<16, 128, true>() + 2048 <= 228 * 1024, "two fp8 CTAs fit on one SM");
+static_assert((2 * 16 * kMergeSplits + 16) * 4 <= 2 * Layout<16, 64, false>::kPBytes, "merge scratch fits the P buffer");
+
+// Widen this thread's key row of an fp8 tile (128 keys x 128 one-byte codes, 128-byte swizzled as TMA
+// wrote it) into the float16 tile the MMAs read (two 64-column 128-byte-swizzled boxes). Codes convert
+// exactly; the layer's scale is applied to the scores and outputs instead.
+__device__ __forceinline__ void widen_fp8_row(const unsigned char* src, unsigned char* dst, int row) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {                  // 16-byte chunk c = elements 16c .. 16c+15
+    const uint4 w = *reinterpret_cast<const uint4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)         // 4 codes -> 2 float16 pairs, in element order
+      asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+          " cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+          : "=r"(h[2 * i]), "=r"(h[2 * i + 1]) : "r"(in[i]));
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {                // float16 chunk 2c + k: box (2c + k) / 8, chunk (2c + k) % 8
+      const int ch = 2 * c + k, box = ch >> 3, cc = ch & 7;
+      *reinterpret_cast<uint4*>(dst + box * kBoxBytes + row * 128 + ((cc ^ (row & 7)) << 4)) =
+          make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+    }
+  }
+}
 
 // Byte offset of element (row, col) in an [rows][128] 16-bit matrix stored as two 128-byte-swizzled
 // atoms of 64 columns (the layout TMA writes and the tensor cores read, K-major).
@@ -95,18 +131,21 @@ template <typename Tc, int NR, int DH>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
                  const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
-  using Lo = Layout<NR, DH>;
+  constexpr bool kF8 = std::is_same<Tc, fp8>::value;           // fp8 cache: tiles widened to float16
+  using Tm = typename std::conditional<kF8, __half, Tc>::type;  // MMA operand type
+  using Lo = Layout<NR, DH, kF8>;
   constexpr int kStages = Lo::kStages, kPBufs = Lo::kPBufs, kDh = DH, kTileBytes = Lo::kTileBytes;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctl<NR, DH>* ctl = reinterpret_cast<Ctl<NR, DH>*>(sm + Lo::kCtlOff);
+  Ctl<NR, DH, kF8>* ctl = reinterpret_cast<Ctl<NR, DH, kF8>*>(sm + Lo::kCtlOff);
   const uint32_t s_stage = smem_u32(sm + Lo::kStageOff);
   const uint32_t s_q = smem_u32(sm + Lo::kQOff);
   unsigned char* p_base = sm + Lo::kPOff;
   const uint32_t s_p = smem_u32(p_base);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr uint32_t kFmt = std::is_same<Tc, __nv_bfloat16>::value ? 1u : 0u;
+  constexpr uint32_t kFmt = std::is_same<Tm, __nv_bfloat16>::value ? 1u : 0u;
+  const uint32_t s_conv = smem_u32(sm + Lo::kConvOff);       // fp8: the widened tile
 
   // ---- which (unit, K/V head, split) this CTA owns --------------------------------------------
   const int item = blockIdx.x;
@@ -129,8 +168,11 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      // a stage is free again after the MMAs read it (16-bit) or the four softmax warps widened it (fp8)
+      mbar_init(smem_u32(&ctl->empty[s]), kF8 ? kSoftmaxThreads / 32 : 1);
     }
+    mbar_init(smem_u32(&ctl->k_conv[0]), kSoftmaxThreads / 32);
+    mbar_init(smem_u32(&ctl->k_conv[1]), kSoftmaxThreads / 32);
     for (int s = 0; s < kPBufs; ++s) {
       mbar_init(smem_u32(&ctl->p_full[s]), kSoftmaxThreads / 32);
       mbar_init(smem_u32(&ctl->p_empty[s]), 1);
@@ -157,7 +199,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
       x = load_query_rot<Tc>(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh, d, s_b + t);
     }
-    *reinterpret_cast<Tc*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tc>(x);
+    *reinterpret_cast<Tm*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tm>(x);
   }
   for (int i = tid; i < 2 * kPBufs * Lo::kPBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(p_base)[i] = make_uint4(0, 0, 0, 0);
@@ -185,10 +227,11 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       int ok = 1;
       if (lane == 0) {
         ok = mbar_wait(smem_u32(&ctl->empty[st]), ((i / kStages) & 1) ^ 1, abort_flag);
-        if (ok) mbar_expect_tx(full, kTileBytes);
+        if (ok) mbar_expect_tx(full, Lo::kStageBytes);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      issue_piece<kTK, Lo::kBoxes, 128, 64>(pc, isv ? &tv : &tk, s_stage + st * kTileBytes, full, lane);
+      issue_piece<kTK, Lo::kLoadBoxes, 128, Lo::kLoadInner>(pc, isv ? &tv : &tk, s_stage + st * Lo::kStageBytes,
+                                                           full, lane);
       issued = i + 1;
     }
     // drain: the last copy issued into each stage has landed before the CTA can exit
@@ -203,26 +246,28 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       bool ok = true;
       for (int i = 0; i < nkt && ok; ++i) {                 // S^T_i = K_i . Q^T
         const int st = i % kStages;
-        ok = mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag);
+        ok = kF8 ? mbar_wait(smem_u32(&ctl->k_conv[i & 1]), (i >> 1) & 1, abort_flag)
+                 : mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t kt = s_stage + st * kTileBytes;
+        const uint32_t kt = kF8 ? s_conv + (i & 1) * kTileBytes : s_stage + st * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kDh / 16; ++ks)
           umma_f16(tmem + i * NR,
                    umma_desc(kt + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024, kSwizzle128),
                    umma_desc(s_q + (ks >> 2) * (NR * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128),
                    idesc_s, ks > 0);
-        umma_commit(smem_u32(&ctl->empty[st]));
-        umma_commit(smem_u32(&ctl->s_ready[i]));
+        if (!kF8) umma_commit(smem_u32(&ctl->empty[st]));
+        umma_commit(smem_u32(&ctl->s_ready[i]));          // fp8: also "the widened tile is free"
       }
       for (int i = 0; i < nkt && ok; ++i) {                 // O^T += V_i^T . P_i^T (hi, then lo)
         const int ti = nkt + i, st = ti % kStages, pb = i % kPBufs;
-        ok = mbar_wait(smem_u32(&ctl->full[st]), (ti / kStages) & 1, abort_flag) &&
+        // fp8: p_full also means V_i has been widened
+        ok = (kF8 || mbar_wait(smem_u32(&ctl->full[st]), (ti / kStages) & 1, abort_flag)) &&
              mbar_wait(smem_u32(&ctl->p_full[pb]), (i / kPBufs) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t vt = s_stage + st * kTileBytes;
+        const uint32_t vt = kF8 ? s_conv + (ti & 1) * kTileBytes : s_stage + st * kTileBytes;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
           const uint32_t pt = s_p + (pb * 2 + part) * Lo::kPBytes;
@@ -233,8 +278,8 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
                      umma_desc(pt + (ks >> 2) * (NR * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128),
                      idesc_o, (i | part | ks) != 0);
         }
-        umma_commit(smem_u32(&ctl->empty[st]));
-        umma_commit(smem_u32(&ctl->p_empty[pb]));
+        if (!kF8) umma_commit(smem_u32(&ctl->empty[st]));
+        umma_commit(smem_u32(&ctl->p_empty[pb]));          // fp8: also "the widened tile is free"
       }
       if (ok) umma_commit(smem_u32(&ctl->o_full));
       umma_commit(smem_u32(&ctl->done));
@@ -246,7 +291,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     const int kslot = quad * 32 + lane;                     // key within a tile; d in the epilogue
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int w4 = warp - 2;
-    const float scale = kLog2e * rsqrtf(static_cast<float>(kDh));
+    const float scale = kLog2e * rsqrtf(static_cast<float>(kDh)) * a.k_scale;   // k_scale: fp8 codes -> keys
     int trow[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) trow[r] = (r < nrows) ? s_b + (row0 + r) / a.G : -1;   // last visible key
@@ -254,12 +299,34 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     // pass 1, overlapped with the K stream: fold each score tile into the row maxima as soon as
     // its MMAs complete
     bool ok = true;
+    // fp8: widen ring tile `ti` (K tiles 0 .. nkt-1, then V tiles) into float16 buffer ti % 2, release
+    // the ring stage and, for a K tile, tell the MMA warp
+    auto widen = [&](int ti) -> bool {
+      const int st = ti % kStages;
+      if (!mbar_wait(smem_u32(&ctl->full[st]), (ti / kStages) & 1, abort_flag)) return false;
+      widen_fp8_row(sm + Lo::kStageOff + st * Lo::kStageBytes, sm + Lo::kConvOff + (ti & 1) * kTileBytes, kslot);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&ctl->empty[st]));
+        if (ti < nkt) mbar_arrive(smem_u32(&ctl->k_conv[ti & 1]));
+      }
+      return true;
+    };
+    if constexpr (kF8) {                                    // two K tiles ahead of the MMAs
+      ok = widen(0);
+      if (ok && nkt > 1) ok = widen(1);
+    }
     float m_run[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) m_run[r] = -INFINITY;
     for (int i = 0; i < nkt && ok; ++i) {
       ok = mbar_wait(smem_u32(&ctl->s_ready[i]), 0, abort_flag);
       if (!ok) break;
+      // fp8: QK_i has read buffer i % 2, so K_{i+2} takes its place while QK_{i+1} runs
+      if constexpr (kF8) {
+        if (i + 2 < nkt && !(ok = widen(i + 2))) break;
+      }
       tc_fence_after();
       float v[NR];
 #pragma unroll
@@ -285,6 +352,11 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     float l_run[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) l_run[r] = 0.f;
+    // fp8: every QK is done (all S tiles were read above), so both buffers are free for V_0 and V_1
+    if constexpr (kF8) {
+      if (ok) ok = widen(nkt);
+      if (ok && nkt > 1) ok = widen(nkt + 1);
+    }
     for (int i = 0; i < nkt && ok; ++i) {
       const int pb = i % kPBufs;
       ok = mbar_wait(smem_u32(&ctl->p_empty[pb]), ((i / kPBufs) & 1) ^ 1, abort_flag);
@@ -300,16 +372,20 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
         if (r < nrows) {
           const float p = (kabs < k_end && kabs <= trow[r]) ? exp2f(v[r] * scale - m_run[r]) : 0.f;
           l_run[r] += p;
-          const Tc h16 = from_f32<Tc>(p);
-          const Tc l16 = from_f32<Tc>(p - to_f32<Tc>(h16));
+          const Tm h16 = from_f32<Tm>(p);
+          const Tm l16 = from_f32<Tm>(p - to_f32<Tm>(h16));
           const uint32_t off = sw128(NR, r, kslot);
-          *reinterpret_cast<Tc*>(ph + off) = h16;
-          *reinterpret_cast<Tc*>(pl + off) = l16;
+          *reinterpret_cast<Tm*>(ph + off) = h16;
+          *reinterpret_cast<Tm*>(pl + off) = l16;
         }
       }
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[pb]));
+      // fp8: PV_{i-1} is done (p_empty above), so V_{i+1} takes V_{i-1}'s buffer while PV_i runs
+      if constexpr (kF8) {
+        if (i >= 1 && i + 1 < nkt && !(ok = widen(nkt + i + 1))) break;
+      }
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -345,7 +421,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
         if (r < nrows) {
           const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
           if (nsplit == 1) {
-            a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = o[r] / ctl->l[r];
+            a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = o[r] / ctl->l[r] * a.v_scale;
           } else {
             a.part_o[(item_row0 + r) * kDh + d] = o[r];
             if (d == 0) {
@@ -403,7 +479,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
               acc = fmaf(wm[r * kMergeSplits + sp],
                          __ldcg(a.part_o + (first_row + static_cast<long long>(sp) * NR + r) * kDh + d), acc);
             const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-            if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc * linv[r];
+            if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc * linv[r] * a.v_scale;
           }
         } else {
           for (int r = 0; r < nrows && d_ok; ++r) {
@@ -419,7 +495,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
               m = mn;
             }
             const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-            if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l;
+            if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l * a.v_scale;
           }
         }
         if (tid == 64) *counter = 0;
@@ -440,7 +516,7 @@ template <typename Tc, int NR, int DH>
 cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, const CUtensorMap* tv,
                 cudaStream_t st) {
   auto kern = decode_tc_kernel<Tc, NR, DH>;
-  const size_t smem = smem_bytes<NR, DH>();
+  const size_t smem = smem_bytes<NR, DH, std::is_same<Tc, fp8>::value>();
   cudaError_t e = ensure_smem_limit<decode_tc_kernel<Tc, NR, DH>>(smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(p.n_items), dim3(kThreads), smem, st, a, p, *tk, *tv);
@@ -451,16 +527,19 @@ cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, co
 // Up to 16 query rows per K/V head (decode, G * T <= 16); longer chunks run on the chunk kernel,
 // which measured faster from 32 rows on.
 bool decode_tc_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys, int* max_tiles) {
-  if ((dt != KVC_F16 && dt != KVC_BF16) || (D != 64 && D != 128) || rows > 16) return false;
+  if (rows > 16) return false;
+  if (dt == KVC_FP8_E4M3 ? D != 128 : ((dt != KVC_F16 && dt != KVC_BF16) || (D != 64 && D != 128))) return false;
   *rows_per_tile = 16;
   *tile_keys = kTK;
-  *max_tiles = Layout<16, 128>::kSTiles;
+  *max_tiles = Layout<16, 128, false>::kSTiles;
   return true;
 }
 
 cudaError_t launch_decode_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
                              const CUtensorMap* tv, cudaStream_t st) {
   if (p.rows_per_tile != 16) return cudaErrorInvalidValue;
+  if (a.cache_dtype == KVC_FP8_E4M3)
+    return a.D == 128 ? run<fp8, 16, 128>(a, p, tk, tv, st) : cudaErrorInvalidValue;
   if (a.D == 128)
     return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16, 128>(a, p, tk, tv, st) : run<__half, 16, 128>(a, p, tk, tv, st);
   return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16, 64>(a, p, tk, tv, st) : run<__half, 16, 64>(a, p, tk, tv, st);

@@ -134,6 +134,9 @@ WORKLOADS = {
     "llama3-8b-decode-bf16-rope": dict(L=32, B=64, H_q=32, H_kv=8, d_h=128, s_lo=512, s_hi=4096, T=1,
                                        dtype="bf16", max_len=4160, rope_base=500000.0, rope_style="half",
                                        seed=0),
+    # the decode batch in an FP8 E4M3 cache (scale 1 for every layer): half the bytes per key
+    "llama3-8b-decode-fp8": dict(L=32, B=64, H_q=32, H_kv=8, d_h=128, s_lo=512, s_hi=4096, T=1,
+                                 dtype="e4m3", max_len=4160, seed=0),
     "llama3-8b-verify-fp16": dict(L=32, B=16, H_q=32, H_kv=8, d_h=128, s=2048, T=8, rollback=5,
                                   dtype="f16", max_len=2112, seed=0),
     "llama3-8b-prefill-fp16": dict(L=32, B=16, H_q=32, H_kv=8, d_h=128, s=1024, T=512,

@@ -19,8 +19,8 @@ import numpy as np
 import kvc_synth
 from kvc_synth import STREAM_K_PREFILL, STREAM_K_STEP, STREAM_Q, STREAM_V_PREFILL, STREAM_V_STEP, stream_id
 
-DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
-ITEMSIZE = {"f32": 4, "f16": 2, "bf16": 2}
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
+ITEMSIZE = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
 
 
 @dataclass

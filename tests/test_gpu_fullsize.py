@@ -26,7 +26,7 @@ def _run_and_sample(wl, samples):
     kb.kvc_commit(wl.cache)
     kb.kvc_status(wl.cache)
     G = wl.H_q // wl.H_kv
-    view = torch.int32 if wl.dtype == "f32" else torch.int16
+    view = {"f32": torch.int32, "e4m3": torch.uint8}.get(wl.dtype, torch.int16)
     for layer, b, kvh in samples:
         s_b = int(wl.lengths[b])
         ref = OracleKVCache(1, 1, 1, wl.d_h, s_b + wl.T, wl.dtype)
@@ -43,15 +43,16 @@ def _run_and_sample(wl, samples):
         want = gqa_cached_attention(ref, 0, qh[None])
         got = outs[layer][b, kvh * G:(kvh + 1) * G].cpu().numpy()[None]
         check_outputs(got, want, wl.dtype, f"layer {layer} b {b} kvh {kvh}")
-        for store, want_rows in ((wl.cache.k, ref.k[0, 0, 0]), (wl.cache.v, ref.v[0, 0, 0])):
+        for is_k, store, want_rows in ((True, wl.cache.k, ref.k[0, 0, 0]), (False, wl.cache.v, ref.v[0, 0, 0])):
+            bits = store.view(view)             # raw bits first: no indexing on float8 tensors
             if wl.block:                        # gather the sequence's rows through its block table
                 p = torch.arange(s_b + wl.T)
                 blk = torch.tensor(kb.kvc_block_table(wl.cache)[0][b])[p // wl.block]
-                stored = store[layer][blk.cuda(), kvh, (p % wl.block).cuda()]
+                stored = bits[layer][blk.cuda(), kvh, (p % wl.block).cuda()]
             else:
-                stored = store[layer, b, kvh, :s_b + wl.T]
-            stored = stored.contiguous().view(view).cpu().numpy()
-            if wl.rope_base and store is wl.cache.k:
+                stored = bits[layer, b, kvh, :s_b + wl.T]
+            stored = stored.contiguous().cpu().numpy()
+            if wl.rope_base and is_k:
                 check_rotated_store(stored, want_rows.view(stored.dtype), wl.dtype)
             else:
                 np.testing.assert_array_equal(stored, want_rows.view(stored.dtype))
@@ -99,3 +100,10 @@ def test_llama3_8b_decode_bf16_rope_full_size():
     wl = kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-decode-bf16-rope"))
     lo, hi = int(np.argmin(wl.lengths)), int(np.argmax(wl.lengths))
     _run_and_sample(wl, [(0, lo, 0), (31, hi, 7), (9, 30, 4)])
+
+
+def test_llama3_8b_decode_fp8_full_size():
+    """The ragged decode batch in an FP8 E4M3 cache (scale 1): tensor-core decode over widened tiles."""
+    wl = kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-decode-fp8"))
+    lo, hi = int(np.argmin(wl.lengths)), int(np.argmax(wl.lengths))
+    _run_and_sample(wl, [(0, lo, 0), (31, hi, 7), (20, 11, 2)])
