@@ -24,6 +24,8 @@ It computes the plain definitions, in float64, one (sequence, head) at a time:
   decoding", "Why the causal mask makes caching exact");
 * the paged cache: fixed-size blocks and a per-sequence block table ("KV cache decoding",
   "Batching caches of different lengths");
+* the MLA latent cache and the absorbed multi-head latent attention that reads it ("KV cache,
+  incremental decode, ...", §2.6; the attention is DeepSeek-V2's, which the pages name through MLA);
 * rotary positions applied to the keys before they are stored and to the queries before they
   attend ("KV cache decoding", "Position information with a cache"; the formula is the RoFormer
   paper's, which the pages name but do not print).
@@ -546,6 +548,88 @@ def gqa_cached_attention(cache, layer: int, q, T: int | None = None) -> np.ndarr
         for h in range(H_q):
             k, v = cache.stored_f64(layer, b, h // G, N)
             out[b, h] = attend(q64[b, h], k, v, q_offset=s)
+    return out
+
+
+# ----------------------------------------------------------------------------------------------
+# The latent cache ("KV cache, incremental decode, ...", §2.6 "The latent cache": MLA caches one
+# compressed latent c in R^r and one shared RoPE key k^R in R^{d_R} per position instead of per-head
+# K and V; it follows the same rules (per-layer fill, committed length, rollback) on [B, T, r] and
+# [B, T, d_R] chunks, and its nbytes is L B N_max (r + d_R) times the item size).
+# ----------------------------------------------------------------------------------------------
+
+class OracleLatentCache:
+    """Per layer a latent store C [B, max_len, r] and a RoPE-key store KR [B, max_len, d_R]."""
+
+    def __init__(self, n_layers: int, batch: int, r: int, d_rope: int, max_len: int, dtype: str = "f32"):
+        if dtype not in DTYPES or dtype == "e4m3":
+            raise ValueError(f"unsupported dtype {dtype!r}")
+        if min(n_layers, batch, r, d_rope, max_len) <= 0:
+            raise ValueError("all sizes must be positive")
+        self.L, self.B, self.r, self.d_rope, self.max_len, self.dtype = n_layers, batch, r, d_rope, max_len, dtype
+        self.c = np.zeros((n_layers, batch, max_len, r), dtype=storage_np_dtype(dtype))
+        self.kr = np.zeros((n_layers, batch, max_len, d_rope), dtype=storage_np_dtype(dtype))
+        self.fill = np.zeros((n_layers, batch), dtype=np.int64)
+        self.lens = np.zeros(batch, dtype=np.int64)
+
+    seq_len = OracleKVCache.seq_len
+    committed = OracleKVCache.committed
+    positions = OracleKVCache.positions
+    commit = OracleKVCache.commit
+    truncate = OracleKVCache.truncate
+
+    def append(self, layer: int, c_new, kr_new):
+        """Write a [B, T, r] latent chunk and a [B, T, d_R] RoPE-key chunk at each sequence's fill;
+        return the stored rows (rounded) of every sequence as float64."""
+        if not 0 <= layer < self.L:
+            raise ValueError("layer out of range")
+        c_new, kr_new = np.asarray(c_new), np.asarray(kr_new)
+        if c_new.ndim != 3 or kr_new.ndim != 3 or c_new.shape[:2] != kr_new.shape[:2]:
+            raise ValueError("c_new [B, T, r] and kr_new [B, T, d_R] expected")
+        B, T, r = c_new.shape
+        if (B, r, kr_new.shape[2]) != (self.B, self.r, self.d_rope):
+            raise ValueError("shape mismatch")
+        if np.any(self.fill[layer] + T > self.max_len):
+            raise OverflowError("append would exceed max_len")
+        cq, kq = store_round(c_new, self.dtype), store_round(kr_new, self.dtype)
+        for b in range(B):
+            f = int(self.fill[layer, b])
+            self.c[layer, b, f:f + T] = cq[b]
+            self.kr[layer, b, f:f + T] = kq[b]
+        self.fill[layer] += T
+        return [self.stored_f64(layer, b, int(self.fill[layer, b])) for b in range(B)]
+
+    def nbytes(self) -> int:
+        """L * B * N_max * (r + d_R) * itemsize."""
+        return self.L * self.B * self.max_len * (self.r + self.d_rope) * ITEMSIZE[self.dtype]
+
+    def stored_f64(self, layer: int, b: int, n: int):
+        return (stored_to_f64(self.c[layer, b, :n], self.dtype), stored_to_f64(self.kr[layer, b, :n], self.dtype))
+
+
+def mla_cached_attention(cache: OracleLatentCache, layer: int, q_lat, q_rope, scale: float) -> np.ndarray:
+    """Multi-head latent attention over the latent cache, in the absorbed form of DeepSeek-V2 (§2.1):
+    head h's score for key j is (q_lat_h . c_j + q_rope_h . k^R_j) * scale, with q_lat_h the head's
+    no-RoPE query already multiplied by its key up-projection; query t of sequence b sees keys
+    j <= s_b + t; the output is the latent sum_j softmax_j c_j [B, H, T, r] (the value up-projection is
+    applied after). A query for a 16-bit cache is rounded to the cache dtype first.
+    """
+    q_lat, q_rope = np.asarray(q_lat), np.asarray(q_rope)
+    B, H, T, r = q_lat.shape
+    if q_rope.shape != (B, H, T, cache.d_rope) or B != cache.B or r != cache.r:
+        raise ValueError("query shapes do not match the cache")
+    ql, qr = query_as_f64(q_lat, cache.dtype), query_as_f64(q_rope, cache.dtype)
+    out = np.zeros((B, H, T, r), dtype=np.float64)
+    for b in range(B):
+        N = int(cache.fill[layer, b])
+        s = N - T
+        if s != int(cache.lens[b]):
+            raise RuntimeError("the layer must hold exactly the committed rows plus this chunk")
+        c, kr = cache.stored_f64(layer, b, N)
+        for h in range(H):
+            scores = (ql[b, h] @ c.T + qr[b, h] @ kr.T) * scale
+            scores = np.where(offset_causal_mask(T, s), scores, -np.inf)
+            out[b, h] = softmax_rows(scores) @ c
     return out
 
 

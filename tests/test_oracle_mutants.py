@@ -220,3 +220,16 @@ def test_fp8_scale_multiplied_instead_of_divided_is_caught(monkeypatch):
 
     monkeypatch.setattr(ko, "quantize_rows", multiplied)
     _fails(fp8_pins.test_fp8_cache_stores_codes_of_x_over_scale, ko.OracleKVCache)
+
+
+# ---- the latent cache and multi-head latent attention ------------------------------------------------
+from tests import test_oracle_latent as latent_pins
+
+
+def test_mla_without_the_rope_key_term_is_caught(monkeypatch):
+    """Scores from the latent alone, dropping q_rope . k^R."""
+    def mla_no_rope(cache, layer, q_lat, q_rope, scale):
+        return ko.mla_cached_attention(cache, layer, q_lat, np.zeros_like(np.asarray(q_rope)), scale)
+
+    monkeypatch.setattr(latent_pins, "mla_cached_attention", mla_no_rope)
+    _fails(latent_pins.test_absorbed_mla_equals_explicit_per_head_projections, 1, [7, 0, 12])
