@@ -126,6 +126,45 @@ int kvc_create_paged(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_l
  */
 int kvc_block_table(kvc_handle h, int32_t* table_host, int32_t* n_free_host);
 
+/*
+ * kvc_create_latent — a latent cache for multi-head latent attention (MLA): per layer and position one
+ * compressed latent c in R^r and one RoPE key k^R in R^{d_rope} shared by all heads, instead of per-head
+ * K and V.
+ * Defined by: "KV cache, incremental decode, ...", §2.6 "The latent cache" (the same rules as the KV cache
+ * — per-layer fill, committed length, rollback — on [B, T, r] and [B, T, d_R] chunks; nbytes is
+ * L B N_max (r + d_R) times the item size).
+ * Layout: the latent store [L, B, max_len, r] and the RoPE-key store [L, B, max_len, d_rope], in `dtype`
+ * (F32, F16 or BF16). c_store_dev and kr_store_dev: both NULL (the library allocates and zeroes them) or
+ * both caller-owned, 256-byte aligned and zeroed.
+ * The handle works with kvc_append (k_new_dev = the latent chunk [B, T, r], v_new_dev = the RoPE-key
+ * chunk [B, T, d_rope]; the RoPE key is stored as given), kvc_commit, kvc_truncate(_ragged),
+ * kvc_seq_len, kvc_positions, kvc_nbytes (= L B max_len (r + d_rope) itemsize), kvc_layer_ptrs (the
+ * layer's two stores), kvc_status and kvc_destroy, with their usual meaning and errors; it is read by
+ * mla_cached_attn. gqa_cached_attn* and kvc_set_rope reject it.
+ * Limits: r and d_rope multiples of 16, r <= 1024, d_rope <= 256, r + d_rope <= 1152 (the attention
+ * kernel's shared memory), B <= KVC_MAX_BATCH.
+ * Errors: KVC_E_INVAL, KVC_E_UNSUPPORTED (r or d_rope out of range), KVC_E_NOMEM.
+ */
+int kvc_create_latent(kvc_handle* out, int L, int B, int r, int d_rope, int max_len, kvc_dtype dtype,
+                      void* c_store_dev, void* kr_store_dev, void* stream);
+
+/*
+ * mla_cached_attn — multi-head latent attention of a chunk's T queries per head over every stored row of
+ * one layer of a latent cache, in the absorbed form (DeepSeek-V2, §2.1: the key up-projection is folded
+ * into the query, the value up-projection is applied to the output by the caller).
+ * For sequence b, head h and query t (absolute position s_b + t), over keys j <= s_b + t:
+ *   score_j = (q_lat[b,h,t] . c_j + q_rope[b,h,t] . k^R_j) * scale,   out[b,h,t] = sum_j softmax_j c_j.
+ * Defined by: "KV cache, incremental decode, ...", §2.6 (the latent cache MLA reads) and §2.3 (query t
+ * at absolute position s + t sees keys j <= s + t).
+ * q_lat_dev [B, H, T, r], q_rope_dev [B, H, T, d_rope], in `q_dtype` (F32, or the cache dtype; an F32
+ * query meets a 16-bit cache rounded to it). out_dev [B, H, T, r] float32, caller-owned. scale > 0 (the
+ * model's 1 / sqrt(per-head query-key width)). s as in gqa_cached_attn. Precondition: `layer` holds
+ * s_b + T rows (the chunk appended), else KVC_E_STATE. Split partials use the handle's workspace
+ * (grown with cudaMallocAsync when needed).
+ */
+int mla_cached_attn(kvc_handle h, const void* q_lat_dev, const void* q_rope_dev, kvc_dtype q_dtype, int layer,
+                    int s, int T, int H, float scale, float* out_dev, void* stream);
+
 /* kvc_destroy — synchronise the device, free everything the library allocated. NULL is a no-op. */
 int kvc_destroy(kvc_handle h);
 

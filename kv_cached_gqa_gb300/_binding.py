@@ -31,6 +31,9 @@ SIGNATURES = {
     "kvc_create_paged": (_c_int, [ctypes.POINTER(_vp), _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                   _c_int, _vp, _vp, _vp]),
     "kvc_block_table": (_c_int, [_vp, _i32p, _i32p]),
+    "kvc_create_latent": (_c_int, [ctypes.POINTER(_vp), _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp,
+                                   _vp]),
+    "mla_cached_attn": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.c_float, _vp, _vp]),
     "kvc_destroy": (_c_int, [_vp]),
     "kvc_append": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _vp]),
     "kvc_append_rope": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _vp]),
@@ -168,17 +171,65 @@ class PagedCache(Cache):
         self.h = h
 
 
+class LatentCache(Cache):
+    """A latent (MLA) cache over torch-allocated stores: latent c [L, B, max_len, r] (in .k) and RoPE key
+    k^R [L, B, max_len, d_rope] (in .v)."""
+
+    def __init__(self, L, B, r, d_rope, max_len, dtype, device="cuda", stream=None):
+        torch = _torch()
+        self.L, self.B, self.H_kv, self.max_len = L, B, 1, max_len
+        self.r, self.d_rope, self.d_h = r, d_rope, r
+        self.dtype = dtype if isinstance(dtype, int) else dtype_code(dtype)
+        self.k = torch.zeros((L, B, max_len, r), dtype=torch_dtype(self.dtype), device=device)
+        self.v = torch.zeros((L, B, max_len, d_rope), dtype=torch_dtype(self.dtype), device=device)
+        h = ctypes.c_void_p()
+        self.h = None
+        _check(load().kvc_create_latent(ctypes.byref(h), L, B, r, d_rope, max_len, self.dtype,
+                                        self.k.data_ptr(), self.v.data_ptr(), _stream(stream)))
+        self.h = h
+
+
+def kvc_create_latent(L, B, r, d_rope, max_len, dtype, stream=None) -> LatentCache:
+    return LatentCache(L, B, r, d_rope, max_len, dtype, stream=stream)
+
+
+def mla_cached_attn(c: LatentCache, q_lat, q_rope, layer: int, scale: float, s: int = KVC_COMMITTED, out=None,
+                    stream=None):
+    """q_lat [B, H, T, r], q_rope [B, H, T, d_rope] -> out [B, H, T, r] float32 (the attended latent)."""
+    torch = _torch()
+    if q_lat.dim() != 4 or q_lat.shape[0] != c.B or q_lat.shape[3] != c.r:
+        raise ValueError("q_lat must be [B, H, T, r]")
+    if tuple(q_rope.shape) != (q_lat.shape[0], q_lat.shape[1], q_lat.shape[2], c.d_rope) or q_rope.dtype != q_lat.dtype:
+        raise ValueError("q_rope must be [B, H, T, d_rope] of q_lat's dtype")
+    if out is None:
+        out = torch.empty(q_lat.shape, dtype=torch.float32, device=q_lat.device)
+    _check(load().mla_cached_attn(c.h, _ptr(q_lat), _ptr(q_rope), dtype_code(q_lat.dtype), layer, s,
+                                  int(q_lat.shape[2]), int(q_lat.shape[1]), float(scale), _ptr(out),
+                                  _stream(stream)), c.h)
+    return out
+
+
 def kvc_create(L, B, H_kv, d_h, max_len, dtype, stream=None) -> Cache:
     return Cache(L, B, H_kv, d_h, max_len, dtype, stream=stream)
 
 
 def kvc_append(c: Cache, layer: int, k_new, v_new, stream=None):
-    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype or k_new.dim() != 4:
-        raise ValueError("k_new and v_new must both be [B, H_kv, T, d_h] of one dtype")
-    if tuple(k_new.shape[:2]) != (c.B, c.H_kv) or k_new.shape[3] != c.d_h:
-        raise ValueError("k_new shape does not match the cache")
-    _check(load().kvc_append(c.h, layer, _ptr(k_new), _ptr(v_new), dtype_code(k_new.dtype),
-                             int(k_new.shape[2]), _stream(stream)), c.h)
+    """K/V cache: k_new, v_new [B, H_kv, T, d_h]. Latent cache: k_new = latent [B, T, r], v_new = RoPE key
+    [B, T, d_rope]."""
+    if isinstance(c, LatentCache):
+        if k_new.dim() != 3 or v_new.dim() != 3 or k_new.dtype != v_new.dtype or k_new.shape[:2] != v_new.shape[:2]:
+            raise ValueError("latent chunk [B, T, r] and RoPE-key chunk [B, T, d_rope] of one dtype expected")
+        if k_new.shape[0] != c.B or k_new.shape[2] != c.r or v_new.shape[2] != c.d_rope:
+            raise ValueError("chunk shapes do not match the latent cache")
+        T = int(k_new.shape[1])
+    else:
+        if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype or k_new.dim() != 4:
+            raise ValueError("k_new and v_new must both be [B, H_kv, T, d_h] of one dtype")
+        if tuple(k_new.shape[:2]) != (c.B, c.H_kv) or k_new.shape[3] != c.d_h:
+            raise ValueError("k_new shape does not match the cache")
+        T = int(k_new.shape[2])
+    _check(load().kvc_append(c.h, layer, _ptr(k_new), _ptr(v_new), dtype_code(k_new.dtype), T, _stream(stream)),
+           c.h)
 
 
 def kvc_create_paged(L, B, H_kv, d_h, max_len, block_size, n_blocks, dtype, stream=None) -> PagedCache:

@@ -109,13 +109,14 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   dev::pdl_trigger();
   constexpr int N = Pack<Tc>::N;
   constexpr bool kFp8 = std::is_same<Tc, dev::fp8>::value;
-  const int groups_per_row = a.D / N;
   const long long rows = static_cast<long long>(a.B) * a.H * a.T;
-  const long long per_tensor = rows * groups_per_row;
+  const long long per_k = rows * (a.D / N);             // groups of the first store (K, or the latent)
   const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (gid >= 2 * per_tensor) return;
-  const bool is_v = gid >= per_tensor;
-  const long long g = is_v ? gid - per_tensor : gid;
+  if (gid >= per_k + rows * (a.Dv / N)) return;
+  const bool is_v = gid >= per_k;
+  const int W = is_v ? a.Dv : a.D;                      // this store's row width
+  const int groups_per_row = W / N;
+  const long long g = is_v ? gid - per_k : gid;
   const long long row = g / groups_per_row;             // (b, h, t) row of the chunk
   const int grp = static_cast<int>(g % groups_per_row);
   const int t = static_cast<int>(row % a.T);
@@ -134,8 +135,8 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     dst_row = (((static_cast<long long>(a.layer) * a.pg.n_blocks + blk) * a.H + h) << a.pg.block_shift) +
               (pos & ((1 << a.pg.block_shift) - 1));
   }
-  Tc* dst = static_cast<Tc*>(is_v ? a.v_store : a.k_store) + dst_row * a.D + grp * N;
-  const long long src_off = row * a.D + grp * N;
+  Tc* dst = static_cast<Tc*>(is_v ? a.v_store : a.k_store) + dst_row * W + grp * N;
+  const long long src_off = row * W + grp * N;
   const void* src = is_v ? a.v_new : a.k_new;
   const bool rotate = !is_v && a.rope.table != nullptr;
   uint4 out;
@@ -220,7 +221,7 @@ __global__ void positions_kernel(const int32_t* lens, int B, int T, int32_t* out
 template <typename Tc, typename Tin>
 cudaError_t run_append(const AppendArgs& a, cudaStream_t st) {
   constexpr int N = Pack<Tc>::N;
-  const long long total = 2LL * a.B * a.H * a.T * (a.D / N);
+  const long long total = static_cast<long long>(a.B) * a.H * a.T * ((a.D + a.Dv) / N);
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   return launch_pdl(append_kernel<Tc, Tin>, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, a);

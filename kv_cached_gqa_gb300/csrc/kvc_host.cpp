@@ -86,6 +86,7 @@ int init_device_state(kvc_handle h, cudaStream_t st) {
     e = cudaMemsetAsync(h->d_table, 0xFF, tb, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync(block table)");
   }
+  if (h->latent) return KVC_OK;                    // the latent attention kernel reads without TMA maps
   int rows = 0;
   kvc::splitk_shape(h->dtype, h->D, 1, &rows, &h->split_tile_keys);
   std::string err;
@@ -140,7 +141,7 @@ int check_sizes(int L, int B, int H_kv, int d_h, int max_len, int dtype) {
 kvc_handle new_handle(int L, int B, int H_kv, int d_h, int max_len, kvc_dtype dtype) {
   kvc_handle h = new (std::nothrow) kvc_cache();
   if (!h) return nullptr;
-  h->L = L; h->B = B; h->H = H_kv; h->D = d_h; h->max_len = max_len; h->dtype = dtype;
+  h->L = L; h->B = B; h->H = H_kv; h->D = d_h; h->Dv = d_h; h->max_len = max_len; h->dtype = dtype;
   h->fill.assign(static_cast<size_t>(L) * B, 0);
   h->lens.assign(B, 0);
   h->k_scale.assign(L, 1.f);
@@ -148,10 +149,11 @@ kvc_handle new_handle(int L, int B, int H_kv, int d_h, int max_len, kvc_dtype dt
   return h;
 }
 
-// Bytes of one of the two stores (K or V): [L, B, H, max_len, D], or the pool [L, n_blocks, H, block, D].
-size_t store_bytes(kvc_handle h) {
+// Bytes of one store: [L, B, H, max_len, width], or the pool [L, n_blocks, H, block, width]; the first
+// store (K, or the latent) has width D, the second (V, or the RoPE key) width Dv.
+size_t store_bytes(kvc_handle h, bool second = false) {
   const size_t per_layer = h->paged ? static_cast<size_t>(h->n_blocks) * h->block : static_cast<size_t>(h->B) * h->max_len;
-  return static_cast<size_t>(h->L) * per_layer * h->H * h->D * kvc::itemsize(h->dtype);
+  return static_cast<size_t>(h->L) * per_layer * h->H * (second ? h->Dv : h->D) * kvc::itemsize(h->dtype);
 }
 
 // ---- paged pool bookkeeping ------------------------------------------------------------------------
@@ -214,6 +216,19 @@ int paged_grow(kvc_handle h, int layer, int T, cudaStream_t st) {
   for (const auto& ed : edits) h->table[ed.first] = ed.second;
   for (int b = 0; b < h->B; ++b)
     h->held[b] = std::max(h->held[b], blocks_for(h, static_cast<long long>(h->fill[static_cast<size_t>(layer) * h->B + b]) + T));
+  return KVC_OK;
+}
+
+// Grow the handle's split workspace (stream-ordered) to at least `need` floats.
+int ensure_workspace(kvc_handle h, size_t need, cudaStream_t st) {
+  if (need <= h->work_floats) return KVC_OK;
+  const size_t grow = need + need / 4;
+  float* p = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&p), grow * sizeof(float), st);
+  if (e != cudaSuccess) return fail(h, KVC_E_NOMEM, "workspace cudaMallocAsync: %s", cudaGetErrorString(e));
+  if (h->work) cudaFreeAsync(h->work, st);
+  h->work = p;
+  h->work_floats = grow;
   return KVC_OK;
 }
 
@@ -394,18 +409,18 @@ int kvc_create(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len, kv
   kvc_handle h = new_handle(L, B, H_kv, d_h, max_len, dtype);
   if (!h) return fail(nullptr, KVC_E_NOMEM, "host allocation failed");
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t bytes = store_bytes(h);
+  const size_t bytes = store_bytes(h), bytes2 = store_bytes(h, true);
   cudaError_t e = cudaMalloc(&h->k, bytes);
-  if (e == cudaSuccess) e = cudaMalloc(&h->v, bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->v, bytes2);
   h->owns_store = true;
   if (e != cudaSuccess) {
-    rc = fail(nullptr, KVC_E_NOMEM, "cudaMalloc of 2 x %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+    rc = fail(nullptr, KVC_E_NOMEM, "cudaMalloc of %zu + %zu bytes failed: %s", bytes, bytes2, cudaGetErrorString(e));
     cudaGetLastError();
     release(h);
     return rc;
   }
   e = cudaMemsetAsync(h->k, 0, bytes, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->v, 0, bytes, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->v, 0, bytes2, st);
   if (e != cudaSuccess) {
     rc = cuda_fail(nullptr, e, "cudaMemsetAsync(store)");
     release(h);
@@ -507,6 +522,149 @@ int kvc_block_table(kvc_handle h, int32_t* table_host, int32_t* n_free_host) {
   return KVC_OK;
 }
 
+int kvc_create_latent(kvc_handle* out, int L, int B, int r, int d_rope, int max_len, kvc_dtype dtype,
+                      void* c_store, void* kr_store, void* stream) {
+  if (!out) return fail(nullptr, KVC_E_INVAL, "null output handle");
+  *out = nullptr;
+  if (L < 1 || B < 1 || r < 1 || d_rope < 1 || max_len < 1)
+    return fail(nullptr, KVC_E_INVAL, "sizes must be positive (L=%d B=%d r=%d d_R=%d max_len=%d)", L, B, r, d_rope, max_len);
+  if (dtype != KVC_F32 && dtype != KVC_F16 && dtype != KVC_BF16)
+    return fail(nullptr, KVC_E_INVAL, "latent caches store F32, F16 or BF16 (dtype %d)", dtype);
+  if (B > KVC_MAX_BATCH) return fail(nullptr, KVC_E_INVAL, "B=%d exceeds KVC_MAX_BATCH", B);
+  if (r % 16 || d_rope % 16 || r > 1024 || d_rope > 256 || r + d_rope > 1152)
+    return fail(nullptr, KVC_E_UNSUPPORTED, "r=%d, d_R=%d: multiples of 16 with r <= 1024, d_R <= 256, r + d_R <= 1152",
+                r, d_rope);
+  if (static_cast<long long>(L) * B * max_len >= (1LL << 31) || max_len >= (1 << 30))
+    return fail(nullptr, KVC_E_INVAL, "cache too large");
+  if ((c_store == nullptr) != (kr_store == nullptr)) return fail(nullptr, KVC_E_INVAL, "pass both stores or neither");
+  if (c_store && (!aligned(c_store, 256) || !aligned(kr_store, 256)))
+    return fail(nullptr, KVC_E_INVAL, "store pointers must be 256-byte aligned");
+  kvc_handle h = new_handle(L, B, 1, r, max_len, dtype);
+  if (!h) return fail(nullptr, KVC_E_NOMEM, "host allocation failed");
+  h->Dv = d_rope;
+  h->latent = true;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = KVC_OK;
+  if (c_store) {
+    h->k = c_store;
+    h->v = kr_store;
+  } else {
+    const size_t b1 = store_bytes(h), b2 = store_bytes(h, true);
+    h->owns_store = true;
+    cudaError_t e = cudaMalloc(&h->k, b1);
+    if (e == cudaSuccess) e = cudaMalloc(&h->v, b2);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->k, 0, b1, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->v, 0, b2, st);
+    if (e != cudaSuccess) {
+      rc = fail(nullptr, KVC_E_NOMEM, "latent store allocation failed: %s", cudaGetErrorString(e));
+      cudaGetLastError();
+      release(h);
+      return rc;
+    }
+  }
+  rc = init_device_state(h, st);
+  if (rc) {
+    g_err = h->err;
+    release(h);
+    return rc;
+  }
+  *out = h;
+  return KVC_OK;
+}
+
+// Work plan of a latent attention call: units = (sequence, 16-row tile of the T * H query rows), each
+// cut into near-equal whole-tile key splits sized so the launch fills whole waves (two CTAs per SM),
+// longest first. Returns the workspace floats the partials need (0 when no unit splits).
+static int plan_mla(kvc_handle h, int T, int H, kvc::SplitPlan* plan, size_t* work_floats, std::string* err) {
+  const int R = T * H, rpt = kvc::kMlaRows;
+  const int n_rt = (R + rpt - 1) / rpt;
+  if (static_cast<long long>(h->B) * n_rt > kvc::kMaxUnits) {
+    *err = "batch x row tiles exceeds the planner's limit of 2048 units";
+    return KVC_E_UNSUPPORTED;
+  }
+  const int n_units = h->B * n_rt, tile = kvc::mla_tile_keys(h->dtype);
+  plan->n_units = n_units;
+  plan->rows_per_tile = rpt;
+  plan->n_rowtiles = n_rt;
+  std::vector<std::pair<int, int>>& order = h->plan_order;
+  std::vector<int>& nsplit = h->plan_nsplit;
+  order.resize(n_units);
+  nsplit.resize(n_units);
+  long long total = 0;
+  for (int b = 0; b < h->B; ++b)
+    for (int rt = 0; rt < n_rt; ++rt) total += h->lens[b] + std::min(T - 1, ((rt + 1) * rpt - 1) / H) + 1;
+  const long long slots = 2LL * h->num_sms;
+  const long long waves = std::max(1LL, (total + slots * 1024 - 1) / (slots * 1024));
+  const long long w = std::max<long long>(4LL * tile, (total + waves * slots - 1) / (waves * slots));
+  for (int b = 0; b < h->B; ++b)
+    for (int rt = 0; rt < n_rt; ++rt) {
+      const int u = b * n_rt + rt;
+      const int n = h->lens[b] + std::min(T - 1, ((rt + 1) * rpt - 1) / H) + 1;
+      int ns = static_cast<int>(std::max(1LL, (n + w / 2) / w));
+      const int chunk = kvc::split_chunk(n, ns, tile);
+      ns = (n + chunk - 1) / chunk;
+      nsplit[u] = ns;
+      order[u] = {chunk, u};
+    }
+  std::stable_sort(order.begin(), order.end(),
+                   [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; });
+  long long items = 0;
+  plan->prefix[0] = 0;
+  for (int i = 0; i < n_units; ++i) {
+    items += nsplit[order[i].second];
+    plan->prefix[i + 1] = static_cast<int32_t>(items);
+    plan->unit_b[i] = order[i].second;
+  }
+  plan->n_items = static_cast<int>(items);
+  plan->split_keys = n_units ? order[0].first : 0;
+  *work_floats = items > n_units ? static_cast<size_t>(items) * rpt * (h->D + 2) : 0;
+  return KVC_OK;
+}
+
+int mla_cached_attn(kvc_handle h, const void* q_lat, const void* q_rope, kvc_dtype q_dtype, int layer, int s,
+                    int T, int H, float scale, float* out, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (!h->latent) return fail(h, KVC_E_INVAL, "mla_cached_attn reads a latent cache (kvc_create_latent)");
+  if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
+  if (T < 1 || H < 1) return fail(h, KVC_E_INVAL, "T=%d and H=%d must be >= 1", T, H);
+  if (!q_lat || !q_rope || !out) return fail(h, KVC_E_INVAL, "null q_lat/q_rope/out");
+  if (!kvc::query_dtype_ok(h->dtype, q_dtype)) return fail(h, KVC_E_INVAL, "query dtype %d: F32 or the cache dtype", q_dtype);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(h, KVC_E_INVAL, "scale must be positive and finite");
+  if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(out, 16))
+    return fail(h, KVC_E_INVAL, "q_lat/q_rope/out must be 16-byte aligned");
+  if (s < KVC_COMMITTED) return fail(h, KVC_E_INVAL, "s=%d", s);
+  for (int b = 0; b < h->B; ++b) {
+    if (s >= 0 && h->lens[b] != s)
+      return fail(h, KVC_E_STATE, "s=%d but sequence %d has committed length %d", s, b, h->lens[b]);
+    if (h->fill[static_cast<size_t>(layer) * h->B + b] != h->lens[b] + T)
+      return fail(h, KVC_E_STATE, "layer %d holds %d rows of sequence %d; attention needs s_b + T = %d",
+                  layer, h->fill[static_cast<size_t>(layer) * h->B + b], b, h->lens[b] + T);
+  }
+  static thread_local kvc::SplitPlan plan;
+  size_t work_floats = 0;
+  std::string perr;
+  const int prc = plan_mla(h, T, H, &plan, &work_floats, &perr);
+  if (prc) return fail(h, prc, "%s", perr.c_str());
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (work_floats) {
+    const int wrc = ensure_workspace(h, work_floats, st);
+    if (wrc) return wrc;
+  }
+  kvc::MlaArgs a{};
+  a.q_lat = q_lat; a.q_rope = q_rope; a.q_dtype = q_dtype; a.out = out;
+  a.part_o = h->work;
+  a.part_ml = h->work ? h->work + static_cast<size_t>(plan.n_items) * kvc::kMlaRows * h->D : nullptr;
+  a.counters = h->d_counters;
+  a.lens = h->d_lens; a.status = h->d_status;
+  a.c_store = h->k; a.kr_store = h->v;
+  a.layer = layer; a.B = h->B; a.H = H; a.T = T; a.r = h->D; a.dR = h->Dv; a.max_len = h->max_len;
+  a.scale = scale; a.cache_dtype = h->dtype;
+  cudaError_t e = kvc::launch_mla(a, plan, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "latent attention launch");
+  h->launches += 1;
+  return KVC_OK;
+}
+
 int kvc_destroy(kvc_handle h) {
   release(h);
   return KVC_OK;
@@ -515,6 +673,7 @@ int kvc_destroy(kvc_handle h) {
 static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
                        int T, bool rope, void* stream) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (rope && h->latent) return fail(h, KVC_E_UNSUPPORTED, "fused RoPE is for K/V caches");
   if (rope && !h->d_rope) return fail(h, KVC_E_STATE, "no rotary table: call kvc_set_rope first");
   if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
   if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
@@ -537,7 +696,7 @@ static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v
   }
   kvc::AppendArgs a{};
   a.k_store = h->k; a.v_store = h->v; a.k_new = k_new; a.v_new = v_new; a.lens = h->d_lens;
-  a.layer = layer; a.B = h->B; a.H = h->H; a.D = h->D; a.T = T; a.max_len = h->max_len;
+  a.layer = layer; a.B = h->B; a.H = h->H; a.D = h->D; a.Dv = h->Dv; a.T = T; a.max_len = h->max_len;
   a.delta = delta; a.cache_dtype = h->dtype; a.in_dtype = in_dtype;
   a.pg = kvc_paging(h);
   if (rope) {
@@ -565,6 +724,7 @@ int kvc_append_rope(kvc_handle h, int layer, const void* k_new, const void* v_ne
 
 int kvc_set_rope(kvc_handle h, double base, kvc_rope_style style, void* stream) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (h->latent) return fail(h, KVC_E_UNSUPPORTED, "fused RoPE is for K/V caches");
   if (!(base > 1.0) || base > 1e12) return fail(h, KVC_E_INVAL, "RoPE base %g must be in (1, 1e12]", base);
   if (style != KVC_ROPE_HALF && style != KVC_ROPE_INTERLEAVED) return fail(h, KVC_E_INVAL, "RoPE style %d", style);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -676,20 +836,20 @@ int kvc_positions(kvc_handle h, int T, int32_t* out, void* stream) {
   return KVC_OK;
 }
 
-size_t kvc_nbytes(kvc_handle h) { return h ? 2 * store_bytes(h) : 0; }
+size_t kvc_nbytes(kvc_handle h) { return h ? store_bytes(h) + store_bytes(h, true) : 0; }
 
 int kvc_layer_ptrs(kvc_handle h, int layer, void** k, void** v) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
   if (layer < 0 || layer >= h->L || !k || !v) return fail(h, KVC_E_INVAL, "bad layer or null output");
-  const size_t off = store_bytes(h) / h->L * layer;
-  *k = static_cast<char*>(h->k) + off;
-  *v = static_cast<char*>(h->v) + off;
+  *k = static_cast<char*>(h->k) + store_bytes(h) / h->L * layer;
+  *v = static_cast<char*>(h->v) + store_bytes(h, true) / h->L * layer;
   return KVC_OK;
 }
 
 static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
                      float* out, bool rope, void* stream) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (h->latent) return fail(h, KVC_E_INVAL, "a latent cache is read by mla_cached_attn");
   if (rope && !h->d_rope) return fail(h, KVC_E_STATE, "no rotary table: call kvc_set_rope first");
   if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
   if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
@@ -717,16 +877,8 @@ static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, 
 
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (ap.workspace_floats) {
-    const size_t need = ap.workspace_floats;
-    if (need > h->work_floats) {
-      const size_t grow = need + need / 4;
-      float* p = nullptr;
-      cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&p), grow * sizeof(float), st);
-      if (e != cudaSuccess) return fail(h, KVC_E_NOMEM, "workspace cudaMallocAsync: %s", cudaGetErrorString(e));
-      if (h->work) cudaFreeAsync(h->work, st);
-      h->work = p;
-      h->work_floats = grow;
-    }
+    const int wrc = ensure_workspace(h, ap.workspace_floats, st);
+    if (wrc) return wrc;
   }
   kvc::AttnArgs a{};
   a.q = q; a.q_dtype = q_dtype; a.out = out;

@@ -76,6 +76,7 @@ struct AppendArgs {
   const void* v_new;
   const int32_t* lens;      // device committed lengths [B]
   int layer, B, H, D, T, max_len;
+  int Dv;                   // width of the second store's rows (= D, or d_R for a latent cache)
   int delta;                // this layer's fill minus the committed length (uniform over b)
   kvc_dtype cache_dtype, in_dtype;
   Paging pg;                // paged store: rows go through the block table
@@ -150,6 +151,29 @@ bool prefill_tc_shape(kvc_dtype dt, int D, int* rows_per_tile);
 cudaError_t launch_prefill_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
                               const CUtensorMap* tv, cudaStream_t st);
 
+// Multi-head latent attention over a latent cache (absorbed form): per query row (t, h), scores
+// (q_lat . c_j + q_rope . kR_j) * scale over keys j <= s_b + t, output sum_j softmax_j c_j.
+struct MlaArgs {
+  const void* q_lat;        // [B, H, T, r]
+  const void* q_rope;       // [B, H, T, dR]
+  kvc_dtype q_dtype;
+  float* out;               // [B, H, T, r]
+  float* part_o;            // [n_items, rows_per_tile, r] workspace
+  float* part_ml;           // [n_items, rows_per_tile, 2]
+  int* counters;            // [units] finished-split counters, zero between launches
+  const int32_t* lens;
+  int* status;
+  const void* c_store;      // [L, B, max_len, r]
+  const void* kr_store;     // [L, B, max_len, dR]
+  int layer, B, H, T, r, dR, max_len;
+  float scale;              // softmax scale (1 / sqrt of the per-head query-key width)
+  kvc_dtype cache_dtype;
+};
+constexpr int kMlaRows = 16;                 // query rows per CTA
+int mla_tile_keys(kvc_dtype dt);             // keys per shared-memory tile
+size_t mla_smem_bytes(kvc_dtype dt, int r, int dR);
+cudaError_t launch_mla(const MlaArgs& a, const SplitPlan& p, cudaStream_t st);
+
 // Which attention kernel serves a call, and its work plan (built from the host mirror of the lengths).
 enum class AttnKernel { SplitK, DecodeTC, PrefillTC };
 struct AttnPlan {
@@ -217,6 +241,10 @@ cudaError_t ensure_smem_limit(size_t bytes) {
 
 struct kvc_cache {
   int L = 0, B = 0, H = 0, D = 0, max_len = 0;
+  // latent (MLA) cache: H = 1, the first store holds the latent c (width D = r), the second the
+  // shared RoPE key k^R (width Dv = d_R); for a KV cache Dv = D
+  int Dv = 0;
+  bool latent = false;
   kvc_dtype dtype = KVC_F32;
   bool owns_store = false;
   // paged store: pool blocks, device table and its host mirror, and the free list

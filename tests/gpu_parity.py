@@ -8,8 +8,8 @@ from __future__ import annotations
 import numpy as np
 
 import kvc_synth
-from oracle.kvc_oracle import (OracleKVCache, OraclePagedKVCache, gqa_cached_attention, rope_chunk,
-                               set_fp8_scales, store_round, stored_to_f64)
+from oracle.kvc_oracle import (OracleKVCache, OracleLatentCache, OraclePagedKVCache, gqa_cached_attention,
+                               mla_cached_attention, rope_chunk, set_fp8_scales, store_round, stored_to_f64)
 
 DT = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
 QUERY_DT = {"f32": "f32", "f16": "f16", "bf16": "bf16", "e4m3": "f16"}   # the type a query is used in
@@ -192,6 +192,71 @@ class Mirror:
             table, n_free = self.kb.kvc_block_table(self.gpu)
             np.testing.assert_array_equal(np.array(table), self.ref.table)
             assert n_free == len(self.ref.free)
+
+    def close(self):
+        self.gpu.close()
+
+
+class LatentMirror:
+    """A GPU latent (MLA) cache and the oracle's, driven by the same calls."""
+
+    def __init__(self, L, B, r, d_rope, max_len, dtype, seed=0):
+        import torch
+        from kv_cached_gqa_gb300 import _binding as kb
+        self.torch, self.kb = torch, kb
+        self.L, self.B, self.r, self.dR, self.max_len, self.dtype, self.seed = L, B, r, d_rope, max_len, dtype, seed
+        self.gpu = kb.LatentCache(L, B, r, d_rope, max_len, DT[dtype])
+        self.ref = OracleLatentCache(L, B, r, d_rope, max_len, dtype)
+        self.n_draws = 0
+
+    def draw(self, shape):
+        self.n_draws += 1
+        return kvc_synth.normal_f32(shape, self.seed, 5000 + self.n_draws)
+
+    def dev(self, x, dtype=None):
+        t = self.torch.from_numpy(np.ascontiguousarray(x)).cuda()
+        return t if dtype is None else t.to(dtype)
+
+    def append(self, layer, T, in_dtype="f32"):
+        c, kr = self.draw((self.B, T, self.r)), self.draw((self.B, T, self.dR))
+
+        def given(x):
+            return x if in_dtype == "f32" else stored_to_f64(store_round(x, in_dtype), in_dtype).astype(np.float32)
+        self.ref.append(layer, given(c), given(kr))
+        tdt = None if in_dtype == "f32" else self.kb.torch_dtype(DT[in_dtype])
+        self.kb.kvc_append(self.gpu, layer, self.dev(c, tdt), self.dev(kr, tdt))
+
+    def attend(self, layer, H, T, scale, q_in="f32"):
+        ql, qr = self.draw((self.B, H, T, self.r)), self.draw((self.B, H, T, self.dR))
+        want = mla_cached_attention(self.ref, layer, ql, qr, scale)
+        tdt = None if q_in == "f32" else self.kb.torch_dtype(DT[q_in])
+        got = self.kb.mla_cached_attn(self.gpu, self.dev(ql, tdt), self.dev(qr, tdt), layer, scale).cpu().numpy()
+        return got, want
+
+    def commit(self):
+        self.ref.commit()
+        self.kb.kvc_commit(self.gpu)
+
+    def truncate(self, n):
+        self.ref.truncate(n)
+        self.kb.kvc_truncate_ragged(self.gpu, [int(x) for x in np.broadcast_to(n, (self.B,))])
+
+    def forward(self, T, H, scale, what=""):
+        for layer in range(self.L):
+            self.append(layer, T)
+            got, want = self.attend(layer, H, T, scale)
+            check_outputs(got, want, self.dtype, f"{what} layer {layer}")
+        self.commit()
+
+    def check_state(self):
+        torch = self.torch
+        view, npview = (torch.int32, np.int32) if self.dtype == "f32" else (torch.int16, np.int16)
+        np.testing.assert_array_equal(self.gpu.k.view(view).cpu().numpy(), self.ref.c.view(npview))
+        np.testing.assert_array_equal(self.gpu.v.view(view).cpu().numpy(), self.ref.kr.view(npview))
+        assert self.kb.kvc_seq_len(self.gpu, -1) == [int(x) for x in self.ref.committed()]
+        for layer in range(self.L):
+            assert self.kb.kvc_seq_len(self.gpu, layer) == [int(x) for x in self.ref.seq_len(layer)]
+        np.testing.assert_array_equal(self.kb.kvc_positions(self.gpu, 2).cpu().numpy(), self.ref.positions(2))
 
     def close(self):
         self.gpu.close()

@@ -34,7 +34,8 @@ def test_headers_declare_the_entry_points():
     names = declared_symbols()
     for n in ("kvc_create", "kvc_append", "kvc_commit", "kvc_truncate", "kvc_nbytes", "gqa_cached_attn",
               "kvc_truncate_ragged", "kvc_seq_len", "kvc_positions", "kvc_layer_ptrs", "kvc_status",
-              "kvc_create_paged", "kvc_block_table", "kvc_set_rope", "kvc_append_rope", "gqa_cached_attn_rope", "kvc_set_kv_scales"):
+              "kvc_create_paged", "kvc_block_table", "kvc_set_rope", "kvc_append_rope", "gqa_cached_attn_rope", "kvc_set_kv_scales",
+              "kvc_create_latent", "mla_cached_attn"):
         assert n in names
 
 
@@ -89,6 +90,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.kvc_block_table(None, None, None) == -1
     assert lib.kvc_set_rope(None, 10000.0, 0, None) == -1
     assert lib.kvc_set_kv_scales(None, None, None) == -1
+    assert lib.kvc_create_latent(ctypes.byref(h), 1, 1, 24, 64, 16, 2, None, None, None) == -6   # r % 16
+    assert lib.kvc_create_latent(ctypes.byref(h), 1, 1, 512, 64, 16, 3, None, None, None) == -1  # fp8
+    assert lib.kvc_create_latent(ctypes.byref(h), 1, 1, 512, 64, 16, 2, 256, None, None) == -1   # one store
+    assert lib.mla_cached_attn(None, None, None, 0, 0, -1, 1, 1, ctypes.c_float(1.0), None, None) == -1
     assert lib.kvc_create(ctypes.byref(h), 1, 1, 1, 32, 16, 3, None) == -6     # fp8 rows of 32 bytes
     assert lib.kvc_create(ctypes.byref(h), 1, 1, 1, 64, 16, 4, None) == -1     # unknown dtype
     assert lib.kvc_append_rope(None, 0, None, None, 0, 1, None) == -1
