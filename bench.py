@@ -164,6 +164,32 @@ def cpu_sample_child(arg):
 
     def rot(x, start):                 # the workload's rotary positions, if it has them
         return rope_chunk(x, [start], sp.rope_base, sp.rope_style) if sp.rope_base else x
+
+    if sp.mla:
+        from oracle.kvc_oracle import OracleLatentCache, mla_cached_attention
+        caches, queries = [], []
+        for b in range(cfg["n_seq"]):
+            s_b = int(sp.lengths[b])
+            c = OracleLatentCache(1, 1, sp.d_h, sp.d_rope, s_b + sp.T, sp.dtype)
+            if s_b:
+                c.append(0, *(x[None] for x in sp.host_prefill_latent(0, b, s_b)))
+                c.commit()
+            c.append(0, *(x[None] for x in sp.host_step_latent(0, 0, b)))
+            caches.append(c)
+            queries.append(tuple(x[None] for x in sp.host_queries_mla(0, 0, b, range(sp.H_q))))
+        t_end = time.perf_counter() + cfg["seconds"]
+        passes, elapsed, times = 0, 0.0, []
+        while time.perf_counter() < t_end or passes < cfg.get("min_passes", 1):
+            t0 = time.perf_counter()
+            for c, (ql, qr) in zip(caches, queries):
+                mla_cached_attention(c, 0, ql, qr, sp.mla_scale)
+            times.append(time.perf_counter() - t0)
+            elapsed += times[-1]
+            passes += 1
+        print(json.dumps({"bytes_per_pass": sp.attn_bytes(range(cfg["n_seq"])), "passes": passes, "seconds": elapsed,
+                          "pass_seconds": times, "n_seq": cfg["n_seq"], "layer_bytes": sp.attn_bytes(),
+                          "step_bytes": sp.step_bytes()}))
+        return
     seqs = list(range(cfg["n_seq"]))
     caches, queries = [], []
     for b in seqs:
@@ -257,8 +283,28 @@ def run_reference(args):
     return 0
 
 
+def attention_kernel_name(sp):
+    """The kernel that serves the workload's attention calls (the library's own choice, restated)."""
+    if sp.mla:
+        return "mla_cached_attn (mla_kernel: CUDA-core latent attention, split keys, fused merge)"
+    rows = sp.T * (sp.H_q // sp.H_kv)
+    tc_decode = rows <= 16 and ((sp.dtype in ("f16", "bf16") and sp.d_h in (64, 128)) or
+                                (sp.dtype == "e4m3" and sp.d_h == 128))
+    if tc_decode:
+        return "gqa_cached_attn (decode_tc_kernel: tcgen05 split-K attention with fused merge)"
+    if sp.dtype in ("f16", "bf16") and sp.d_h == 128:
+        return "gqa_cached_attn (prefill_tc_kernel: tcgen05 chunk attention)"
+    return "gqa_cached_attn (splitk_kernel: CUDA-core split-K attention)"
+
+
 def workload_config(sp, note=None):
     import numpy as np
+    if sp.mla:
+        c = {"workload": sp.name, "L": sp.L, "B": sp.B, "heads": sp.H_q, "r": sp.d_h, "d_rope": sp.d_rope,
+             "scale": sp.mla_scale, "T": sp.T, "cache_dtype": sp.dtype, "max_len": sp.max_len,
+             "s_b": {"min": int(np.min(sp.lengths)), "mean": float(np.mean(sp.lengths)), "max": int(np.max(sp.lengths))},
+             "l2": "no flush: the latent rows read per layer are larger than the 129 MB L2"}
+        return c
     c = {"workload": sp.name, "L": sp.L, "B": sp.B, "H_q": sp.H_q, "H_kv": sp.H_kv, "d_h": sp.d_h,
          "T": sp.T, "cache_dtype": sp.dtype, "max_len": sp.max_len,
          "s_b": {"min": int(np.min(sp.lengths)), "mean": float(np.mean(sp.lengths)),
@@ -301,11 +347,11 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
-        for layer, (q, k, v) in enumerate(inputs):
+        for layer, (*qs, k, v) in enumerate(inputs):
             wl.append(layer, k, v)
             if ev is not None:
                 ev[layer][0].record(stream)
-            wl.attend(q, layer, out=outs[layer])
+            wl.attend(qs, layer, out=outs[layer])
             if ev is not None:
                 ev[layer][1].record(stream)
         kb.kvc_commit(wl.cache)
@@ -389,9 +435,9 @@ def run_ours(args):
             for layer in range(sp.L):
                 for d_, h_ in zip(dev_in[layer], host_in[layer]):
                     d_.copy_(h_, non_blocking=True)
-                q, k, v = dev_in[layer]
+                *qs, k, v = dev_in[layer]
                 wl.append(layer, k, v)
-                wl.attend(q, layer, out=outs[layer])
+                wl.attend(qs, layer, out=outs[layer])
                 host_out[layer].copy_(outs[layer], non_blocking=True)
             kb.kvc_commit(wl.cache)
             kb.kvc_truncate_ragged(wl.cache, lengths)
@@ -440,7 +486,7 @@ def run_ours(args):
                          "note": "the same step captured once in a CUDA graph and replayed (no host launches)"},
         "pct_of_peak": {"measured_hbm": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / 8000.0, 2)},
-        "roofline": {"kernel": "gqa_cached_attn (decode_tc_kernel: tcgen05 split-K attention with fused merge)",
+        "roofline": {"kernel": attention_kernel_name(sp),
                      "bound": "hbm",
                      "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(attn_gbs / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",

@@ -106,6 +106,7 @@ STREAM_V_STEP = 5
 STREAM_LENGTHS = 6
 STREAM_WEIGHTS = 7
 STREAM_PROMPT = 8
+STREAM_Q_ROPE = 9           # the RoPE part of a latent-attention query
 
 
 def stream_id(base: int, layer: int = 0, step: int = 0) -> int:
@@ -137,6 +138,10 @@ WORKLOADS = {
     # the decode batch in an FP8 E4M3 cache (scale 1 for every layer): half the bytes per key
     "llama3-8b-decode-fp8": dict(L=32, B=64, H_q=32, H_kv=8, d_h=128, s_lo=512, s_hi=4096, T=1,
                                  dtype="e4m3", max_len=4160, seed=0),
+    # multi-head latent attention over a latent cache, DeepSeek-V2-Lite-shaped (27 layers, 16 heads,
+    # latent 512, RoPE key 64, softmax scale 1/sqrt(128 + 64)); the decode batch's lengths
+    "deepseek-v2-lite-mla-decode-bf16": dict(L=27, B=64, H=16, r=512, d_rope=64, s_lo=512, s_hi=4096, T=1,
+                                             dtype="bf16", max_len=4160, mla_scale=192 ** -0.5, seed=0),
     "llama3-8b-verify-fp16": dict(L=32, B=16, H_q=32, H_kv=8, d_h=128, s=2048, T=8, rollback=5,
                                   dtype="f16", max_len=2112, seed=0),
     "llama3-8b-prefill-fp16": dict(L=32, B=16, H_q=32, H_kv=8, d_h=128, s=1024, T=512,

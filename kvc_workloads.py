@@ -17,7 +17,8 @@ from dataclasses import dataclass
 import numpy as np
 
 import kvc_synth
-from kvc_synth import STREAM_K_PREFILL, STREAM_K_STEP, STREAM_Q, STREAM_V_PREFILL, STREAM_V_STEP, stream_id
+from kvc_synth import (STREAM_K_PREFILL, STREAM_K_STEP, STREAM_Q, STREAM_Q_ROPE, STREAM_V_PREFILL, STREAM_V_STEP,
+                       stream_id)
 
 DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
 ITEMSIZE = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
@@ -39,6 +40,12 @@ class WorkloadSpec:
     block: int = 0          # paged cache block (positions); 0 = contiguous cache
     rope_base: float = 0.0  # fused rotary positions (kvc_append_rope / gqa_cached_attn_rope); 0 = none
     rope_style: str = "half"
+    d_rope: int = 0         # latent (MLA) workload: RoPE-key width; then H_q = heads, H_kv = 1, d_h = r
+    mla_scale: float = 0.0
+
+    @property
+    def mla(self) -> bool:
+        return self.d_rope > 0
 
     @property
     def S0(self) -> int:
@@ -77,14 +84,20 @@ class WorkloadSpec:
     # -- accounting -----------------------------------------------------------------------------
     def attn_bytes(self, seqs=None) -> int:
         """Algorithmic HBM bytes of one attention call over sequences `seqs` (default all): each
-        stored K and V row read once per K/V head, the float32 queries read, float32 outputs written."""
+        stored K and V row read once per K/V head (latent: each latent and RoPE-key row once), the
+        float32 queries read, float32 outputs written."""
         lens = self.lengths if seqs is None else self.lengths[list(seqs)]
         n = len(lens)
+        if self.mla:
+            rows = (self.d_h + self.d_rope) * ITEMSIZE[self.dtype] * int((lens + self.T).sum())
+            return rows + n * self.H_q * self.T * 4 * (2 * self.d_h + self.d_rope)
         kv = 2 * self.H_kv * self.d_h * ITEMSIZE[self.dtype] * int((lens + self.T).sum())
         return kv + 2 * n * self.H_q * self.T * self.d_h * 4
 
     def append_bytes(self) -> int:
-        """Float32 chunk read plus rounded rows written, for K and V, one layer."""
+        """Float32 chunk read plus rounded rows written, for K and V (latent and RoPE key), one layer."""
+        if self.mla:
+            return self.B * self.T * (self.d_h + self.d_rope) * (4 + ITEMSIZE[self.dtype])
         n = self.B * self.H_kv * self.T * self.d_h
         return 2 * n * (4 + ITEMSIZE[self.dtype])
 
@@ -96,7 +109,37 @@ class WorkloadSpec:
         pairs = 0
         for s in self.lengths:
             pairs += self.T * int(s) + self.T * (self.T + 1) // 2
+        if self.mla:
+            return 2 * (2 * self.d_h + self.d_rope) * self.H_q * pairs
         return 4 * self.d_h * self.H_q * pairs
+
+    # -- latent (MLA) host redraws: latent [B, S0, r] / RoPE key [B, S0, d_R] per layer, step chunks
+    #    [B, T, r] / [B, T, d_R], queries [B, H, T, r] / [B, H, T, d_R] --------------------------------
+    def host_prefill_latent(self, layer, b, n):
+        c = kvc_synth.normal_f32_at(b * self.S0 * self.d_h + np.arange(n * self.d_h, dtype=np.int64), self.seed,
+                                    stream_id(STREAM_K_PREFILL, layer)).reshape(n, self.d_h)
+        kr = kvc_synth.normal_f32_at(b * self.S0 * self.d_rope + np.arange(n * self.d_rope, dtype=np.int64),
+                                     self.seed, stream_id(STREAM_V_PREFILL, layer)).reshape(n, self.d_rope)
+        return c, kr
+
+    def host_step_latent(self, layer, step, b):
+        T = self.T
+        c = kvc_synth.normal_f32_at(b * T * self.d_h + np.arange(T * self.d_h, dtype=np.int64), self.seed,
+                                    stream_id(STREAM_K_STEP, layer, step + 1)).reshape(T, self.d_h)
+        kr = kvc_synth.normal_f32_at(b * T * self.d_rope + np.arange(T * self.d_rope, dtype=np.int64), self.seed,
+                                     stream_id(STREAM_V_STEP, layer, step + 1)).reshape(T, self.d_rope)
+        return c, kr
+
+    def host_queries_mla(self, layer, step, b, heads):
+        ql, qr = [], []
+        for h in heads:
+            row = (b * self.H_q + h) * self.T
+            ql.append(kvc_synth.normal_f32_at(row * self.d_h + np.arange(self.T * self.d_h, dtype=np.int64),
+                                              self.seed, stream_id(STREAM_Q, layer, step + 1)))
+            qr.append(kvc_synth.normal_f32_at(row * self.d_rope + np.arange(self.T * self.d_rope, dtype=np.int64),
+                                              self.seed, stream_id(STREAM_Q_ROPE, layer, step + 1)))
+        return (np.stack(ql).reshape(len(heads), self.T, self.d_h),
+                np.stack(qr).reshape(len(heads), self.T, self.d_rope))
 
 
 def spec(name: str, seed: int = 0) -> WorkloadSpec:
@@ -105,6 +148,9 @@ def spec(name: str, seed: int = 0) -> WorkloadSpec:
         lengths = kvc_synth.ragged_lengths(w["B"], w["s_lo"], w["s_hi"], seed)
     else:
         lengths = np.full(w["B"], w["s"], dtype=np.int64)
+    if "r" in w:                        # latent (MLA) workload
+        return WorkloadSpec(name, w["L"], w["B"], w["H"], 1, w["r"], w["max_len"], w["dtype"], lengths, T=w["T"],
+                            seed=seed, d_rope=w["d_rope"], mla_scale=w["mla_scale"])
     return WorkloadSpec(name, w["L"], w["B"], w["H_q"], w["H_kv"], w["d_h"], w["max_len"], w["dtype"],
                         lengths, T=w["T"], seed=seed, block=w.get("block", 0),
                         rope_base=w.get("rope_base", 0.0), rope_style=w.get("rope_style", "half"))
@@ -117,7 +163,9 @@ class GpuWorkload:
         import torch
         from kv_cached_gqa_gb300 import _binding as kb
         self.torch, self.kb, self.spec, self.device = torch, kb, sp, device
-        if sp.block:
+        if sp.mla:
+            self.cache = kb.LatentCache(sp.L, sp.B, sp.d_h, sp.d_rope, sp.max_len, DTYPE_CODE[sp.dtype], device=device)
+        elif sp.block:
             n_blocks = sp.B * (-(-sp.max_len // sp.block))
             self.cache = kb.PagedCache(sp.L, sp.B, sp.H_kv, sp.d_h, sp.max_len, sp.block, n_blocks,
                                        DTYPE_CODE[sp.dtype], device=device)
@@ -130,10 +178,13 @@ class GpuWorkload:
         """The workload's append: kvc_append, or kvc_append_rope when it rotates keys."""
         (self.kb.kvc_append_rope if self.spec.rope_base else self.kb.kvc_append)(self.cache, layer, k, v)
 
-    def attend(self, q, layer, out=None):
-        """The workload's attention: gqa_cached_attn, or gqa_cached_attn_rope when it rotates queries."""
+    def attend(self, qs, layer, out=None):
+        """The workload's attention over its query tensors `qs`: gqa_cached_attn(_rope) of qs[0], or
+        mla_cached_attn of (q_lat, q_rope)."""
+        if self.spec.mla:
+            return self.kb.mla_cached_attn(self.cache, qs[0], qs[1], layer, self.spec.mla_scale, out=out)
         fn = self.kb.gqa_cached_attn_rope if self.spec.rope_base else self.kb.gqa_cached_attn
-        return fn(self.cache, q, layer, out=out)
+        return fn(self.cache, qs[0], layer, out=out)
 
     def __getattr__(self, name):                      # shape fields and host redraws of the spec
         return getattr(self.__dict__["spec"], name)
@@ -152,6 +203,12 @@ class GpuWorkload:
         shape = (sp.B, sp.H_kv, sp.S0, sp.d_h)
         chunk = sp.block or sp.S0
         for layer in range(sp.L):
+            if sp.mla:
+                c = self.draw((sp.B, sp.S0, sp.d_h), stream_id(STREAM_K_PREFILL, layer))
+                kr = self.draw((sp.B, sp.S0, sp.d_rope), stream_id(STREAM_V_PREFILL, layer))
+                self.append(layer, c, kr)
+                del c, kr
+                continue
             k = self.draw(shape, stream_id(STREAM_K_PREFILL, layer))
             v = self.draw(shape, stream_id(STREAM_V_PREFILL, layer))
             for c0 in range(0, sp.S0, chunk):
@@ -165,10 +222,17 @@ class GpuWorkload:
         kb.kvc_truncate_ragged(self.cache, [int(x) for x in sp.lengths])
 
     def step_inputs(self, step):
-        """(q, k_new, v_new) float32 device tensors of every layer for step `step`."""
+        """Float32 device tensors of every layer for step `step`: (q, k_new, v_new), or for a latent
+        workload (q_lat, q_rope, c_new, kr_new); the last two are what the append takes."""
         sp = self.spec
         out = []
         for layer in range(sp.L):
+            if sp.mla:
+                out.append((self.draw((sp.B, sp.H_q, sp.T, sp.d_h), stream_id(STREAM_Q, layer, step + 1)),
+                            self.draw((sp.B, sp.H_q, sp.T, sp.d_rope), stream_id(STREAM_Q_ROPE, layer, step + 1)),
+                            self.draw((sp.B, sp.T, sp.d_h), stream_id(STREAM_K_STEP, layer, step + 1)),
+                            self.draw((sp.B, sp.T, sp.d_rope), stream_id(STREAM_V_STEP, layer, step + 1))))
+                continue
             q = self.draw((sp.B, sp.H_q, sp.T, sp.d_h), stream_id(STREAM_Q, layer, step + 1))
             k = self.draw((sp.B, sp.H_kv, sp.T, sp.d_h), stream_id(STREAM_K_STEP, layer, step + 1))
             v = self.draw((sp.B, sp.H_kv, sp.T, sp.d_h), stream_id(STREAM_V_STEP, layer, step + 1))

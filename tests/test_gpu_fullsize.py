@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import kvc_workloads
-from oracle.kvc_oracle import OracleKVCache, gqa_cached_attention, rope_chunk
+from oracle.kvc_oracle import OracleKVCache, OracleLatentCache, gqa_cached_attention, mla_cached_attention, rope_chunk
 from tests.gpu_parity import check_outputs, check_rotated_store
 
 pytestmark = pytest.mark.gpu
@@ -20,9 +20,9 @@ def _run_and_sample(wl, samples):
     wl.prefill()
     inputs = wl.step_inputs(0)
     outs = []
-    for layer, (q, k, v) in enumerate(inputs):
+    for layer, (*qs, k, v) in enumerate(inputs):
         wl.append(layer, k, v)
-        outs.append(wl.attend(q, layer))
+        outs.append(wl.attend(qs, layer))
     kb.kvc_commit(wl.cache)
     kb.kvc_status(wl.cache)
     G = wl.H_q // wl.H_kv
@@ -107,3 +107,34 @@ def test_llama3_8b_decode_fp8_full_size():
     wl = kvc_workloads.GpuWorkload(kvc_workloads.spec("llama3-8b-decode-fp8"))
     lo, hi = int(np.argmin(wl.lengths)), int(np.argmax(wl.lengths))
     _run_and_sample(wl, [(0, lo, 0), (31, hi, 7), (20, 11, 2)])
+
+
+def test_deepseek_v2_lite_mla_decode_full_size():
+    """Latent attention over a latent cache, DeepSeek-V2-Lite-shaped: 27 layers, 16 heads, r = 512,
+    d_R = 64, the ragged 64-sequence decode batch; sampled (layer, sequence) pairs recomputed by the oracle
+    from host redraws, all 16 heads, and their stored latent and RoPE-key rows bit-exact."""
+    import torch
+    from kv_cached_gqa_gb300 import _binding as kb
+    wl = kvc_workloads.GpuWorkload(kvc_workloads.spec("deepseek-v2-lite-mla-decode-bf16"))
+    wl.prefill()
+    inputs = wl.step_inputs(0)
+    outs = []
+    for layer, (*qs, c, kr) in enumerate(inputs):
+        wl.append(layer, c, kr)
+        outs.append(wl.attend(qs, layer))
+    kb.kvc_commit(wl.cache)
+    kb.kvc_status(wl.cache)
+    lo, hi = int(np.argmin(wl.lengths)), int(np.argmax(wl.lengths))
+    for layer, b in [(0, lo), (26, hi), (13, 7)]:
+        s_b = int(wl.lengths[b])
+        ref = OracleLatentCache(1, 1, wl.d_h, wl.d_rope, s_b + wl.T, wl.dtype)
+        ref.append(0, *(x[None] for x in wl.host_prefill_latent(layer, b, s_b)))
+        ref.commit()
+        ref.append(0, *(x[None] for x in wl.host_step_latent(layer, 0, b)))
+        ql, qr = wl.host_queries_mla(layer, 0, b, range(wl.H_q))
+        want = mla_cached_attention(ref, 0, ql[None], qr[None], wl.mla_scale)
+        check_outputs(outs[layer][b:b + 1].cpu().numpy(), want, wl.dtype, f"mla layer {layer} b {b}")
+        for store, want_rows in ((wl.cache.k, ref.c[0, 0]), (wl.cache.v, ref.kr[0, 0])):
+            got = store[layer, b, :s_b + wl.T].contiguous().view(torch.int16).cpu().numpy()
+            np.testing.assert_array_equal(got, want_rows.view(np.int16))
+    wl.close()
