@@ -286,6 +286,8 @@ def run_reference(args):
 def attention_kernel_name(sp):
     """The kernel that serves the workload's attention calls (the library's own choice, restated)."""
     if sp.mla:
+        if sp.dtype in ("f16", "bf16") and sp.d_h in (256, 512) and sp.d_rope == 64:
+            return "mla_cached_attn (mla_tc_kernel: tcgen05 latent attention, online softmax, fused merge)"
         return "mla_cached_attn (mla_kernel: CUDA-core latent attention, split keys, fused merge)"
     rows = sp.T * (sp.H_q // sp.H_kv)
     tc_decode = rows <= 16 and ((sp.dtype in ("f16", "bf16") and sp.d_h in (64, 128)) or

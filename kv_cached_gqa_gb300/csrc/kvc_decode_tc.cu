@@ -192,14 +192,33 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int k_begin = split * chunk;
   const int k_end = min(k_begin + chunk, n_eff);
   const int nkt = (k_end - k_begin + kTK - 1) / kTK;
-  for (int i = tid; i < NR * kDh; i += kThreads) {
-    const int r = i / kDh, d = i % kDh;
-    float x = 0.f;
-    if (r < nrows) {
-      const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-      x = load_query_rot<Tc>(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh, d, s_b + t);
+  if (a.rope.table != nullptr) {                           // rotated queries: element by element
+    for (int i = tid; i < NR * kDh; i += kThreads) {
+      const int r = i / kDh, d = i % kDh;
+      float x = 0.f;
+      if (r < nrows) {
+        const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+        x = load_query_rot<Tc>(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh, d, s_b + t);
+      }
+      *reinterpret_cast<Tm*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tm>(x);
     }
-    *reinterpret_cast<Tm*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tm>(x);
+  } else {                                                  // four elements per load, all loads first
+    constexpr int kQuads = NR * kDh / 4, kIter = (kQuads + kThreads - 1) / kThreads;
+    uint4 x[kIter];
+#pragma unroll
+    for (int k = 0; k < kIter; ++k) {
+      const int i = tid + k * kThreads, r = (4 * i) / kDh, d = (4 * i) % kDh;
+      x[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < kQuads && r < nrows) {
+        const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+        x[k] = load_query4_raw<Tc>(a.q, a.q_dtype, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kIter; ++k) {
+      const int i = tid + k * kThreads, r = (4 * i) / kDh, d = (4 * i) % kDh;
+      if (i < kQuads) *reinterpret_cast<uint2*>(sm + Lo::kQOff + sw128(NR, r, d)) = query4_to<Tc, Tm>(x[k], a.q_dtype);
+    }
   }
   for (int i = tid; i < 2 * kPBufs * Lo::kPBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(p_base)[i] = make_uint4(0, 0, 0, 0);

@@ -281,5 +281,32 @@ __device__ __forceinline__ float load_query_rot(const AttnArgs& a, long long row
   return r;
 }
 
+// Four consecutive query elements (element index i, a multiple of 4), as raw bits: a float4 of an F32
+// query, or the low 8 bytes of a uint4 holding four elements of the query type. Nothing uses the value
+// here, so a thread can issue all of its loads before the first one returns.
+template <typename Tc>
+__device__ __forceinline__ uint4 load_query4_raw(const void* q, kvc_dtype qt, long long i) {
+  using Q = typename QueryOf<Tc>::T;
+  if (qt == KVC_F32) return *reinterpret_cast<const uint4*>(static_cast<const float*>(q) + i);
+  if constexpr (sizeof(Q) == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const Q*>(q) + i);
+    return make_uint4(w.x, w.y, 0u, 0u);
+  } else {
+    return *reinterpret_cast<const uint4*>(static_cast<const float*>(q) + i);
+  }
+}
+// Those four elements in the MMA operand type M (a 16-bit type): an F32 query rounded once to M, which
+// is its query-type rounding when M is the query type; a query already in the query type copied.
+template <typename Tc, typename M>
+__device__ __forceinline__ uint2 query4_to(uint4 raw, kvc_dtype qt) {
+  using Q = typename QueryOf<Tc>::T;
+  if (qt == KVC_F32 || sizeof(Q) != 2) {
+    M v[4] = {from_f32<M>(__uint_as_float(raw.x)), from_f32<M>(__uint_as_float(raw.y)),
+              from_f32<M>(__uint_as_float(raw.z)), from_f32<M>(__uint_as_float(raw.w))};
+    return *reinterpret_cast<const uint2*>(v);
+  }
+  return make_uint2(raw.x, raw.y);
+}
+
 }  // namespace dev
 }  // namespace kvc

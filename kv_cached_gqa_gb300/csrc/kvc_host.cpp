@@ -86,7 +86,17 @@ int init_device_state(kvc_handle h, cudaStream_t st) {
     e = cudaMemsetAsync(h->d_table, 0xFF, tb, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync(block table)");
   }
-  if (h->latent) return KVC_OK;                    // the latent attention kernel reads without TMA maps
+  if (h->latent) {                                 // maps for the tensor-core latent attention, 64 x 64 boxes
+    if (kvc::mla_tc_shape(h->dtype, h->D, h->Dv)) {
+      std::string err;
+      const long long planes = static_cast<long long>(h->L) * h->B;
+      if (!kvc::encode_store_map(&h->tmap_k_tc, h->k, h->dtype, h->D, h->max_len, planes, kvc::kMlaTcKeys, &err) ||
+          !kvc::encode_store_map(&h->tmap_v_tc, h->v, h->dtype, h->Dv, h->max_len, planes, kvc::kMlaTcKeys, &err))
+        return fail(h, KVC_E_CUDA, "%s", err.c_str());
+      h->has_tc = true;
+    }
+    return KVC_OK;
+  }
   int rows = 0;
   kvc::splitk_shape(h->dtype, h->D, 1, &rows, &h->split_tile_keys);
   std::string err;
@@ -575,14 +585,15 @@ int kvc_create_latent(kvc_handle* out, int L, int B, int r, int d_rope, int max_
 // Work plan of a latent attention call: units = (sequence, 16-row tile of the T * H query rows), each
 // cut into near-equal whole-tile key splits sized so the launch fills whole waves (two CTAs per SM),
 // longest first. Returns the workspace floats the partials need (0 when no unit splits).
-static int plan_mla(kvc_handle h, int T, int H, kvc::SplitPlan* plan, size_t* work_floats, std::string* err) {
+static int plan_mla(kvc_handle h, int T, int H, int tile, int ctas_per_sm, kvc::SplitPlan* plan,
+                    size_t* work_floats, std::string* err) {
   const int R = T * H, rpt = kvc::kMlaRows;
   const int n_rt = (R + rpt - 1) / rpt;
   if (static_cast<long long>(h->B) * n_rt > kvc::kMaxUnits) {
     *err = "batch x row tiles exceeds the planner's limit of 2048 units";
     return KVC_E_UNSUPPORTED;
   }
-  const int n_units = h->B * n_rt, tile = kvc::mla_tile_keys(h->dtype);
+  const int n_units = h->B * n_rt;
   plan->n_units = n_units;
   plan->rows_per_tile = rpt;
   plan->n_rowtiles = n_rt;
@@ -593,7 +604,7 @@ static int plan_mla(kvc_handle h, int T, int H, kvc::SplitPlan* plan, size_t* wo
   long long total = 0;
   for (int b = 0; b < h->B; ++b)
     for (int rt = 0; rt < n_rt; ++rt) total += h->lens[b] + std::min(T - 1, ((rt + 1) * rpt - 1) / H) + 1;
-  const long long slots = 2LL * h->num_sms;
+  const long long slots = static_cast<long long>(ctas_per_sm) * h->num_sms;
   const long long waves = std::max(1LL, (total + slots * 1024 - 1) / (slots * 1024));
   const long long w = std::max<long long>(4LL * tile, (total + waves * slots - 1) / (waves * slots));
   for (int b = 0; b < h->B; ++b)
@@ -643,7 +654,9 @@ int mla_cached_attn(kvc_handle h, const void* q_lat, const void* q_rope, kvc_dty
   static thread_local kvc::SplitPlan plan;
   size_t work_floats = 0;
   std::string perr;
-  const int prc = plan_mla(h, T, H, &plan, &work_floats, &perr);
+  const bool tc = h->has_tc && kvc::mla_tc_shape(h->dtype, h->D, h->Dv);
+  const int prc = tc ? plan_mla(h, T, H, kvc::kMlaTcKeys, 1, &plan, &work_floats, &perr)
+                     : plan_mla(h, T, H, kvc::mla_tile_keys(h->dtype), 2, &plan, &work_floats, &perr);
   if (prc) return fail(h, prc, "%s", perr.c_str());
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (work_floats) {
@@ -659,7 +672,7 @@ int mla_cached_attn(kvc_handle h, const void* q_lat, const void* q_rope, kvc_dty
   a.c_store = h->k; a.kr_store = h->v;
   a.layer = layer; a.B = h->B; a.H = H; a.T = T; a.r = h->D; a.dR = h->Dv; a.max_len = h->max_len;
   a.scale = scale; a.cache_dtype = h->dtype;
-  cudaError_t e = kvc::launch_mla(a, plan, st);
+  cudaError_t e = tc ? kvc::launch_mla_tc(a, plan, &h->tmap_k_tc, &h->tmap_v_tc, st) : kvc::launch_mla(a, plan, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "latent attention launch");
   h->launches += 1;
   return KVC_OK;

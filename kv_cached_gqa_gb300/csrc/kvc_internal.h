@@ -173,6 +173,11 @@ constexpr int kMlaRows = 16;                 // query rows per CTA
 int mla_tile_keys(kvc_dtype dt);             // keys per shared-memory tile
 size_t mla_smem_bytes(kvc_dtype dt, int r, int dR);
 cudaError_t launch_mla(const MlaArgs& a, const SplitPlan& p, cudaStream_t st);
+// Tensor-core latent attention: 16-bit caches, r = 256 or 512, d_R = 64 (64-key tiles, one CTA per SM).
+constexpr int kMlaTcKeys = 64;
+bool mla_tc_shape(kvc_dtype dt, int r, int dR);
+cudaError_t launch_mla_tc(const MlaArgs& a, const SplitPlan& p, const CUtensorMap* tc, const CUtensorMap* tr,
+                          cudaStream_t st);
 
 // Which attention kernel serves a call, and its work plan (built from the host mirror of the lengths).
 enum class AttnKernel { SplitK, DecodeTC, PrefillTC };

@@ -142,6 +142,9 @@ WORKLOADS = {
     # latent 512, RoPE key 64, softmax scale 1/sqrt(128 + 64)); the decode batch's lengths
     "deepseek-v2-lite-mla-decode-bf16": dict(L=27, B=64, H=16, r=512, d_rope=64, s_lo=512, s_hi=4096, T=1,
                                              dtype="bf16", max_len=4160, mla_scale=192 ** -0.5, seed=0),
+    # the same with DeepSeek-V3's 128 heads and 61 layers
+    "deepseek-v3-mla-decode-bf16": dict(L=61, B=64, H=128, r=512, d_rope=64, s_lo=512, s_hi=4096, T=1,
+                                        dtype="bf16", max_len=4160, mla_scale=192 ** -0.5, seed=0),
     "llama3-8b-verify-fp16": dict(L=32, B=16, H_q=32, H_kv=8, d_h=128, s=2048, T=8, rollback=5,
                                   dtype="f16", max_len=2112, seed=0),
     "llama3-8b-prefill-fp16": dict(L=32, B=16, H_q=32, H_kv=8, d_h=128, s=1024, T=512,

@@ -38,12 +38,15 @@ def test_latent_append_commit_truncate_bit_exact(dtype):
 
 MLA_CASES = [
     # dtype, r, d_R, H, T, lengths
+    # r in {256, 512} with d_R = 64 and a 16-bit cache run on tensor cores, the rest on CUDA cores
     ("bf16", 512, 64, 16, 1, [0, 1, 31, 32, 33, 700, 1500]),     # DeepSeek-V2-Lite-shaped decode
     ("bf16", 512, 64, 128, 1, [300, 5]),                         # 128 heads: 8 row tiles per sequence
     ("f16", 512, 64, 16, 4, [129, 0, 64]),                       # a chunk: diagonal masking
     ("f32", 128, 32, 8, 3, [100, 33]),
     ("bf16", 64, 16, 4, 17, [0, 40]),
     ("f16", 256, 32, 32, 1, [2000, 17, 999]),                    # several key splits per sequence
+    ("bf16", 256, 64, 8, 2, [100, 1000, 7, 3000]),               # tensor cores, r = 256
+    ("f16", 512, 64, 32, 1, [4000, 1, 2500]),                    # tensor cores, many splits and a merge
 ]
 
 
