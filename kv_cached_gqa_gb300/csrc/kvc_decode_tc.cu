@@ -183,6 +183,10 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     ctl->abort = 0;
     fence_mbar_init();
   }
+  // TMEM address and barriers visible to every warp
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   // from here on the lengths and the queries, which earlier kernels write, are read
   pdl_wait();
   pdl_trigger();
@@ -192,40 +196,6 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int k_begin = split * chunk;
   const int k_end = min(k_begin + chunk, n_eff);
   const int nkt = (k_end - k_begin + kTK - 1) / kTK;
-  if (a.rope.table != nullptr) {                           // rotated queries: element by element
-    for (int i = tid; i < NR * kDh; i += kThreads) {
-      const int r = i / kDh, d = i % kDh;
-      float x = 0.f;
-      if (r < nrows) {
-        const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-        x = load_query_rot<Tc>(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh, d, s_b + t);
-      }
-      *reinterpret_cast<Tm*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tm>(x);
-    }
-  } else {                                                  // four elements per load, all loads first
-    constexpr int kQuads = NR * kDh / 4, kIter = (kQuads + kThreads - 1) / kThreads;
-    uint4 x[kIter];
-#pragma unroll
-    for (int k = 0; k < kIter; ++k) {
-      const int i = tid + k * kThreads, r = (4 * i) / kDh, d = (4 * i) % kDh;
-      x[k] = make_uint4(0u, 0u, 0u, 0u);
-      if (i < kQuads && r < nrows) {
-        const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-        x[k] = load_query4_raw<Tc>(a.q, a.q_dtype, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kIter; ++k) {
-      const int i = tid + k * kThreads, r = (4 * i) / kDh, d = (4 * i) % kDh;
-      if (i < kQuads) *reinterpret_cast<uint2*>(sm + Lo::kQOff + sw128(NR, r, d)) = query4_to<Tc, Tm>(x[k], a.q_dtype);
-    }
-  }
-  for (int i = tid; i < 2 * kPBufs * Lo::kPBytes / 16; i += kThreads)
-    reinterpret_cast<uint4*>(p_base)[i] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   const uint32_t tmem = ctl->tmem;
   const uint32_t tmem_o = tmem + (kTmemCols - NR);
   volatile int* abort_flag = &ctl->abort;
@@ -257,270 +227,306 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     if (lane == 0)
       for (int i = max(0, issued - kStages); i < issued; ++i)
         mbar_drain(smem_u32(&ctl->full[i % kStages]), (i / kStages) & 1);
-  } else if (warp == 1) {
-    // ---------------------------------- MMA issuer ----------------------------------------------
-    if (lane == 0) {
-      const uint32_t idesc_s = umma_idesc(kTK, NR, kFmt, 0, 0);
-      const uint32_t idesc_o = umma_idesc(kDh, NR, kFmt, 1, 0);
-      bool ok = true;
-      for (int i = 0; i < nkt && ok; ++i) {                 // S^T_i = K_i . Q^T
-        const int st = i % kStages;
-        ok = kF8 ? mbar_wait(smem_u32(&ctl->k_conv[i & 1]), (i >> 1) & 1, abort_flag)
-                 : mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kt = kF8 ? s_conv + (i & 1) * kTileBytes : s_stage + st * kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < kDh / 16; ++ks)
-          umma_f16(tmem + i * NR,
-                   umma_desc(kt + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024, kSwizzle128),
-                   umma_desc(s_q + (ks >> 2) * (NR * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128),
-                   idesc_s, ks > 0);
-        if (!kF8) umma_commit(smem_u32(&ctl->empty[st]));
-        umma_commit(smem_u32(&ctl->s_ready[i]));          // fp8: also "the widened tile is free"
-      }
-      for (int i = 0; i < nkt && ok; ++i) {                 // O^T += V_i^T . P_i^T (hi, then lo)
-        const int ti = nkt + i, st = ti % kStages, pb = i % kPBufs;
-        // fp8: p_full also means V_i has been widened
-        ok = (kF8 || mbar_wait(smem_u32(&ctl->full[st]), (ti / kStages) & 1, abort_flag)) &&
-             mbar_wait(smem_u32(&ctl->p_full[pb]), (i / kPBufs) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t vt = kF8 ? s_conv + (ti & 1) * kTileBytes : s_stage + st * kTileBytes;
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t pt = s_p + (pb * 2 + part) * Lo::kPBytes;
-#pragma unroll
-          for (int ks = 0; ks < kTK / 16; ++ks)
-            umma_f16(tmem_o,
-                     umma_desc(vt + ks * 2048, kBoxBytes, 1024, kSwizzle128),
-                     umma_desc(pt + (ks >> 2) * (NR * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128),
-                     idesc_o, (i | part | ks) != 0);
-        }
-        if (!kF8) umma_commit(smem_u32(&ctl->empty[st]));
-        umma_commit(smem_u32(&ctl->p_empty[pb]));          // fp8: also "the widened tile is free"
-      }
-      if (ok) umma_commit(smem_u32(&ctl->o_full));
-      umma_commit(smem_u32(&ctl->done));
-      mbar_drain(smem_u32(&ctl->done), 0);                  // every MMA done before TMEM is freed
-    }
   } else {
-    // ---------------------------------- softmax and epilogue ------------------------------------
-    const int quad = warp & 3;                              // this warp's TMEM lane quadrant
-    const int kslot = quad * 32 + lane;                     // key within a tile; d in the epilogue
-    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const int w4 = warp - 2;
-    const float scale = kLog2e * rsqrtf(static_cast<float>(kDh)) * a.k_scale;   // k_scale: fp8 codes -> keys
-    int trow[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) trow[r] = (r < nrows) ? s_b + (row0 + r) / a.G : -1;   // last visible key
-
-    // pass 1, overlapped with the K stream: fold each score tile into the row maxima as soon as
-    // its MMAs complete
-    bool ok = true;
-    // fp8: widen ring tile `ti` (K tiles 0 .. nkt-1, then V tiles) into float16 buffer ti % 2, release
-    // the ring stage and, for a K tile, tell the MMA warp
-    auto widen = [&](int ti) -> bool {
-      const int st = ti % kStages;
-      if (!mbar_wait(smem_u32(&ctl->full[st]), (ti / kStages) & 1, abort_flag)) return false;
-      widen_fp8_row(sm + Lo::kStageOff + st * Lo::kStageBytes, sm + Lo::kConvOff + (ti & 1) * kTileBytes, kslot);
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&ctl->empty[st]));
-        if (ti < nkt) mbar_arrive(smem_u32(&ctl->k_conv[ti & 1]));
-      }
-      return true;
-    };
-    if constexpr (kF8) {                                    // two K tiles ahead of the MMAs
-      ok = widen(0);
-      if (ok && nkt > 1) ok = widen(1);
-    }
-    float m_run[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) m_run[r] = -INFINITY;
-    for (int i = 0; i < nkt && ok; ++i) {
-      ok = mbar_wait(smem_u32(&ctl->s_ready[i]), 0, abort_flag);
-      if (!ok) break;
-      // fp8: QK_i has read buffer i % 2, so K_{i+2} takes its place while QK_{i+1} runs
-      if constexpr (kF8) {
-        if (i + 2 < nkt && !(ok = widen(i + 2))) break;
-      }
-      tc_fence_after();
-      float v[NR];
-#pragma unroll
-      for (int c = 0; c < NR; c += 16) tmem_ld16(tmem + lane_base + i * NR + c, v + c);
-      const int kabs = k_begin + i * kTK + kslot;
-#pragma unroll
-      for (int r = 0; r < NR; ++r)
-        if (kabs < k_end && kabs <= trow[r]) m_run[r] = fmaxf(m_run[r], v[r] * scale);
-    }
-    // row maxima over the split's keys: warp shuffles, then across the four warps
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m_run[r] = fmaxf(m_run[r], __shfl_xor_sync(0xffffffffu, m_run[r], o));
-      if (lane == 0) ctl->red[w4][r] = m_run[r];
-    }
-    named_sync(1, kSoftmaxThreads);
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-      m_run[r] = fmaxf(fmaxf(ctl->red[0][r], ctl->red[1][r]), fmaxf(ctl->red[2][r], ctl->red[3][r]));
-    named_sync(1, kSoftmaxThreads);
-
-    float l_run[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) l_run[r] = 0.f;
-    // fp8: every QK is done (all S tiles were read above), so both buffers are free for V_0 and V_1
-    if constexpr (kF8) {
-      if (ok) ok = widen(nkt);
-      if (ok && nkt > 1) ok = widen(nkt + 1);
-    }
-    for (int i = 0; i < nkt && ok; ++i) {
-      const int pb = i % kPBufs;
-      ok = mbar_wait(smem_u32(&ctl->p_empty[pb]), ((i / kPBufs) & 1) ^ 1, abort_flag);
-      if (!ok) break;
-      float v[NR];
-#pragma unroll
-      for (int c = 0; c < NR; c += 16) tmem_ld16(tmem + lane_base + i * NR + c, v + c);
-      const int kabs = k_begin + i * kTK + kslot;
-      unsigned char* ph = p_base + (pb * 2) * Lo::kPBytes;
-      unsigned char* pl = ph + Lo::kPBytes;
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        if (r < nrows) {
-          const float p = (kabs < k_end && kabs <= trow[r]) ? exp2f(v[r] * scale - m_run[r]) : 0.f;
-          l_run[r] += p;
-          const Tm h16 = from_f32<Tm>(p);
-          const Tm l16 = from_f32<Tm>(p - to_f32<Tm>(h16));
-          const uint32_t off = sw128(NR, r, kslot);
-          *reinterpret_cast<Tm*>(ph + off) = h16;
-          *reinterpret_cast<Tm*>(pl + off) = l16;
-        }
-      }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[pb]));
-      // fp8: PV_{i-1} is done (p_empty above), so V_{i+1} takes V_{i-1}'s buffer while PV_i runs
-      if constexpr (kF8) {
-        if (i >= 1 && i + 1 < nkt && !(ok = widen(nkt + i + 1))) break;
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], o);
-      if (lane == 0) ctl->red[w4][r] = l_run[r];
-    }
-    named_sync(1, kSoftmaxThreads);
-    if (tid == 64) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        ctl->m[r] = m_run[r];
-        ctl->l[r] = ctl->red[0][r] + ctl->red[1][r] + ctl->red[2][r] + ctl->red[3][r];
-      }
-    }
-    named_sync(1, kSoftmaxThreads);
-
-    // ---- epilogue: thread = d; O^T row d from TMEM -----------------------------------------------
-    ok = ok && mbar_wait(smem_u32(&ctl->o_full), 0, abort_flag);
-    tc_fence_after();
-    float o[NR];
-#pragma unroll
-    for (int c = 0; c < NR; c += 16) tmem_ld16(tmem_o + lane_base + c, o + c);
-    const bool aborted = *abort_flag != 0;
-    // O^T row d sits in TMEM lane d for M = 128; for M = 64 in lane 32 * (d / 16) + d % 16, i.e. the
-    // lower 16 lanes of each warp's quadrant
-    const bool d_ok = DH == 128 || lane < 16;
-    const int d = DH == 128 ? kslot : quad * 16 + (lane & 15);
-    const long long item_row0 = static_cast<long long>(item) * NR;
-    if (!aborted && d_ok) {
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
+    // ---- warps 1-5, while warp 0 already streams: Q^T and zeroed P^T ----------------------------
+    if (a.rope.table != nullptr) {                           // rotated queries: element by element
+      for (int i = tid - 32; i < NR * kDh; i += kThreads - 32) {
+        const int r = i / kDh, d = i % kDh;
+        float x = 0.f;
         if (r < nrows) {
           const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-          if (nsplit == 1) {
-            a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = o[r] / ctl->l[r] * a.v_scale;
-          } else {
-            a.part_o[(item_row0 + r) * kDh + d] = o[r];
-            if (d == 0) {
-              a.part_ml[(item_row0 + r) * 2] = ctl->m[r];
-              a.part_ml[(item_row0 + r) * 2 + 1] = ctl->l[r];
+          x = load_query_rot<Tc>(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh, d, s_b + t);
+        }
+        *reinterpret_cast<Tm*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tm>(x);
+      }
+    } else {                                                  // four elements per load, all loads first
+      constexpr int kStagers = kThreads - 32, kQuads = NR * kDh / 4, kIter = (kQuads + kStagers - 1) / kStagers;
+      uint4 x[kIter];
+#pragma unroll
+      for (int k = 0; k < kIter; ++k) {
+        const int i = (tid - 32) + k * kStagers, r = (4 * i) / kDh, d = (4 * i) % kDh;
+        x[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < kQuads && r < nrows) {
+          const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+          x[k] = load_query4_raw<Tc>(a.q, a.q_dtype, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kIter; ++k) {
+        const int i = (tid - 32) + k * kStagers, r = (4 * i) / kDh, d = (4 * i) % kDh;
+        if (i < kQuads) *reinterpret_cast<uint2*>(sm + Lo::kQOff + sw128(NR, r, d)) = query4_to<Tc, Tm>(x[k], a.q_dtype);
+      }
+    }
+    for (int i = tid - 32; i < 2 * kPBufs * Lo::kPBytes / 16; i += kThreads - 32)
+      reinterpret_cast<uint4*>(p_base)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async();
+    named_sync(2, kThreads - 32);                             // Q^T and P^T ready for the MMA warp
+    if (warp == 1) {
+      // ---------------------------------- MMA issuer ----------------------------------------------
+      if (lane == 0) {
+        const uint32_t idesc_s = umma_idesc(kTK, NR, kFmt, 0, 0);
+        const uint32_t idesc_o = umma_idesc(kDh, NR, kFmt, 1, 0);
+        bool ok = true;
+        for (int i = 0; i < nkt && ok; ++i) {                 // S^T_i = K_i . Q^T
+          const int st = i % kStages;
+          ok = kF8 ? mbar_wait(smem_u32(&ctl->k_conv[i & 1]), (i >> 1) & 1, abort_flag)
+                   : mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kt = kF8 ? s_conv + (i & 1) * kTileBytes : s_stage + st * kTileBytes;
+  #pragma unroll
+          for (int ks = 0; ks < kDh / 16; ++ks)
+            umma_f16(tmem + i * NR,
+                     umma_desc(kt + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024, kSwizzle128),
+                     umma_desc(s_q + (ks >> 2) * (NR * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128),
+                     idesc_s, ks > 0);
+          if (!kF8) umma_commit(smem_u32(&ctl->empty[st]));
+          umma_commit(smem_u32(&ctl->s_ready[i]));          // fp8: also "the widened tile is free"
+        }
+        for (int i = 0; i < nkt && ok; ++i) {                 // O^T += V_i^T . P_i^T (hi, then lo)
+          const int ti = nkt + i, st = ti % kStages, pb = i % kPBufs;
+          // fp8: p_full also means V_i has been widened
+          ok = (kF8 || mbar_wait(smem_u32(&ctl->full[st]), (ti / kStages) & 1, abort_flag)) &&
+               mbar_wait(smem_u32(&ctl->p_full[pb]), (i / kPBufs) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vt = kF8 ? s_conv + (ti & 1) * kTileBytes : s_stage + st * kTileBytes;
+  #pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t pt = s_p + (pb * 2 + part) * Lo::kPBytes;
+  #pragma unroll
+            for (int ks = 0; ks < kTK / 16; ++ks)
+              umma_f16(tmem_o,
+                       umma_desc(vt + ks * 2048, kBoxBytes, 1024, kSwizzle128),
+                       umma_desc(pt + (ks >> 2) * (NR * 128) + (ks & 3) * 32, 16, 1024, kSwizzle128),
+                       idesc_o, (i | part | ks) != 0);
+          }
+          if (!kF8) umma_commit(smem_u32(&ctl->empty[st]));
+          umma_commit(smem_u32(&ctl->p_empty[pb]));          // fp8: also "the widened tile is free"
+        }
+        if (ok) umma_commit(smem_u32(&ctl->o_full));
+        umma_commit(smem_u32(&ctl->done));
+        mbar_drain(smem_u32(&ctl->done), 0);                  // every MMA done before TMEM is freed
+      }
+    } else {
+      // ---------------------------------- softmax and epilogue ------------------------------------
+      const int quad = warp & 3;                              // this warp's TMEM lane quadrant
+      const int kslot = quad * 32 + lane;                     // key within a tile; d in the epilogue
+      const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+      const int w4 = warp - 2;
+      const float scale = kLog2e * rsqrtf(static_cast<float>(kDh)) * a.k_scale;   // k_scale: fp8 codes -> keys
+      int trow[NR];
+  #pragma unroll
+      for (int r = 0; r < NR; ++r) trow[r] = (r < nrows) ? s_b + (row0 + r) / a.G : -1;   // last visible key
+
+      // pass 1, overlapped with the K stream: fold each score tile into the row maxima as soon as
+      // its MMAs complete
+      bool ok = true;
+      // fp8: widen ring tile `ti` (K tiles 0 .. nkt-1, then V tiles) into float16 buffer ti % 2, release
+      // the ring stage and, for a K tile, tell the MMA warp
+      auto widen = [&](int ti) -> bool {
+        const int st = ti % kStages;
+        if (!mbar_wait(smem_u32(&ctl->full[st]), (ti / kStages) & 1, abort_flag)) return false;
+        widen_fp8_row(sm + Lo::kStageOff + st * Lo::kStageBytes, sm + Lo::kConvOff + (ti & 1) * kTileBytes, kslot);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&ctl->empty[st]));
+          if (ti < nkt) mbar_arrive(smem_u32(&ctl->k_conv[ti & 1]));
+        }
+        return true;
+      };
+      if constexpr (kF8) {                                    // two K tiles ahead of the MMAs
+        ok = widen(0);
+        if (ok && nkt > 1) ok = widen(1);
+      }
+      float m_run[NR];
+  #pragma unroll
+      for (int r = 0; r < NR; ++r) m_run[r] = -INFINITY;
+      for (int i = 0; i < nkt && ok; ++i) {
+        ok = mbar_wait(smem_u32(&ctl->s_ready[i]), 0, abort_flag);
+        if (!ok) break;
+        // fp8: QK_i has read buffer i % 2, so K_{i+2} takes its place while QK_{i+1} runs
+        if constexpr (kF8) {
+          if (i + 2 < nkt && !(ok = widen(i + 2))) break;
+        }
+        tc_fence_after();
+        float v[NR];
+  #pragma unroll
+        for (int c = 0; c < NR; c += 16) tmem_ld16(tmem + lane_base + i * NR + c, v + c);
+        const int kabs = k_begin + i * kTK + kslot;
+  #pragma unroll
+        for (int r = 0; r < NR; ++r)
+          if (kabs < k_end && kabs <= trow[r]) m_run[r] = fmaxf(m_run[r], v[r] * scale);
+      }
+      // row maxima over the split's keys: warp shuffles, then across the four warps
+  #pragma unroll
+      for (int r = 0; r < NR; ++r) {
+  #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m_run[r] = fmaxf(m_run[r], __shfl_xor_sync(0xffffffffu, m_run[r], o));
+        if (lane == 0) ctl->red[w4][r] = m_run[r];
+      }
+      named_sync(1, kSoftmaxThreads);
+  #pragma unroll
+      for (int r = 0; r < NR; ++r)
+        m_run[r] = fmaxf(fmaxf(ctl->red[0][r], ctl->red[1][r]), fmaxf(ctl->red[2][r], ctl->red[3][r]));
+      named_sync(1, kSoftmaxThreads);
+
+      float l_run[NR];
+  #pragma unroll
+      for (int r = 0; r < NR; ++r) l_run[r] = 0.f;
+      // fp8: every QK is done (all S tiles were read above), so both buffers are free for V_0 and V_1
+      if constexpr (kF8) {
+        if (ok) ok = widen(nkt);
+        if (ok && nkt > 1) ok = widen(nkt + 1);
+      }
+      for (int i = 0; i < nkt && ok; ++i) {
+        const int pb = i % kPBufs;
+        ok = mbar_wait(smem_u32(&ctl->p_empty[pb]), ((i / kPBufs) & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        float v[NR];
+  #pragma unroll
+        for (int c = 0; c < NR; c += 16) tmem_ld16(tmem + lane_base + i * NR + c, v + c);
+        const int kabs = k_begin + i * kTK + kslot;
+        unsigned char* ph = p_base + (pb * 2) * Lo::kPBytes;
+        unsigned char* pl = ph + Lo::kPBytes;
+  #pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          if (r < nrows) {
+            const float p = (kabs < k_end && kabs <= trow[r]) ? exp2f(v[r] * scale - m_run[r]) : 0.f;
+            l_run[r] += p;
+            const Tm h16 = from_f32<Tm>(p);
+            const Tm l16 = from_f32<Tm>(p - to_f32<Tm>(h16));
+            const uint32_t off = sw128(NR, r, kslot);
+            *reinterpret_cast<Tm*>(ph + off) = h16;
+            *reinterpret_cast<Tm*>(pl + off) = l16;
+          }
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[pb]));
+        // fp8: PV_{i-1} is done (p_empty above), so V_{i+1} takes V_{i-1}'s buffer while PV_i runs
+        if constexpr (kF8) {
+          if (i >= 1 && i + 1 < nkt && !(ok = widen(nkt + i + 1))) break;
+        }
+      }
+  #pragma unroll
+      for (int r = 0; r < NR; ++r) {
+  #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], o);
+        if (lane == 0) ctl->red[w4][r] = l_run[r];
+      }
+      named_sync(1, kSoftmaxThreads);
+      if (tid == 64) {
+  #pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          ctl->m[r] = m_run[r];
+          ctl->l[r] = ctl->red[0][r] + ctl->red[1][r] + ctl->red[2][r] + ctl->red[3][r];
+        }
+      }
+      named_sync(1, kSoftmaxThreads);
+
+      // ---- epilogue: thread = d; O^T row d from TMEM -----------------------------------------------
+      ok = ok && mbar_wait(smem_u32(&ctl->o_full), 0, abort_flag);
+      tc_fence_after();
+      float o[NR];
+  #pragma unroll
+      for (int c = 0; c < NR; c += 16) tmem_ld16(tmem_o + lane_base + c, o + c);
+      const bool aborted = *abort_flag != 0;
+      // O^T row d sits in TMEM lane d for M = 128; for M = 64 in lane 32 * (d / 16) + d % 16, i.e. the
+      // lower 16 lanes of each warp's quadrant
+      const bool d_ok = DH == 128 || lane < 16;
+      const int d = DH == 128 ? kslot : quad * 16 + (lane & 15);
+      const long long item_row0 = static_cast<long long>(item) * NR;
+      if (!aborted && d_ok) {
+  #pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          if (r < nrows) {
+            const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+            if (nsplit == 1) {
+              a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = o[r] / ctl->l[r] * a.v_scale;
+            } else {
+              a.part_o[(item_row0 + r) * kDh + d] = o[r];
+              if (d == 0) {
+                a.part_ml[(item_row0 + r) * 2] = ctl->m[r];
+                a.part_ml[(item_row0 + r) * 2 + 1] = ctl->l[r];
+              }
             }
           }
         }
+      } else if (tid == 64) {
+        atomicExch(a.status, kStatusTimeout);
       }
-    } else if (tid == 64) {
-      atomicExch(a.status, kStatusTimeout);
-    }
-    if (nsplit > 1) {
-      // ---- the CTA that finishes a unit's last split merges its partials -----------------------
-      __threadfence();
-      named_sync(1, kSoftmaxThreads);
-      int* counter = a.counters + unit * a.H_kv + kvh;
-      if (tid == 64) ctl->last = (atomicAdd(counter, 1) == nsplit - 1);
-      named_sync(1, kSoftmaxThreads);
-      if (ctl->last) {
+      if (nsplit > 1) {
+        // ---- the CTA that finishes a unit's last split merges its partials -----------------------
         __threadfence();
-        const long long first_row = static_cast<long long>(plan.prefix[unit] + kvh * nsplit) * NR;
-        if (nsplit <= kMergeSplits) {
-          // every split's (m, l) at once into the P buffer (free now), then one set of weights per
-          // row, then independent loads of the partial outputs
-          float* wm = reinterpret_cast<float*>(p_base);            // [NR][kMergeSplits] m, then weight
-          float* wl = wm + NR * kMergeSplits;                      // [NR][kMergeSplits] l
-          float* linv = wl + NR * kMergeSplits;                    // [NR]
-          for (int i = tid - 64; i < nrows * nsplit; i += kSoftmaxThreads) {
-            const int r = i / nsplit, sp = i % nsplit;
-            const long long row = first_row + static_cast<long long>(sp) * NR + r;
-            wm[r * kMergeSplits + sp] = __ldcg(a.part_ml + row * 2);
-            wl[r * kMergeSplits + sp] = __ldcg(a.part_ml + row * 2 + 1);
-          }
-          named_sync(1, kSoftmaxThreads);
-          if (tid - 64 < nrows) {
-            const int r = tid - 64;
-            float m = -INFINITY;
-            for (int sp = 0; sp < nsplit; ++sp)
-              if (wl[r * kMergeSplits + sp] > 0.f) m = fmaxf(m, wm[r * kMergeSplits + sp]);
-            float lsum = 0.f;
-            for (int sp = 0; sp < nsplit; ++sp) {
-              const float ls = wl[r * kMergeSplits + sp];
-              const float w = ls > 0.f ? exp2f(wm[r * kMergeSplits + sp] - m) : 0.f;
-              wm[r * kMergeSplits + sp] = w;
-              lsum += w * ls;
-            }
-            linv[r] = 1.f / lsum;
-          }
-          named_sync(1, kSoftmaxThreads);
-          for (int r = 0; r < nrows && d_ok; ++r) {
-            float acc = 0.f;
-#pragma unroll 4
-            for (int sp = 0; sp < nsplit; ++sp)
-              acc = fmaf(wm[r * kMergeSplits + sp],
-                         __ldcg(a.part_o + (first_row + static_cast<long long>(sp) * NR + r) * kDh + d), acc);
-            const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-            if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc * linv[r] * a.v_scale;
-          }
-        } else {
-          for (int r = 0; r < nrows && d_ok; ++r) {
-            float m = -INFINITY, l = 0.f, acc = 0.f;
-            for (int sp = 0; sp < nsplit; ++sp) {
+        named_sync(1, kSoftmaxThreads);
+        int* counter = a.counters + unit * a.H_kv + kvh;
+        if (tid == 64) ctl->last = (atomicAdd(counter, 1) == nsplit - 1);
+        named_sync(1, kSoftmaxThreads);
+        if (ctl->last) {
+          __threadfence();
+          const long long first_row = static_cast<long long>(plan.prefix[unit] + kvh * nsplit) * NR;
+          if (nsplit <= kMergeSplits) {
+            // every split's (m, l) at once into the P buffer (free now), then one set of weights per
+            // row, then independent loads of the partial outputs
+            float* wm = reinterpret_cast<float*>(p_base);            // [NR][kMergeSplits] m, then weight
+            float* wl = wm + NR * kMergeSplits;                      // [NR][kMergeSplits] l
+            float* linv = wl + NR * kMergeSplits;                    // [NR]
+            for (int i = tid - 64; i < nrows * nsplit; i += kSoftmaxThreads) {
+              const int r = i / nsplit, sp = i % nsplit;
               const long long row = first_row + static_cast<long long>(sp) * NR + r;
-              const float ms = __ldcg(a.part_ml + row * 2), ls = __ldcg(a.part_ml + row * 2 + 1);
-              if (!(ls > 0.f)) continue;
-              const float mn = fmaxf(m, ms);
-              const float c_old = exp2f(m - mn), c_new = exp2f(ms - mn);
-              l = l * c_old + ls * c_new;
-              acc = acc * c_old + __ldcg(a.part_o + row * kDh + d) * c_new;
-              m = mn;
+              wm[r * kMergeSplits + sp] = __ldcg(a.part_ml + row * 2);
+              wl[r * kMergeSplits + sp] = __ldcg(a.part_ml + row * 2 + 1);
             }
-            const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-            if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l * a.v_scale;
+            named_sync(1, kSoftmaxThreads);
+            if (tid - 64 < nrows) {
+              const int r = tid - 64;
+              float m = -INFINITY;
+              for (int sp = 0; sp < nsplit; ++sp)
+                if (wl[r * kMergeSplits + sp] > 0.f) m = fmaxf(m, wm[r * kMergeSplits + sp]);
+              float lsum = 0.f;
+              for (int sp = 0; sp < nsplit; ++sp) {
+                const float ls = wl[r * kMergeSplits + sp];
+                const float w = ls > 0.f ? exp2f(wm[r * kMergeSplits + sp] - m) : 0.f;
+                wm[r * kMergeSplits + sp] = w;
+                lsum += w * ls;
+              }
+              linv[r] = 1.f / lsum;
+            }
+            named_sync(1, kSoftmaxThreads);
+            for (int r = 0; r < nrows && d_ok; ++r) {
+              float acc = 0.f;
+  #pragma unroll 4
+              for (int sp = 0; sp < nsplit; ++sp)
+                acc = fmaf(wm[r * kMergeSplits + sp],
+                           __ldcg(a.part_o + (first_row + static_cast<long long>(sp) * NR + r) * kDh + d), acc);
+              const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+              if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc * linv[r] * a.v_scale;
+            }
+          } else {
+            for (int r = 0; r < nrows && d_ok; ++r) {
+              float m = -INFINITY, l = 0.f, acc = 0.f;
+              for (int sp = 0; sp < nsplit; ++sp) {
+                const long long row = first_row + static_cast<long long>(sp) * NR + r;
+                const float ms = __ldcg(a.part_ml + row * 2), ls = __ldcg(a.part_ml + row * 2 + 1);
+                if (!(ls > 0.f)) continue;
+                const float mn = fmaxf(m, ms);
+                const float c_old = exp2f(m - mn), c_new = exp2f(ms - mn);
+                l = l * c_old + ls * c_new;
+                acc = acc * c_old + __ldcg(a.part_o + row * kDh + d) * c_new;
+                m = mn;
+              }
+              const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+              if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l * a.v_scale;
+            }
           }
+          if (tid == 64) *counter = 0;
         }
-        if (tid == 64) *counter = 0;
       }
     }
-  }
+
+  }  // warps 1-5
 
   // ---- teardown: every TMEM access is complete before the allocating warp frees it -------------
   tc_fence_before();
