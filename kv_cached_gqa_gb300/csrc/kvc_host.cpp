@@ -356,23 +356,48 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
   const int cmax = max_tiles * tile;
   const long long slots = 2LL * h->num_sms;
   const long long work = total_keys * h->H;
+  // splits of about w keys: a unit of n keys takes round(n / w) near-equal whole-tile splits, at most
+  // cmax keys each; `ns = ceil(n / chunk)` keeps the kernels' recomputed chunk and leaves no split empty
+  auto splits_for = [&](long long n, long long w_, int* chunk_out) {
+    int ns = static_cast<int>(std::max(1LL, (n + w_ / 2) / w_));
+    while (kvc::split_chunk(static_cast<int>(n), ns, tile) > cmax) ++ns;
+    const int chunk = kvc::split_chunk(static_cast<int>(n), ns, tile);
+    *chunk_out = chunk;
+    return static_cast<int>((n + chunk - 1) / chunk);
+  };
   long long w = h->split_keys_override;
   if (w <= 0) {
     const long long waves = std::max(1LL, (work + slots * 1536 - 1) / (slots * 1536));
     w = (work + waves * slots - 1) / (waves * slots);
+    // at least 4 tiles per split when the work spans several waves (shorter splits cost more in
+    // set-up and merging than they return); down to one tile when it fits one wave, where the time is
+    // the latency of each CTA's chain of tiles
+    w = std::max<long long>(w, (waves > 1 ? 4LL : 1LL) * tile);
+    // the per-unit rounding can add CTAs past the whole waves aimed at, leaving a short last wave:
+    // take the smallest split size (binary search, the CTA count falls as it grows) whose CTAs fit
+    const long long target = waves * slots;
+    auto items_at = [&](long long w_) {
+      long long n_items = 0;
+      int c = 0;
+      for (int u = 0; u < n_units; ++u) n_items += static_cast<long long>(h->H) * splits_for(n_eff[u], w_, &c);
+      return n_items;
+    };
+    if (items_at(w) > target) {
+      long long lo_w = w, hi_w = std::max<long long>(w, cmax);
+      if (items_at(hi_w) <= target) {
+        while (hi_w - lo_w > 1) {
+          const long long mid = (lo_w + hi_w) / 2;
+          if (items_at(mid) <= target) hi_w = mid; else lo_w = mid;
+        }
+        w = hi_w;
+      }
+    }
   }
-  // at least 4 tiles per split unless overridden: shorter splits cost more in set-up and merging
-  // than their parallelism returns
-  if (h->split_keys_override <= 0) w = std::max<long long>(w, 4LL * tile);
   w = std::max(1LL, w);
   for (int u = 0; u < n_units; ++u) {
-    const int n = static_cast<int>(n_eff[u]);
-    int ns = static_cast<int>(std::max(1LL, (n_eff[u] + w / 2) / w));
-    while (kvc::split_chunk(n, ns, tile) > cmax) ++ns;
-    const int chunk = kvc::split_chunk(n, ns, tile);        // whole tiles, as the kernels recompute it
-    ns = (n + chunk - 1) / chunk;                           // same chunk, no empty trailing split
+    int chunk = 0;
+    nsplit[u] = splits_for(n_eff[u], w, &chunk);             // whole tiles, as the kernels recompute it
     order[u] = {chunk, u};
-    nsplit[u] = ns;
   }
   std::stable_sort(order.begin(), order.end(), longest_first);
   long long items = 0;
