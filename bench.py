@@ -423,26 +423,47 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         graph_ms = float(t[0])
 
-    # end to end through the public API with host buffers: pinned inputs copied in and outputs
-    # read back inside the timed region, every step
+    # end to end through the public API with host buffers: every step copies every layer's inputs in
+    # from pinned host memory and reads every layer's output back, inside the timed region. The copies
+    # run on their own stream, as a serving loop would issue them: layer l + 1's inputs arrive while
+    # layer l computes, and layer l's output leaves while layer l + 1 computes. Device buffers are
+    # double-buffered across steps; events order every copy against the kernels that use its data.
     e2e = None
     if not args.no_e2e:
         host_in = [tuple(x.cpu().pin_memory() for x in trio) for trio in inputs]
-        host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
-        dev_in = [tuple(torch.empty_like(x) for x in trio) for trio in inputs]
+        host_out = [[torch.empty_like(o, device="cpu").pin_memory() for o in outs] for _ in range(2)]
+        dev_in = [[tuple(torch.empty_like(x) for x in trio) for trio in inputs] for _ in range(2)]
+        dev_out = [[torch.empty_like(o) for o in outs] for _ in range(2)]
         h2d = sum(x.numel() * x.element_size() for trio in host_in for x in trio)
-        d2h = sum(o.numel() * o.element_size() for o in host_out)
+        d2h = sum(o.numel() * o.element_size() for o in host_out[0])
+        copy_stream = torch.cuda.Stream()
+        ev_in = [[torch.cuda.Event() for _ in range(sp.L)] for _ in range(2)]
+        ev_done = [[torch.cuda.Event() for _ in range(sp.L)] for _ in range(2)]
+        ev_set_free = [torch.cuda.Event() for _ in range(2)]
+        n_step = [0]
 
         def e2e_step():
+            st = n_step[0] % 2
+            n_step[0] += 1
+            copy_stream.wait_event(ev_set_free[st])          # the step that last used this set is done
+            with torch.cuda.stream(copy_stream):
+                for layer in range(sp.L):
+                    for d_, h_ in zip(dev_in[st][layer], host_in[layer]):
+                        d_.copy_(h_, non_blocking=True)
+                    ev_in[st][layer].record(copy_stream)
             for layer in range(sp.L):
-                for d_, h_ in zip(dev_in[layer], host_in[layer]):
-                    d_.copy_(h_, non_blocking=True)
-                *qs, k, v = dev_in[layer]
+                stream.wait_event(ev_in[st][layer])
+                *qs, k, v = dev_in[st][layer]
                 wl.append(layer, k, v)
-                wl.attend(qs, layer, out=outs[layer])
-                host_out[layer].copy_(outs[layer], non_blocking=True)
+                wl.attend(qs, layer, out=dev_out[st][layer])
+                ev_done[st][layer].record(stream)
+                copy_stream.wait_event(ev_done[st][layer])
+                with torch.cuda.stream(copy_stream):
+                    host_out[st][layer].copy_(dev_out[st][layer], non_blocking=True)
             kb.kvc_commit(wl.cache)
             kb.kvc_truncate_ragged(wl.cache, lengths)
+            ev_set_free[st].record(copy_stream)              # after the step's last read-back
+            stream.wait_event(ev_set_free[st])               # the step ends when its outputs are home
 
         for _ in range(max(3, args.warmup)):
             e2e_step()
