@@ -31,6 +31,8 @@ if ROOT not in sys.path:
 METRIC = "cached GQA decode-attention HBM GB/s (% of peak) and decode steps/sec"
 DEFAULT_WORKLOAD = "llama3-8b-decode-bf16"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TFLOPS = 1900.0             # dense bf16, burst (fallback only)
+FALLBACK_TFLOPS_SUSTAINED = 1700.0   # dense bf16, sustained (fallback only)
 
 
 def parse_args(argv=None):
@@ -66,30 +68,56 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense 16-bit tensor TFLOP/s (bf16 and f16 run at the same rate): the sustained cuBLAS figure,
+    since the attention kernel is timed inside a step of many back-to-back layers."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_TFLOPS_SUSTAINED, FALLBACK_TFLOPS, "fallback"
+
+
 # The attention call of every TIMED_EVERY-th layer is bracketed by CUDA events (the roofline's kernel
 # time); an event between two launches ends their programmatic overlap, so not every layer is timed.
 TIMED_EVERY = 4
 
-KERNEL_SOURCES = ("kvc_decode_tc.cu", "kvc_splitk.cu", "kvc_device.cuh", "kvc_host.cpp", "kvc_internal.h")
+# The sources that define each attention kernel and its launch plan: a stored DRAM traffic figure
+# stands only while these are unchanged since its ncu capture.
+_SHARED_SOURCES = ("kvc_device.cuh", "kvc_host.cpp", "kvc_internal.h")
+KERNEL_SOURCES = {
+    "decode_tc_kernel": ("kvc_decode_tc.cu", "kvc_splitk.cu") + _SHARED_SOURCES,
+    "prefill_tc_kernel": ("kvc_prefill_tc.cu",) + _SHARED_SOURCES,
+    "mla_tc_kernel": ("kvc_mla_tc.cu",) + _SHARED_SOURCES,
+    "mla_kernel": ("kvc_mla.cu",) + _SHARED_SOURCES,
+    "splitk_kernel": ("kvc_splitk.cu",) + _SHARED_SOURCES,
+}
 
 
-def kernel_source_hash():
-    """Hash of the sources that define the attention kernels and their launch plan."""
+def kernel_of(sp):
+    """The attention kernel's name, as `attention_kernel_name` states it."""
+    return attention_kernel_name(sp).split("(")[1].split(":")[0]
+
+
+def kernel_source_hash(kernel):
+    """Hash of the sources that define `kernel` and its launch plan."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "kv_cached_gqa_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch(workload):
+def traffic_per_launch(sp):
     """DRAM bytes per attention launch from the committed ncu summary, if the kernel is unchanged."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d[workload]
-        if e.get("kernel_sha") == kernel_source_hash():
+        e = d[sp.name]
+        if e.get("kernel_sha") == kernel_source_hash(kernel_of(sp)):
             return e["dram_bytes_per_launch"]
     except (OSError, KeyError, ValueError):
         pass
@@ -515,14 +543,7 @@ def run_ours(args):
                          "note": "the same step captured once in a CUDA graph and replayed (no host launches)"},
         "pct_of_peak": {"measured_hbm": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / 8000.0, 2)},
-        "roofline": {"kernel": attention_kernel_name(sp),
-                     "bound": "hbm",
-                     "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(attn_gbs / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                     "bytes_per_launch": sp.attn_bytes(), "launch_ms": round(attn_avg_ms, 5),
-                     "timing": f"CUDA events around the attention call of every {TIMED_EVERY}th layer" + (
-                         " (in a pass without the graph)" if args.graph else " inside the timed region"),
-                     "traffic": traffic_per_launch(args.workload)},
+        "roofline": roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args),
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -534,6 +555,30 @@ def run_ours(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args):
+    """The attention kernel against its roofline: HBM GB/s, or dense tensor TFLOP/s when the call's
+    arithmetic intensity (causal-counted flops per algorithmic byte) is above the ridge point."""
+    t_sus, t_burst, t_kind = measured_tensor_peak()
+    flops = sp.attn_flops()
+    ridge = t_sus * 1e12 / (peak * 1e9)
+    timing = f"CUDA events around the attention call of every {TIMED_EVERY}th layer" + (
+        " (in a pass without the graph)" if args.graph else " inside the timed region")
+    e = {"kernel": attention_kernel_name(sp)}
+    if flops / sp.attn_bytes() > ridge:
+        tflops = flops / (attn_avg_ms * 1e-3) / 1e12
+        e.update({"bound": "tensor", "achieved": round(tflops, 2), "peak": t_sus, "unit": "TFLOP/s",
+                  "frac": round(tflops / t_sus, 4), "peak_source": f"{t_kind} bf16_tflops_sustained",
+                  "frac_of_burst_peak": round(tflops / t_burst, 4),
+                  "flops_per_launch": flops, "flops_counted": "causal: unmasked (query, key) pairs only",
+                  "hbm_gbs": round(attn_gbs, 2)})
+    else:
+        e.update({"bound": "hbm", "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
+                  "frac": round(attn_gbs / peak, 4), "peak_source": f"{peak_kind} hbm_gbs"})
+    e.update({"bytes_per_launch": sp.attn_bytes(), "launch_ms": round(attn_avg_ms, 5), "timing": timing,
+              "traffic": traffic_per_launch(sp)})
+    return e
 
 
 def main(argv=None):

@@ -1,26 +1,32 @@
 // Chunk (prefill) attention over the KV cache on the 5th-generation tensor cores (tcgen05 + TMEM),
-// for 16-bit caches with d_h = 128 and many query rows per K/V head (G * T > 32).
+// for 16-bit caches with d_h = 128 and many query rows per K/V head (G * T > 16).
 //
 // What it computes ("KV cache, incremental decode, ...", §2.3 and §4 test_chunked_prefill_equals_whole;
 // "KV cache decoding", "Prefill and decode"; "Heads, GQA and K/V cache"): query row (t, h) of a chunk
 // at positions s_b .. s_b + T - 1 attends over stored keys j <= s_b + t.
 //
-// How: the G query heads of one K/V head and 128 / G consecutive chunk positions form a tile of 128
-// query rows (rows r = t * G + g), the M dimension; 128-key tiles are N:
-//   S  [128 rows x 128 keys] = Q . K_j^T        A = Q (K-major), B = K tile (K-major)
-//   Ot [128 rows x 128 d   ] = P_j . V_j        A = P (K-major, shared memory), B = V tile (MN-major)
-// One CTA per (sequence, K/V head, row tile), one CTA per SM (all 512 TMEM columns):
-//   warp 0     TMA: K_j and V_j tiles through a ring;
-//   warp 1     owns TMEM, issues QK(j + 1) before PV(j) so the tensor cores run ahead of the softmax;
-//   warps 2-5  one thread per query row: online softmax in base 2 against a per-row reference
-//              maximum m_ref; P = 2^(s - m_ref) goes to shared memory (f16; for bf16 a hi + lo pair,
-//              so P keeps ~2^-16 relative accuracy). The output accumulates in TMEM across tiles;
-//              it is rescaled (read, multiply, write back) only when a row's maximum passes
-//              m_ref + 8, which keeps P <= 2^8 and happens only on the first tiles of a row in
-//              practice. The final division by the row sum uses the same reference, so the result
-//              is the plain softmax.
-// Tiles of keys past a row tile's last visible key are skipped; the diagonal tiles are masked per
-// row. Every wait is bounded (~1 s) and reported through the device status word.
+// How: the G query heads of one K/V head and consecutive chunk positions form query rows
+// r = t * G + g. A CTA takes 256 of them as two MMA tiles of 128 rows (the M dimension), so every
+// K/V tile it loads serves both; 128-key tiles are N:
+//   S_t [128 rows x 128 keys] = Q_t . K_j^T    A = Q_t (K-major, shared memory), B = K tile (K-major)
+//   O_t [128 rows x 128 d   ] += P_t . V_j     A = P_t (tensor memory), B = V tile (MN-major)
+// Tensor memory (512 columns) holds, per tile t, S_t in 128 columns and O_t in the next 128. Each
+// softmax thread overwrites its row of S_t with P_t in 16-bit form once it has read the scores, and
+// the PV product takes P_t straight from there, so P never passes through shared memory.
+// Roles (352 threads, one CTA per SM):
+//   warp 0      TMA: K_j and V_j tiles through a ring;
+//   warps 1, 10 one thread each issues the MMAs of tile 0 and of tile 1: PV_t(j), then QK_t(j+1),
+//               so the tensor cores work on one tile while the softmax of the other runs, and the
+//               two tiles' products (independent accumulators) overlap in the tensor pipe;
+//   warps 2-5   softmax of tile 0, warps 6-9 softmax of tile 1: one thread per query row, online
+//               softmax in base 2 against a per-row reference maximum m_ref; P = 2^(s - m_ref) in
+//               f16 (for bf16 a hi + lo pair, so P keeps ~2^-16 relative accuracy). O accumulates
+//               in tensor memory across key tiles and is rescaled (read, multiply, write back) only
+//               when a row's maximum passes m_ref + 8, which keeps P <= 2^8 and happens only on the
+//               first tiles of a row in practice. The final division by the row sum uses the same
+//               reference, so the result is the plain softmax.
+// Tiles of keys past a tile's last visible key are skipped; the diagonal tiles are masked per row.
+// Every wait is bounded (~1 s) and reported through the device status word.
 #include "kvc_device.cuh"
 #include "kvc_internal.h"
 
@@ -29,36 +35,31 @@ namespace {
 
 using namespace dev;
 
-constexpr int kRows = 128;                   // query rows per CTA (MMA M)
+constexpr int kRows = 128;                   // query rows per MMA tile (MMA M)
+constexpr int kTiles = 2;                    // MMA tiles per CTA
+constexpr int kUnitRows = kTiles * kRows;    // query rows per CTA
 constexpr int kKeys = 128;                   // keys per tile (MMA N of QK, K of PV)
 constexpr int kDh = 128;
 constexpr int kBox = 128 * 128;              // one 128-byte-swizzled atom column of 128 rows (16 KB)
 constexpr int kTile = 2 * kBox;              // 32 KB: 128 rows x 128 16-bit values
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kTmemCols = 512;
+constexpr int kSoftmaxThreads = 128;         // per MMA tile
+constexpr int kThreads = 32 + kTiles * kSoftmaxThreads + kTiles * 32;   // TMA, softmax, one MMA issuer per tile
+constexpr int kTmemCols = 512;               // per tile: S_t / P_t (128 columns), then O_t (128)
+constexpr int kStages = 5;                   // K/V ring, one 32 KB tile per stage
 
-template <typename Tc>
-struct PLayout {
-  static constexpr bool kHiLo = std::is_same<Tc, __nv_bfloat16>::value;
-  static constexpr int kParts = kHiLo ? 2 : 1;
-  static constexpr int kStages = kHiLo ? 3 : 4;             // K/V ring (each stage one 32 KB tile)
-  static constexpr int kQOff = 0;
-  static constexpr int kRingOff = kQOff + kTile;
-  static constexpr int kPOff = kRingOff + kStages * kTile;
-  static constexpr int kCtlOff = kPOff + kParts * kTile;
-};
+constexpr int kQOff = 0;                     // Q_0, Q_1
+constexpr int kRingOff = kQOff + kTiles * kTile;
+constexpr int kCtlOff = kRingOff + kStages * kTile;
 
 struct __align__(8) PCtl {
-  unsigned long long full[4], empty[4];
-  unsigned long long s_full[2], s_free[2];
-  unsigned long long p_full, p_free, o_full, done;
+  unsigned long long full[kStages], empty[kStages];
+  unsigned long long s_full[kTiles], p_full[kTiles], pv_done[kTiles];
+  unsigned long long done[kTiles];
   uint32_t tmem;
   int abort;
 };
 
-template <typename Tc>
-constexpr size_t prefill_smem() { return 1024 + PLayout<Tc>::kCtlOff + sizeof(PCtl); }
+constexpr size_t prefill_smem() { return 1024 + kCtlOff + sizeof(PCtl); }
 
 // offset of 16-byte chunk `c` (0..15) of row `r` in a [128 rows][128 16-bit] swizzled tile
 __device__ __forceinline__ uint32_t chunk_off(int r, int c) {
@@ -72,30 +73,70 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+#define KVC_R8(b) "=r"(r[b]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), "=r"(r[b + 4]), \
+                  "=r"(r[b + 5]), "=r"(r[b + 6]), "=r"(r[b + 7])
+
+// 128 consecutive 32-bit columns of this thread's TMEM lane in one load (warp w: lanes 32*(w%4)..+31)
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* v) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
+      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,"
+      "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+      "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127"
+      "}, [%128];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : KVC_R8(0), KVC_R8(8), KVC_R8(16), KVC_R8(24), KVC_R8(32), KVC_R8(40), KVC_R8(48), KVC_R8(56),
+        KVC_R8(64), KVC_R8(72), KVC_R8(80), KVC_R8(88), KVC_R8(96), KVC_R8(104), KVC_R8(112), KVC_R8(120)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : KVC_R8(0), KVC_R8(8), KVC_R8(16), KVC_R8(24)
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+#undef KVC_R8
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+// 32 consecutive 32-bit columns of this thread's TMEM lane (completion: tcgen05.wait::st)
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* w) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-      :: "r"(taddr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
-         "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]),
-         "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]),
-         "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      :: "r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+         "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
+         "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
+         "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
       : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      :: "r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+         "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D (tensor memory) [+]= A (tensor memory, K-major) . B (shared memory descriptor)
+__device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+      :: "r"(tmem_d), "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 // 2^x with the hardware approximation (relative error ~2^-22), flushing subnormal results to zero
@@ -105,7 +146,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// two floats -> one 32-bit word of two 16-bit values (round to nearest even), in one conversion
+// two floats -> one 32-bit word of two 16-bit values (round to nearest even), in one conversion;
+// the first float takes the low half (the lower key index of a K-major operand)
 template <typename Tc>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   if constexpr (std::is_same<Tc, __half>::value) {
@@ -127,81 +169,63 @@ template <typename Tc>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
-  using Lo = PLayout<Tc>;
-  constexpr int kStages = Lo::kStages;
+  constexpr bool kHiLo = std::is_same<Tc, __nv_bfloat16>::value;
+  constexpr uint32_t kFmt = kHiLo ? 1u : 0u;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  PCtl* ctl = reinterpret_cast<PCtl*>(sm + Lo::kCtlOff);
-  const uint32_t s_q = smem_u32(sm + Lo::kQOff);
-  const uint32_t s_ring = smem_u32(sm + Lo::kRingOff);
-  unsigned char* p_base = sm + Lo::kPOff;
-  const uint32_t s_p = smem_u32(p_base);
+  PCtl* ctl = reinterpret_cast<PCtl*>(sm + kCtlOff);
+  const uint32_t s_q = smem_u32(sm + kQOff);
+  const uint32_t s_ring = smem_u32(sm + kRingOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr uint32_t kFmt = std::is_same<Tc, __nv_bfloat16>::value ? 1u : 0u;
 
-  // ---- work item: (unit = sequence x row tile, K/V head) -----------------------------------------
+  // ---- work item: (unit = sequence x 256-row tile, K/V head) -------------------------------------
   const int item = blockIdx.x;
   const int unit = item / a.H_kv, kvh = item % a.H_kv;
   const int b = plan.unit_b[unit] / plan.n_rowtiles;
-  const int rt = plan.unit_b[unit] % plan.n_rowtiles;
-  const int row0 = rt * kRows;
-  const int nrows = min(kRows, a.T * a.G - row0);
+  const int row0 = (plan.unit_b[unit] % plan.n_rowtiles) * kUnitRows;
+  const int n_rows = a.T * a.G;
 
   // ---- set-up ------------------------------------------------------------------------------------
   if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&ctl->tmem));
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), kTiles);          // one release per MMA issuer
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&ctl->s_full[s]), 1);
-      mbar_init(smem_u32(&ctl->s_free[s]), kSoftmaxThreads / 32);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(smem_u32(&ctl->s_full[t]), 1);
+      mbar_init(smem_u32(&ctl->p_full[t]), kSoftmaxThreads / 32);
+      mbar_init(smem_u32(&ctl->pv_done[t]), 1);
     }
-    mbar_init(smem_u32(&ctl->p_full), kSoftmaxThreads / 32);
-    mbar_init(smem_u32(&ctl->p_free), 1);
-    mbar_init(smem_u32(&ctl->o_full), 1);
-    mbar_init(smem_u32(&ctl->done), 1);
+    for (int t = 0; t < kTiles; ++t) mbar_init(smem_u32(&ctl->done[t]), 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
-  // from here on the lengths and the queries, which earlier kernels write, are read
-  pdl_wait();
-  pdl_trigger();
-  const int s_b = a.lens[b] + a.delta - a.T;
-  const int first_t = row0 / a.G, last_t = (row0 + nrows - 1) / a.G;
-  const int n_keys = s_b + last_t + 1;                       // keys visible to the tile's last row
-  const int nkt = (n_keys + kKeys - 1) / kKeys;
-  const int unmasked_keys = s_b + first_t + 1;               // keys visible to every row of the tile
-  // Q tile: 128 rows x 128 d in the cache dtype, 128-byte swizzled (rows past the chunk are zero)
-  for (int i = tid; i < kRows * (kDh / 8); i += kThreads) {
-    const int r = i / (kDh / 8), c = i % (kDh / 8);
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (r < nrows) {
-      const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-      const long long base = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + c * 8;
-      if (a.rope.table != nullptr) {          // rotated to position s_b + t, element by element
-        float x[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[j] = load_query_rot<Tc>(a, base - c * 8, c * 8 + j, s_b + t);
-        w = make_uint4(pack2<Tc>(x[0], x[1]), pack2<Tc>(x[2], x[3]), pack2<Tc>(x[4], x[5]), pack2<Tc>(x[6], x[7]));
-      } else if (a.q_dtype == KVC_F32) {
-        const float4 x0 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + base);
-        const float4 x1 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + base + 4);
-        w = make_uint4(pack2<Tc>(x0.x, x0.y), pack2<Tc>(x0.z, x0.w), pack2<Tc>(x1.x, x1.y), pack2<Tc>(x1.z, x1.w));
-      } else {
-        w = *reinterpret_cast<const uint4*>(static_cast<const Tc*>(a.q) + base);
-      }
-    }
-    *reinterpret_cast<uint4*>(sm + Lo::kQOff + chunk_off(r, c)) = w;
-  }
-  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
   volatile int* abort_flag = &ctl->abort;
+
+  // from here on the lengths and the queries, which earlier kernels write, are read
+  pdl_wait();
+  pdl_trigger();
+  const int s_b = a.lens[b] + a.delta - a.T;
+  // key tiles of MMA tile t: up to the key its last row sees; 0 for a tile past the chunk's rows
+  int nk[kTiles];
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    const int first = row0 + t * kRows, last = min(first + kRows, n_rows) - 1;
+    nk[t] = last >= first ? (s_b + last / a.G + 1 + kKeys - 1) / kKeys : 0;
+  }
+  const int nkt = max(nk[0], nk[1]);
+  // Where step j of tile t keeps S / P and which barriers (s_full, p_full, pv_done) it uses. Two
+  // tiles: tile t's slot, the barriers' phase j. One tile: the two slots in turn (phase j / 2), so
+  // QK(j+1) need not wait for PV(j).
+  const bool pair = nk[1] > 0;
+  struct Slot { int bar, phase; };
+  auto slot = [pair](int t, int j) -> Slot { return pair ? Slot{t, j} : Slot{j & 1, j >> 1}; };
 
   if (warp == 0) {
     // ---------------------------------- TMA producer (whole warp): K0, V0, K1, V1, ... -------------
@@ -226,160 +250,263 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     if (lane == 0)
       for (int i = max(0, issued - kStages); i < issued; ++i)
         mbar_drain(smem_u32(&ctl->full[i % kStages]), (i / kStages) & 1);
-  } else if (warp == 1) {
-    // ---------------------------------- MMA issuer ------------------------------------------------
-    if (lane == 0) {
-      const uint32_t idesc_s = umma_idesc(kRows, kKeys, kFmt, 0, 0);
-      const uint32_t idesc_o = umma_idesc(kRows, kDh, kFmt, 0, 1);
-      bool ok = true;
-      auto issue_qk = [&](int j) -> bool {
-        const int i = 2 * j, st = i % kStages, sb = j & 1;
-        if (!mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag)) return false;
-        if (!mbar_wait(smem_u32(&ctl->s_free[sb]), ((j >> 1) & 1) ^ 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t kt = s_ring + st * kTile;
-#pragma unroll
-        for (int ks = 0; ks < kDh / 16; ++ks)
-          umma_f16(tmem + sb * kKeys,
-                   umma_desc(s_q + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128),
-                   umma_desc(kt + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128), idesc_s, ks > 0);
-        umma_commit(smem_u32(&ctl->empty[st]));
-        umma_commit(smem_u32(&ctl->s_full[sb]));
-        return true;
-      };
-      if (nkt > 0) ok = issue_qk(0);
-      for (int j = 0; j < nkt && ok; ++j) {
-        if (j + 1 < nkt) ok = issue_qk(j + 1);
-        if (!ok) break;
-        const int i = 2 * j + 1, st = i % kStages;
-        ok = mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag) &&
-             mbar_wait(smem_u32(&ctl->p_full), j & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t vt = s_ring + st * kTile;
-#pragma unroll
-        for (int part = 0; part < Lo::kParts; ++part)
-#pragma unroll
-          for (int ks = 0; ks < kKeys / 16; ++ks)
-            umma_f16(tmem + 2 * kKeys,
-                     umma_desc(s_p + part * kTile + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128),
-                     umma_desc(vt + ks * 2048, kBox, 1024, kSwizzle128), idesc_o, (j | part | ks) != 0);
-        umma_commit(smem_u32(&ctl->empty[st]));
-        umma_commit(smem_u32(&ctl->p_free));
-      }
-      if (ok) umma_commit(smem_u32(&ctl->o_full));
-      umma_commit(smem_u32(&ctl->done));
-      mbar_drain(smem_u32(&ctl->done), 0);
-    }
   } else {
-    // ---------------------------------- softmax and epilogue ---------------------------------------
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;                          // this thread's query row (TMEM lane)
-    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tmem_o = tmem + lane_base + 2 * kKeys;
-    const bool row_ok = r < nrows;
-    const int t_row = row_ok ? (row0 + r) / a.G : 0;
-    const int last_key = s_b + t_row;                        // this row sees keys <= last_key
-    const float scale = kLog2e * rsqrtf(static_cast<float>(kDh));
-    constexpr float kSlack = 8.f;                            // P <= 2^kSlack before a rescale is forced
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkt && ok; ++j) {
-      const int sb = j & 1;
-      ok = mbar_wait(smem_u32(&ctl->s_full[sb]), (j >> 1) & 1, abort_flag);
-      if (!ok) break;
-      tc_fence_after();
-      float v[kKeys];
+    // ---- Q_0, Q_1: 256 rows x 128 d in the cache dtype, 128-byte swizzled (rows past the chunk zero)
+    constexpr int kChunks = kUnitRows * (kDh / 8);
+    constexpr int kStagers = kThreads - 32;
+    constexpr int kBatch = (kChunks + kStagers - 1) / kStagers;   // every load in flight at once
+    for (int i0 = tid - 32; i0 < kChunks; i0 += kBatch * kStagers) {
+      uint4 raw[kBatch][2];
 #pragma unroll
-      for (int c = 0; c < kKeys; c += 32) tmem_ld32(tmem + lane_base + sb * kKeys + c, v + c);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free[sb]));  // S buffer may be overwritten now
-      const int key0 = j * kKeys;
-      if ((j + 1) * kKeys > unmasked_keys || !row_ok) {        // diagonal tile (or padding row)
-#pragma unroll
-        for (int e = 0; e < kKeys; ++e)
-          if (!row_ok || key0 + e > last_key) v[e] = -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = v[k];
-#pragma unroll
-      for (int e = 8; e < kKeys; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
-      const float tmax = scale * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      // a new reference when this row's maximum passes the old one by more than kSlack
-      const bool bump = tmax > m_ref + kSlack;
-      const float m_new = bump ? tmax : m_ref;
-      const float alpha = bump ? ((m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new)) : 1.f;
-      // the previous tile's PV must be done before P is overwritten or the output rescaled
-      ok = mbar_wait(smem_u32(&ctl->p_free), (j & 1) ^ 1, abort_flag);
-      if (!ok) break;
-      if (j > 0 && __any_sync(0xffffffffu, bump)) {
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < kDh; c += 32) {
-          float ov[32];
-          tmem_ld32(tmem_o + c, ov);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-          tmem_st32(tmem_o + c, ov);
+      for (int k = 0; k < kBatch; ++k) {                     // all of this batch's loads first
+        raw[k][0] = raw[k][1] = make_uint4(0, 0, 0, 0);
+        const int i = i0 + k * kStagers;
+        const int r = i / (kDh / 8), c = i % (kDh / 8);
+        if (i < kChunks && row0 + r < n_rows && a.rope.table == nullptr) {
+          const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+          const long long base = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + c * 8;
+          raw[k][0] = load_query4_raw<Tc>(a.q, a.q_dtype, base);
+          raw[k][1] = load_query4_raw<Tc>(a.q, a.q_dtype, base + 4);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      l *= alpha;
-      m_ref = m_new;
-      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;   // padding rows: every score is -inf
-      float ls[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+      for (int k = 0; k < kBatch; ++k) {
+        const int i = i0 + k * kStagers;
+        if (i >= kChunks) break;
+        const int r = i / (kDh / 8), c = i % (kDh / 8);
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (row0 + r < n_rows) {
+          if (a.rope.table != nullptr) {       // rotated to position s_b + t, element by element
+            const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+            const long long row = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh;
+            float x[8];
 #pragma unroll
-      for (int c8 = 0; c8 < kKeys / 8; ++c8) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = fast_exp2(fmaf(v[c8 * 8 + e], scale, neg_m));  // 0 for masked keys (-inf)
-          ls[e] += p[e];
-        }
-        const uint4 w = make_uint4(pack2<Tc>(p[0], p[1]), pack2<Tc>(p[2], p[3]), pack2<Tc>(p[4], p[5]),
-                                   pack2<Tc>(p[6], p[7]));
-        *reinterpret_cast<uint4*>(p_base + chunk_off(r, c8)) = w;
-        if constexpr (Lo::kParts == 2) {
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-          uint32_t lo[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 h = unpack2<Tc>(ww[k]);
-            lo[k] = pack2<Tc>(p[2 * k] - h.x, p[2 * k + 1] - h.y);
+            for (int e = 0; e < 8; ++e) x[e] = load_query_rot<Tc>(a, row, c * 8 + e, s_b + t);
+            w = make_uint4(pack2<Tc>(x[0], x[1]), pack2<Tc>(x[2], x[3]), pack2<Tc>(x[4], x[5]),
+                           pack2<Tc>(x[6], x[7]));
+          } else {
+            const uint2 lo = query4_to<Tc, Tc>(raw[k][0], a.q_dtype);
+            const uint2 hi = query4_to<Tc, Tc>(raw[k][1], a.q_dtype);
+            w = make_uint4(lo.x, lo.y, hi.x, hi.y);
           }
-          *reinterpret_cast<uint4*>(p_base + kTile + chunk_off(r, c8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+        *reinterpret_cast<uint4*>(sm + kQOff + (r / kRows) * kTile + chunk_off(r % kRows, c)) = w;
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tc_fence_before();
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
     }
-    // ---- epilogue: O / l ---------------------------------------------------------------------------
-    ok = ok && mbar_wait(smem_u32(&ctl->o_full), 0, abort_flag);
-    tc_fence_after();
-    const bool aborted = *abort_flag != 0;
-    if (aborted) {
-      if (tid == 64) atomicExch(a.status, kStatusTimeout);
+    fence_proxy_async();
+    named_sync(1, kStagers);                                   // Q is in place for the MMAs
+
+    if (warp == 1 || warp == kThreads / 32 - 1) {
+      // ---------------------------------- MMA issuer of tile t (one thread) --------------------------
+      const int t = warp == 1 ? 0 : 1;
+      if (lane == 0 && (t == 0 || pair)) {
+        const uint32_t idesc_s = umma_idesc(kRows, kKeys, kFmt, 0, 0);
+        const uint32_t idesc_o = umma_idesc(kRows, kDh, kFmt, 0, 1);
+        // S_t(j) = Q_t K_j^T into its slot. P_t(j') of the slot's previous step lives there until
+        // PV_t(j') has read it, so QK_t(j) waits for that product to complete.
+        auto issue_qk = [&](int j) -> bool {
+          const int i = 2 * j, st = i % kStages;
+          if (!mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag)) return false;
+          const int prev = j - (pair ? 1 : 2);
+          if (prev >= 0) {
+            const Slot q = slot(t, prev);
+            if (!mbar_wait(smem_u32(&ctl->pv_done[q.bar]), q.phase & 1, abort_flag)) return false;
+          }
+          const Slot sl = slot(t, j);
+          tc_fence_after();
+          const uint32_t kt = s_ring + st * kTile, qt = s_q + t * kTile;
+#pragma unroll
+          for (int ks = 0; ks < kDh / 16; ++ks)
+            umma_f16(tmem + sl.bar * 256,
+                     umma_desc(qt + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128),
+                     umma_desc(kt + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128), idesc_s, ks > 0);
+          umma_commit(smem_u32(&ctl->s_full[sl.bar]));
+          return true;
+        };
+        // O_t += P_t V_j, P_t from tensor memory: 16 keys are 8 columns (two 16-bit values each); for
+        // bf16 the 16 keys of step ks are hi in columns 16 ks .. 16 ks + 7 and lo in the next 8
+        auto issue_pv = [&](int j) -> bool {
+          const int i = 2 * j + 1, st = i % kStages;
+          const Slot sl = slot(t, j);
+          if (!mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag) ||
+              !mbar_wait(smem_u32(&ctl->p_full[sl.bar]), sl.phase & 1, abort_flag))
+            return false;
+          tc_fence_after();
+          const uint32_t vt = s_ring + st * kTile, p_t = tmem + sl.bar * 256, o_t = tmem + t * 256 + 128;
+#pragma unroll
+          for (int ks = 0; ks < kKeys / 16; ++ks) {
+            const uint64_t vd = umma_desc(vt + ks * 2048, kBox, 1024, kSwizzle128);
+            if constexpr (kHiLo) {
+              umma_f16_ts(o_t, p_t + ks * 16, vd, idesc_o, (j | ks) != 0);
+              umma_f16_ts(o_t, p_t + ks * 16 + 8, vd, idesc_o, 1);
+            } else {
+              umma_f16_ts(o_t, p_t + ks * 8, vd, idesc_o, (j | ks) != 0);
+            }
+          }
+          umma_commit(smem_u32(&ctl->pv_done[sl.bar]));
+          return true;
+        };
+        // a ring stage is refilled after both issuers released it; with one tile, its issuer releases
+        // for both
+        auto release = [&](int i) {
+          umma_commit(smem_u32(&ctl->empty[i % kStages]));
+          if (!pair) umma_commit(smem_u32(&ctl->empty[i % kStages]));
+        };
+        bool ok = issue_qk(0);
+        if (ok) release(0);
+        for (int j = 0; j < nk[t] && ok; ++j) {
+          if (pair) {
+            // PV_t(j), then QK_t(j+1) (which waits for it)
+            ok = issue_pv(j);
+            if (!ok) break;
+            release(2 * j + 1);
+            if (j + 1 < nk[t]) {
+              ok = issue_qk(j + 1);
+              if (ok) release(2 * j + 2);
+            }
+          } else {
+            // one tile: QK(j+1) into the other slot before PV(j), so the softmax of j+1 follows j's
+            if (j + 1 < nk[t]) {
+              ok = issue_qk(j + 1);
+              if (!ok) break;
+              release(2 * j + 2);
+            }
+            ok = issue_pv(j);
+            if (ok) release(2 * j + 1);
+          }
+        }
+        // loads past this tile's keys (tile 0 may end a key tile before tile 1) still take this
+        // issuer's release, in order: wait until each is in place, then arrive
+        for (int i = 2 * nk[t]; i < 2 * nkt && ok; ++i) {
+          ok = mbar_wait(smem_u32(&ctl->full[i % kStages]), (i / kStages) & 1, abort_flag);
+          if (ok) mbar_arrive(smem_u32(&ctl->empty[i % kStages]));
+        }
+        umma_commit(smem_u32(&ctl->done[t]));
+        mbar_drain(smem_u32(&ctl->done[t]), 0);
+      }
     } else {
-      const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-      float* dst = row_ok ? a.out + ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh : nullptr;
-      const float inv = 1.f / l;
+      // ---------------------------------- softmax and epilogue of tile t ---------------------------
+      const int t = (warp - 2) / 4;
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;                        // this thread's query row (TMEM lane)
+      const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+      const uint32_t tmem_o = tmem + lane_base + t * 256 + 128;
+      const int gr = row0 + t * kRows + r;
+      const bool row_ok = gr < n_rows;
+      const int t_row = row_ok ? gr / a.G : 0;
+      const int last_key = s_b + t_row;                      // this row sees keys <= last_key
+      const int first_t = (row0 + t * kRows) / a.G;
+      const int unmasked_keys = s_b + first_t + 1;           // keys visible to every row of the tile
+      const float scale = kLog2e * rsqrtf(static_cast<float>(kDh));
+      constexpr float kSlack = 8.f;                          // P <= 2^kSlack before a rescale is forced
+      float m_ref = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nk[t] && ok; ++j) {
+        const Slot sl = slot(t, j);
+        const uint32_t tmem_s = tmem + lane_base + sl.bar * 256;
+        // warp-uniform waits: the tensor-memory loads and stores below are warp-collective
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full[sl.bar]), sl.phase & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        float v[kKeys];
+        tmem_ld128(tmem_s, v);
+        const int key0 = j * kKeys;
+        if ((j + 1) * kKeys > unmasked_keys || !row_ok) {      // diagonal tile (or padding row)
 #pragma unroll
-      for (int c = 0; c < kDh; c += 32) {
-        float ov[32];
-        tmem_ld32(tmem_o + c, ov);                             // warp-wide: every lane takes part
-        if (row_ok) {
+          for (int e = 0; e < kKeys; ++e)
+            if (!row_ok || key0 + e > last_key) v[e] = -INFINITY;
+        }
+        float mx[8];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + c + i) =
-                make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
+        for (int k = 0; k < 8; ++k) mx[k] = v[k];
+#pragma unroll
+        for (int e = 8; e < kKeys; ++e) mx[e & 7] = fmaxf(mx[e & 7], v[e]);
+        const float tmax = scale * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        // a new reference when this row's maximum passes the old one by more than kSlack
+        const bool bump = tmax > m_ref + kSlack;
+        const float m_new = bump ? tmax : m_ref;
+        const float alpha = bump ? ((m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new)) : 1.f;
+        l *= alpha;
+        m_ref = m_new;
+        const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;   // padding rows: every score is -inf
+        float ls[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+        // P_t over S_t: f16, keys 2w and 2w+1 in column w; bf16, the 16 keys of MMA step ks as 8 hi
+        // columns (16 ks ..) then 8 lo columns (16 ks + 8 ..)
+        constexpr int kGroup = kHiLo ? 16 : 32;                  // keys per 16-column store
+#pragma unroll
+        for (int g0 = 0; g0 < kKeys; g0 += kGroup) {
+          uint32_t w[16];
+#pragma unroll
+          for (int c8 = 0; c8 < kGroup / 8; ++c8) {
+            float p[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              p[e] = fast_exp2(fmaf(v[g0 + c8 * 8 + e], scale, neg_m));   // 0 for masked keys (-inf)
+              ls[e] += p[e];
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t hi = pack2<Tc>(p[2 * k], p[2 * k + 1]);
+              w[c8 * 4 + k] = hi;
+              if constexpr (kHiLo) {
+                const float2 h = unpack2<Tc>(hi);
+                w[8 + c8 * 4 + k] = pack2<Tc>(p[2 * k] - h.x, p[2 * k + 1] - h.y);
+              }
+            }
+          }
+          tmem_st16(tmem_s + (kHiLo ? g0 : g0 / 2), w);
+        }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        // O_t *= alpha once PV_t(j-1) is complete (with two tiles it is: QK_t(j) was issued after
+        // it); PV_t(j) waits for p_full, which follows these stores.
+        if (j > 0 && __any_sync(0xffffffffu, bump)) {
+          const Slot q = slot(t, j - 1);
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done[q.bar]), q.phase & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < kDh; c += 32) {
+            float ov[32];
+            tmem_ld32(tmem_o + c, ov);
+            uint32_t w[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(ov[e] * alpha);
+            tmem_st32(tmem_o + c, w);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[sl.bar]));
+      }
+      // ---- epilogue: O_t / l -------------------------------------------------------------------------
+      if (nk[t] > 0) {
+        const Slot q = slot(t, nk[t] - 1);
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->pv_done[q.bar]), q.phase & 1, abort_flag));
+        tc_fence_after();
+        const bool aborted = __any_sync(0xffffffffu, !ok || *abort_flag != 0);
+        if (aborted) {
+          if (tid == 64) atomicExch(a.status, kStatusTimeout);
+        } else {
+          const int tq = row_ok ? gr / a.G : 0, g = row_ok ? gr % a.G : 0;
+          float* dst = a.out + ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + tq) * kDh;
+          const float inv = 1.f / l;
+#pragma unroll
+          for (int c = 0; c < kDh; c += 32) {
+            float ov[32];
+            tmem_ld32(tmem_o + c, ov);                           // warp-wide: every lane takes part
+            if (row_ok) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(dst + c + i) =
+                    make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
+            }
+          }
         }
       }
     }
@@ -397,21 +524,21 @@ template <typename Tc>
 cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, const CUtensorMap* tv,
                 cudaStream_t st) {
   auto kern = prefill_tc_kernel<Tc>;
-  const size_t smem = prefill_smem<Tc>();
+  constexpr size_t smem = prefill_smem();
   cudaError_t e = ensure_smem_limit<prefill_tc_kernel<Tc>>(smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(p.n_units * a.H_kv), dim3(kThreads), smem, st, a, p, *tk, *tv);
 }
 
-static_assert(prefill_smem<__half>() > 114 * 1024 && prefill_smem<__nv_bfloat16>() > 114 * 1024,
-              "one CTA per SM: each holds all 512 TMEM columns");
-static_assert(prefill_smem<__half>() <= 227 * 1024 && prefill_smem<__nv_bfloat16>() <= 227 * 1024, "smem");
+static_assert(prefill_smem() > 114 * 1024, "one CTA per SM: each holds all 512 TMEM columns");
+static_assert(prefill_smem() <= 227 * 1024, "smem");
+static_assert(kThreads - 32 == 320, "the named barrier counts warps 1-10");
 
 }  // namespace
 
 bool prefill_tc_shape(kvc_dtype dt, int D, int* rows_per_tile) {
   if ((dt != KVC_F16 && dt != KVC_BF16) || D != kDh) return false;
-  *rows_per_tile = kRows;
+  *rows_per_tile = kUnitRows;
   return true;
 }
 

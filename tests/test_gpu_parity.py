@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import kvc_synth
-from oracle.kvc_oracle import OracleKVCache, full_recompute_attention, store_round, stored_to_f64
+from oracle.kvc_oracle import OracleKVCache, full_recompute_attention, gqa_cached_attention, store_round, stored_to_f64
 from tests.gpu_parity import Mirror, check_outputs
 
 pytestmark = pytest.mark.gpu
@@ -113,6 +113,9 @@ CASES = [
     ("f16", 128, 32, 8, 64, [5, 700]),         # 256 rows: two full row tiles
     ("bf16", 128, 16, 2, 17, [130, 0, 3]),     # G = 8, 136 rows: a ragged last tile
     ("f16", 128, 8, 8, 200, [0, 129]),         # G = 1, 200 rows, diagonal masking over many tiles
+    ("f16", 128, 32, 8, 64, [90, 1000]),       # the first 128 rows of a CTA end a key tile earlier
+    ("bf16", 128, 32, 8, 96, [10, 400]),       # 384 rows: the second CTA has one 128-row tile
+    ("f16", 128, 16, 4, 75, [0, 333]),         # 300 rows: the second CTA has one ragged tile
 ]
 
 
@@ -129,6 +132,37 @@ def test_attention_matches_oracle(dtype, d, Hq, Hkv, T, lengths):
         m.truncate(np.array(lengths))
     m.forward(T, Hq, what=f"{dtype} d={d} G={Hq // Hkv} T={T}")
     m.check_state()
+    m.close()
+
+
+@pytest.mark.parametrize("dtype,T", [("f16", 64), ("bf16", 96), ("bf16", 1), ("f16", 8)])
+def test_scores_growing_along_the_keys(dtype, T):
+    """Keys aligned with the queries and growing with position: every key tile's largest score passes
+    the previous tiles' by far, so a running softmax must rescale its partial output on every tile."""
+    import torch
+    from kv_cached_gqa_gb300 import _binding as kb
+    B, H, Hq, d = 2, 2, 8, 128
+    lengths = [700, 301]
+    n = max(lengths)
+    m = Mirror(L=1, B=B, H_kv=H, d_h=d, max_len=n + T + 8, dtype=dtype, seed=77)
+    pos = np.arange(n + T, dtype=np.float32)
+    k_all = (pos[None, None, :, None] / 32.0 + 0.3 * kvc_synth.normal_f32((B, H, n + T, d), 77, 1)).astype(np.float32)
+    v_all = kvc_synth.normal_f32((B, H, n + T, d), 77, 2)
+
+    def append(k, v):
+        m.ref.append(0, k, v)
+        kb.kvc_append(m.gpu, 0, m.dev(k), m.dev(v))
+
+    append(k_all[:, :, :n], v_all[:, :, :n])
+    m.commit()
+    m.truncate(np.array(lengths))
+    append(np.stack([k_all[b, :, s:s + T] for b, s in enumerate(lengths)]),
+           np.stack([v_all[b, :, s:s + T] for b, s in enumerate(lengths)]))
+    q = (1.0 + 0.3 * kvc_synth.normal_f32((B, Hq, T, d), 77, 3)).astype(np.float32)
+    want = gqa_cached_attention(m.ref, 0, q)
+    got = kb.gqa_cached_attn(m.gpu, m.dev(q), 0).cpu().numpy()
+    check_outputs(got, want, dtype, f"growing scores {dtype} T={T}")
+    torch.cuda.synchronize()
     m.close()
 
 
