@@ -401,12 +401,21 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       constexpr float kSlack = 8.f;                          // P <= 2^kSlack before a rescale is forced
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
+      // a warp whose 32 rows are all past the chunk (short chunks fill a tile partly) has nothing to
+      // compute: its lanes of S hold the scores of zero queries, 0, which read as P = 0, and its
+      // output rows are not stored; it only keeps the barrier protocol
+      const bool idle = __all_sync(0xffffffffu, !row_ok);
       for (int j = 0; j < nk[t] && ok; ++j) {
         const Slot sl = slot(t, j);
         const uint32_t tmem_s = tmem + lane_base + sl.bar * 256;
         // warp-uniform waits: the tensor-memory loads and stores below are warp-collective
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full[sl.bar]), sl.phase & 1, abort_flag));
         if (!ok) break;
+        if (idle) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[sl.bar]));
+          continue;
+        }
         tc_fence_after();
         float v[kKeys];
         tmem_ld128(tmem_s, v);
@@ -492,7 +501,7 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
         const bool aborted = __any_sync(0xffffffffu, !ok || *abort_flag != 0);
         if (aborted) {
           if (tid == 64) atomicExch(a.status, kStatusTimeout);
-        } else {
+        } else if (!idle) {
           const int tq = row_ok ? gr / a.G : 0, g = row_ok ? gr % a.G : 0;
           float* dst = a.out + ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + tq) * kDh;
           const float inv = 1.f / l;
