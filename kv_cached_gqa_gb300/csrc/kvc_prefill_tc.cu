@@ -53,7 +53,7 @@ constexpr int kCtlOff = kRingOff + kStages * kTile;
 
 struct __align__(8) PCtl {
   unsigned long long full[kStages], empty[kStages];
-  unsigned long long s_full[kTiles], p_full[kTiles], pv_done[kTiles];
+  unsigned long long s_full[kTiles], s_free[kTiles], p_full[kTiles], pv_done[kTiles];
   unsigned long long done[kTiles];
   uint32_t tmem;
   int abort;
@@ -185,6 +185,15 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const int b = plan.unit_b[unit] / plan.n_rowtiles;
   const int row0 = (plan.unit_b[unit] % plan.n_rowtiles) * kUnitRows;
   const int n_rows = a.T * a.G;
+  // rows of MMA tile t in this CTA, and its softmax warps that hold any (the others sit out: their
+  // lanes of S hold the scores of zero queries, 0, which read as P = 0, and their rows are not stored)
+  int rows_t[kTiles], warps_t[kTiles];
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    rows_t[t] = min(max(n_rows - (row0 + t * kRows), 0), kRows);
+    warps_t[t] = (rows_t[t] + 31) / 32;
+  }
+  const bool pair = rows_t[1] > 0;
 
   // ---- set-up ------------------------------------------------------------------------------------
   if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&ctl->tmem));
@@ -195,7 +204,10 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(smem_u32(&ctl->s_full[t]), 1);
-      mbar_init(smem_u32(&ctl->p_full[t]), kSoftmaxThreads / 32);
+      // arrivals: the softmax warps that hold rows (with one tile, both slots belong to tile 0)
+      const int arrivals = max(1, pair ? warps_t[t] : warps_t[0]);
+      mbar_init(smem_u32(&ctl->s_free[t]), arrivals);
+      mbar_init(smem_u32(&ctl->p_full[t]), arrivals);
       mbar_init(smem_u32(&ctl->pv_done[t]), 1);
     }
     for (int t = 0; t < kTiles; ++t) mbar_init(smem_u32(&ctl->done[t]), 1);
@@ -220,12 +232,23 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     nk[t] = last >= first ? (s_b + last / a.G + 1 + kKeys - 1) / kKeys : 0;
   }
   const int nkt = max(nk[0], nk[1]);
-  // Where step j of tile t keeps S / P and which barriers (s_full, p_full, pv_done) it uses. Two
-  // tiles: tile t's slot, the barriers' phase j. One tile: the two slots in turn (phase j / 2), so
-  // QK(j+1) need not wait for PV(j).
-  const bool pair = nk[1] > 0;
+  // Where step j of tile t keeps S and P, and which barriers it uses ({barrier, phase}).
+  //   Two tiles: S and P share tile t's first 128 columns (P over S once the scores are read); every
+  //   barrier of slot t, phase j. QK_t(j+1) waits for PV_t(j), which read P_t(j) from there.
+  //   One tile: S alternates between columns 0 and 256 (s_full / s_free of slot j & 1, phase j / 2)
+  //   and P has its own columns 384 .. 511 (f16: two 64-column buffers, j & 1; bf16: one 128-column
+  //   hi + lo buffer), with p_full / pv_done of its buffer. QK(j+1) then waits only until the softmax
+  //   has read S(j-1), and the softmax waits for the PV that last read its P buffer.
   struct Slot { int bar, phase; };
-  auto slot = [pair](int t, int j) -> Slot { return pair ? Slot{t, j} : Slot{j & 1, j >> 1}; };
+  auto s_slot = [pair](int t, int j) -> Slot { return pair ? Slot{t, j} : Slot{j & 1, j >> 1}; };
+  auto p_slot = [pair](int t, int j) -> Slot {
+    return pair ? Slot{t, j} : (kHiLo ? Slot{0, j} : Slot{j & 1, j >> 1});
+  };
+  auto s_col = [pair](int t, int j) -> uint32_t { return pair ? t * 256 : (j & 1) * 256; };
+  auto p_col = [pair](int t, int j) -> uint32_t {
+    return pair ? t * 256 : 384 + (kHiLo ? 0 : (j & 1) * 64);
+  };
+
 
   if (warp == 0) {
     // ---------------------------------- TMA producer (whole warp): K0, V0, K1, V1, ... -------------
@@ -307,17 +330,20 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
         auto issue_qk = [&](int j) -> bool {
           const int i = 2 * j, st = i % kStages;
           if (!mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag)) return false;
-          const int prev = j - (pair ? 1 : 2);
-          if (prev >= 0) {
-            const Slot q = slot(t, prev);
+          if (pair && j > 0) {                                 // P_t(j-1) over S_t: PV_t(j-1) read it
+            const Slot q = p_slot(t, j - 1);
             if (!mbar_wait(smem_u32(&ctl->pv_done[q.bar]), q.phase & 1, abort_flag)) return false;
           }
-          const Slot sl = slot(t, j);
+          if (!pair && j > 1) {                                // the softmax has read S(j-2)
+            const Slot q = s_slot(t, j - 2);
+            if (!mbar_wait(smem_u32(&ctl->s_free[q.bar]), q.phase & 1, abort_flag)) return false;
+          }
+          const Slot sl = s_slot(t, j);
           tc_fence_after();
           const uint32_t kt = s_ring + st * kTile, qt = s_q + t * kTile;
 #pragma unroll
           for (int ks = 0; ks < kDh / 16; ++ks)
-            umma_f16(tmem + sl.bar * 256,
+            umma_f16(tmem + s_col(t, j),
                      umma_desc(qt + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128),
                      umma_desc(kt + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024, kSwizzle128), idesc_s, ks > 0);
           umma_commit(smem_u32(&ctl->s_full[sl.bar]));
@@ -327,12 +353,12 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
         // bf16 the 16 keys of step ks are hi in columns 16 ks .. 16 ks + 7 and lo in the next 8
         auto issue_pv = [&](int j) -> bool {
           const int i = 2 * j + 1, st = i % kStages;
-          const Slot sl = slot(t, j);
+          const Slot sl = p_slot(t, j);
           if (!mbar_wait(smem_u32(&ctl->full[st]), (i / kStages) & 1, abort_flag) ||
               !mbar_wait(smem_u32(&ctl->p_full[sl.bar]), sl.phase & 1, abort_flag))
             return false;
           tc_fence_after();
-          const uint32_t vt = s_ring + st * kTile, p_t = tmem + sl.bar * 256, o_t = tmem + t * 256 + 128;
+          const uint32_t vt = s_ring + st * kTile, p_t = tmem + p_col(t, j), o_t = tmem + t * 256 + 128;
 #pragma unroll
           for (int ks = 0; ks < kKeys / 16; ++ks) {
             const uint64_t vd = umma_desc(vt + ks * 2048, kBox, 1024, kSwizzle128);
@@ -401,24 +427,21 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       constexpr float kSlack = 8.f;                          // P <= 2^kSlack before a rescale is forced
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
-      // a warp whose 32 rows are all past the chunk (short chunks fill a tile partly) has nothing to
-      // compute: its lanes of S hold the scores of zero queries, 0, which read as P = 0, and its
-      // output rows are not stored; it only keeps the barrier protocol
-      const bool idle = __all_sync(0xffffffffu, !row_ok);
-      for (int j = 0; j < nk[t] && ok; ++j) {
-        const Slot sl = slot(t, j);
-        const uint32_t tmem_s = tmem + lane_base + sl.bar * 256;
+      const bool idle = quad >= warps_t[t];                  // no row of this warp is in the chunk
+      for (int j = 0; j < nk[t] && ok && !idle; ++j) {
+        const Slot sl = s_slot(t, j), pl = p_slot(t, j);
+        const uint32_t tmem_s = tmem + lane_base + s_col(t, j), tmem_p = tmem + lane_base + p_col(t, j);
         // warp-uniform waits: the tensor-memory loads and stores below are warp-collective
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full[sl.bar]), sl.phase & 1, abort_flag));
         if (!ok) break;
-        if (idle) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[sl.bar]));
-          continue;
-        }
         tc_fence_after();
         float v[kKeys];
         tmem_ld128(tmem_s, v);
+        if (!pair) {                                           // S(j) is read: QK(j+2) may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free[sl.bar]));
+        }
         const int key0 = j * kKeys;
         if ((j + 1) * kKeys > unmasked_keys || !row_ok) {      // diagonal tile (or padding row)
 #pragma unroll
@@ -439,6 +462,14 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
         l *= alpha;
         m_ref = m_new;
         const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;   // padding rows: every score is -inf
+        if (!pair && j >= (kHiLo ? 1 : 2)) {                   // one tile: the PV that last read this
+          const Slot q = p_slot(t, j - (kHiLo ? 1 : 2));      // P buffer is complete
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done[q.bar]), q.phase & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         float ls[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) ls[k] = 0.f;
@@ -466,13 +497,13 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
               }
             }
           }
-          tmem_st16(tmem_s + (kHiLo ? g0 : g0 / 2), w);
+          tmem_st16(tmem_p + (kHiLo ? g0 : g0 / 2), w);
         }
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         // O_t *= alpha once PV_t(j-1) is complete (with two tiles it is: QK_t(j) was issued after
         // it); PV_t(j) waits for p_full, which follows these stores.
         if (j > 0 && __any_sync(0xffffffffu, bump)) {
-          const Slot q = slot(t, j - 1);
+          const Slot q = p_slot(t, j - 1);
           if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done[q.bar]), q.phase & 1, abort_flag))) {
             ok = false;
             break;
@@ -491,17 +522,17 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[sl.bar]));
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[pl.bar]));
       }
       // ---- epilogue: O_t / l -------------------------------------------------------------------------
-      if (nk[t] > 0) {
-        const Slot q = slot(t, nk[t] - 1);
+      if (nk[t] > 0 && !idle) {
+        const Slot q = p_slot(t, nk[t] - 1);
         ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&ctl->pv_done[q.bar]), q.phase & 1, abort_flag));
         tc_fence_after();
         const bool aborted = __any_sync(0xffffffffu, !ok || *abort_flag != 0);
         if (aborted) {
-          if (tid == 64) atomicExch(a.status, kStatusTimeout);
-        } else if (!idle) {
+          if (lane == 0) atomicExch(a.status, kStatusTimeout);
+        } else {
           const int tq = row_ok ? gr / a.G : 0, g = row_ok ? gr % a.G : 0;
           float* dst = a.out + ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + tq) * kDh;
           const float inv = 1.f / l;
