@@ -12,7 +12,9 @@
 //   O_t [128 rows x 128 d   ] += P_t . V_j     A = P_t (tensor memory), B = V tile (MN-major)
 // Tensor memory (512 columns) holds, per tile t, S_t in 128 columns and O_t in the next 128. Each
 // softmax thread overwrites its row of S_t with P_t in 16-bit form once it has read the scores, and
-// the PV product takes P_t straight from there, so P never passes through shared memory.
+// the PV product takes P_t straight from there, so P never passes through shared memory. A CTA with
+// one tile (short chunks, ragged tails) uses the free half differently: S alternates between two
+// slots and P has columns of its own, so QK(j+1) need not wait for PV(j) (see s_slot below).
 // Roles (352 threads, one CTA per SM):
 //   warp 0      TMA: K_j and V_j tiles through a ring;
 //   warps 1, 10 one thread each issues the MMAs of tile 0 and of tile 1: PV_t(j), then QK_t(j+1),
