@@ -251,7 +251,6 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     return pair ? t * 256 : 384 + (kHiLo ? 0 : (j & 1) * 64);
   };
 
-
   if (warp == 0) {
     // ---------------------------------- TMA producer (whole warp): K0, V0, K1, V1, ... -------------
     if (lane == 0) {
