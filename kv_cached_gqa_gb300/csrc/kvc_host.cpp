@@ -287,8 +287,9 @@ bool encode_store_map(CUtensorMap* map, void* base, kvc_dtype dt, int D, int max
 
 // ---- kernel choice and work plan ------------------------------------------------------------------
 // Tensor cores serve 16-bit caches with d_h = 128: the split decode kernel for up to 16 query rows
-// per K/V head, the chunk kernel beyond that (verify chunks and prefill). Everything else runs on
-// the CUDA-core split-K kernel. For the split kernels, the total key work W = H_kv * sum_u n_u (n_u =
+// per K/V head; beyond that the chunk kernels, the one-CTA-per-SM form for up to 128 rows (verify
+// chunks, one CTA per (sequence, K/V head)) and the two-CTAs-per-SM form with split keys for longer
+// chunks (prefill). Everything else runs on the CUDA-core split-K kernel. For the split kernels, the total key work W = H_kv * sum_u n_u (n_u =
 // keys visible to unit u) is cut into about k waves of resident CTAs (two per SM); each unit's keys
 // are split into near-equal chunks of about W / (k * slots) keys, at most what one CTA can hold, and
 // units are ordered longest chunk first so the hardware scheduler packs the last wave tightly.
@@ -300,7 +301,13 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
   if (h->has_tc && decode_tc_shape(h->dtype, h->D, R, &rpt, &tile, &max_tiles)) {
     kind = AttnKernel::DecodeTC;
   } else if (h->has_tc && R > 16 && prefill_tc_shape(h->dtype, h->D, &rpt)) {
-    kind = AttnKernel::PrefillTC;
+    if (R <= rpt) {
+      kind = AttnKernel::ChunkTC;
+    } else {
+      kind = AttnKernel::PrefillTC;                         // 128-row units; its online softmax
+      tile = 128;                                           // takes any split length
+      max_tiles = 1 << 16;
+    }
   } else {
     if (!splitk_shape(h->dtype, h->D, R, &rpt, &tile)) {
       *err = "no attention kernel for this d_h";
@@ -334,7 +341,7 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
   auto longest_first = [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; };
   out->kernel = kind;
   out->rows_per_tile = rpt;
-  if (kind == AttnKernel::PrefillTC) {
+  if (kind == AttnKernel::ChunkTC) {
     // one CTA per (unit, K/V head). Longest sequences first, and a sequence's row tiles together
     // (longest tile first): the CTAs resident at any time then share a few sequences' K/V, which
     // stays in L2 instead of being re-read from HBM by each row tile
@@ -425,6 +432,7 @@ cudaError_t launch_attention(const AttnPlan& ap, const AttnArgs& a, const SplitP
                              cudaStream_t st) {
   switch (ap.kernel) {
     case AttnKernel::DecodeTC: return launch_decode_tc(a, p, &h->tmap_k_tc, &h->tmap_v_tc, st);
+    case AttnKernel::ChunkTC: return launch_chunk_tc(a, p, &h->tmap_k_tc, &h->tmap_v_tc, st);
     case AttnKernel::PrefillTC: return launch_prefill_tc(a, p, &h->tmap_k_tc, &h->tmap_v_tc, st);
     case AttnKernel::SplitK: return launch_splitk(a, p, &h->tmap_k_split, &h->tmap_v_split, st);
   }

@@ -146,8 +146,12 @@ bool decode_tc_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* til
 cudaError_t launch_decode_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
                              const CUtensorMap* tv, cudaStream_t st);
 
-// Tensor-core chunk (prefill) kernel: 16-bit caches, d_h = 128, 128 query rows per CTA.
+// Tensor-core chunk kernels: 16-bit caches, d_h = 128, 128 query rows per CTA. launch_chunk_tc:
+// at most 128 rows per K/V head (one CTA per (sequence, K/V head), one per SM); launch_prefill_tc:
+// units of 128 rows, keys split over CTAs as the split planner cuts them, two CTAs per SM.
 bool prefill_tc_shape(kvc_dtype dt, int D, int* rows_per_tile);
+cudaError_t launch_chunk_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
+                            const CUtensorMap* tv, cudaStream_t st);
 cudaError_t launch_prefill_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
                               const CUtensorMap* tv, cudaStream_t st);
 
@@ -180,7 +184,7 @@ cudaError_t launch_mla_tc(const MlaArgs& a, const SplitPlan& p, const CUtensorMa
                           cudaStream_t st);
 
 // Which attention kernel serves a call, and its work plan (built from the host mirror of the lengths).
-enum class AttnKernel { SplitK, DecodeTC, PrefillTC };
+enum class AttnKernel { SplitK, DecodeTC, ChunkTC, PrefillTC };
 struct AttnPlan {
   AttnKernel kernel;
   int rows_per_tile;
