@@ -406,7 +406,18 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
     nsplit[u] = splits_for(n_eff[u], w, &chunk);             // whole tiles, as the kernels recompute it
     order[u] = {chunk, u};
   }
-  std::stable_sort(order.begin(), order.end(), longest_first);
+  if (kind == AttnKernel::PrefillTC) {
+    // a sequence's row tiles together (longest sequences first, then longest chunk): the CTAs
+    // resident at a time then read a few sequences' K/V, which stays in L2 for all their row tiles
+    std::stable_sort(order.begin(), order.end(), [&](const std::pair<int, int>& x, const std::pair<int, int>& y) {
+      const int bx = x.second / n_rt, by = y.second / n_rt;
+      if (h->lens[bx] != h->lens[by]) return h->lens[bx] > h->lens[by];
+      if (bx != by) return bx < by;
+      return x.first > y.first;
+    });
+  } else {
+    std::stable_sort(order.begin(), order.end(), longest_first);
+  }
   long long items = 0;
   int max_chunk = 0;
   plan->prefix[0] = 0;
