@@ -327,7 +327,9 @@ def attention_kernel_name(sp):
     if tc_decode:
         return "gqa_cached_attn (decode_tc_kernel: tcgen05 split-K attention with fused merge)"
     if sp.dtype in ("f16", "bf16") and sp.d_h == 128:
-        return "gqa_cached_attn (prefill_tc_kernel: tcgen05 chunk attention)"
+        if rows <= 128:
+            return "gqa_cached_attn (prefill_tc_kernel: tcgen05 chunk attention, wide form, one CTA per SM)"
+        return "gqa_cached_attn (prefill_tc_kernel: tcgen05 chunk attention, narrow form, two CTAs per SM, split keys)"
     return "gqa_cached_attn (splitk_kernel: CUDA-core split-K attention)"
 
 
