@@ -273,6 +273,10 @@ int kvc_layer_ptrs(kvc_handle h, int layer, void** k_dev, void** v_dev);
  * (kvc_append(layer, ...) with the same T since the last commit/truncate), else KVC_E_STATE.
  * The library keeps a device workspace for partial results and grows it (stream-ordered
  * cudaMallocAsync) the first time a larger one is needed.
+ * Limits: the work plan holds at most 2048 (sequence, row tile) units, where a row tile is at most
+ * 16 packed query rows (t, g) on the decode and CUDA-core kernels and 128 on the tensor-core chunk
+ * kernel (16-bit caches, d_h = 128, G * T > 16: B * ceil(G * T / 128) <= 2048 there); beyond,
+ * KVC_E_UNSUPPORTED.
  */
 int gqa_cached_attn(kvc_handle h, const void* q_dev, kvc_dtype q_dtype, int layer, int s, int T,
                     int H_q, float* out_dev, void* stream);
