@@ -287,6 +287,25 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(values, device):
+    """Each value's maximum over the job's ranks (the slowest rank's time), in one all_reduce; the
+    values themselves when the job has one rank or no process group."""
+    import torch
+    import torch.distributed as dist
+    values = [float(v) for v in values]
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return values
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_rate(units_per_rank, ms, world):
+    """Whole-job rate: the units every rank processed (each runs its own replica of the workload)
+    per second of the slowest rank's time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -451,13 +470,7 @@ def run_ours(args):
         del g2
     attn_ms = [ev[l][0].elapsed_time(ev[l][1]) for ev in events for l in range(0, sp.L, TIMED_EVERY)]
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    if world > 1:
-        t = torch.tensor([ms, attn_avg_ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, attn_avg_ms = float(t[0]), float(t[1])
-        t = torch.tensor([graph_ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        graph_ms = float(t[0])
+    ms, attn_avg_ms, graph_ms = max_over_ranks([ms, attn_avg_ms, graph_ms], f"cuda:{local}")
 
     # end to end through the public API with host buffers: every step copies every layer's inputs in
     # from pinned host memory and reads every layer's output back, inside the timed region. The copies
@@ -509,14 +522,10 @@ def run_ours(args):
             e2e_step()
         t1.record(stream)
         barrier()
-        e2e_ms = t0.elapsed_time(t1) / args.steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=f"cuda:{local}")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t[0])
-        e2e = {"value": round(world * sp.step_bytes() / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e_ms, = max_over_ranks([t0.elapsed_time(t1) / args.steps], f"cuda:{local}")
+        e2e = {"value": round(job_rate(sp.step_bytes(), e2e_ms, world) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps_per_s": round(world * 1e3 / e2e_ms, 3)}
+               "steps_per_s": round(job_rate(1, e2e_ms, world), 3)}
     kb.kvc_status(wl.cache)
 
     if rank != 0:
@@ -527,7 +536,7 @@ def run_ours(args):
         return 0
     peak, peak_kind = measured_peaks()
     attn_gbs = sp.attn_bytes() / (attn_avg_ms * 1e-3) / 1e9
-    value = world * sp.step_bytes() / (ms * 1e-3) / 1e9
+    value = job_rate(sp.step_bytes(), ms, world) / 1e9
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline_entry(args.workload, args.cpu_sample_seconds)
@@ -539,9 +548,9 @@ def run_ours(args):
         "data": "synthetic (seeded Philox draws; approximately N(0,1))",
         "config": dict(workload_config(sp, None if not args.layers else "PROFILING CASE: fewer layers, not a bench line"),
                        graph=bool(args.graph)),
-        "steps_per_s": round(world * 1e3 / ms, 3),
-        "graph_replay": {"value": round(world * sp.step_bytes() / (graph_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                         "ms_per_step": round(graph_ms, 4), "steps_per_s": round(world * 1e3 / graph_ms, 3),
+        "steps_per_s": round(job_rate(1, ms, world), 3),
+        "graph_replay": {"value": round(job_rate(sp.step_bytes(), graph_ms, world) / 1e9, 2), "unit": "GB/s",
+                         "ms_per_step": round(graph_ms, 4), "steps_per_s": round(job_rate(1, graph_ms, world), 3),
                          "note": "the same step captured once in a CUDA graph and replayed (no host launches)"},
         "pct_of_peak": {"measured_hbm": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / 8000.0, 2)},
