@@ -30,7 +30,7 @@ It computes the plain definitions, in float64, one (sequence, head) at a time:
   attend ("KV cache decoding", "Position information with a cache"; the formula is the RoFormer
   paper's, which the pages name but do not print).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent (the library follows the same ones):
 * rounding to float16/bfloat16 is round-to-nearest-even; NaN inputs are out of scope;
 * a query for a 16-bit cache is rounded to the cache dtype before use;
 * `commit` is explicit and requires every layer's fill to agree per sequence;

@@ -277,49 +277,45 @@ def test_tiny_decoder_cached_vs_uncached_logits():
     margin is below 1e-4 ("Generation and the KV Cache", verify_cache's margin gate)."""
     import torch
     from kv_cached_gqa_gb300 import _binding as kb
-    from oracle.tiny_decoder import TinyDecoder, generate_with_cache
+    from oracle.tiny_decoder import DecoderShape, build_tiny_decoder, decoder_logits, greedy
     w = kvc_synth.WORKLOADS["tiny-decoder-fp32"]
-    model = TinyDecoder(w["vocab"], w["d_model"], w["n_heads"], w["n_layers"], w["max_len"], seed=w["seed"],
-                        init="baseline", cache_dtype="f32")
+    shape = DecoderShape(w["vocab"], w["d_model"], w["n_heads"], w["n_layers"], w["max_len"])
+    model = build_tiny_decoder(shape, seed=w["seed"], init="baseline", cache_dtype="f32")
     prompt = kvc_synth.prompt_ids(w["prompt"], w["vocab"], w["seed"])
-    ids_ref, logits_ref, _ = generate_with_cache(model, prompt, w["new_tokens"])
-    uncached = np.array([model.forward(ids_ref[:len(prompt) + i])[-1] for i in range(w["new_tokens"])])
+    n_new, P = w["new_tokens"], len(prompt)
+    ids_ref, logits_ref, _ = greedy(model, prompt, n_new, use_cache=True)
+    uncached = np.stack([decoder_logits(shape, model.weights, ids_ref[:P + i])[-1] for i in range(n_new)])
     assert np.abs(uncached - logits_ref).max() < 1e-5          # the oracle's own two paths agree
 
-    dev = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float32)).cuda()
-    P = {k: dev(getattr(model, k)) for k in ("tok_emb", "pos_emb", "g_out", "b_out", "w_out")}
-    layers = [{k: dev(v) for k, v in p.items()} for p in model.layers]
-    H, dh, dm = model.n_heads, model.d_head, model.d_model
-    cache = kb.Cache(model.n_layers, 1, H, dh, model.max_len, 0)
+    wt = {k: torch.from_numpy(np.asarray(v, dtype=np.float32)).cuda() for k, v in vars(model.weights).items()}
+    H, dh, dm = shape.n_heads, shape.d_head, shape.d_model
+    cache = kb.Cache(shape.n_layers, 1, H, dh, shape.max_len, 0)
+    norm = lambda x, g, b: torch.nn.functional.layer_norm(x, (dm,), g, b, eps=1e-5)
+    as_heads = lambda y: y.view(-1, H, dh).permute(1, 0, 2).unsqueeze(0).contiguous()   # [1, H, m, dh]
 
-    def ln(x, g, b):
-        return torch.nn.functional.layer_norm(x, (dm,), g, b, eps=1e-5)
-
-    def forward(ids):
+    def run(ids):
         t = kb.kvc_seq_len(cache)[0]
-        m_ = len(ids)
-        x = P["tok_emb"][torch.tensor(ids, device="cuda")] + P["pos_emb"][t:t + m_]
-        for i, p in enumerate(layers):
-            h = ln(x, p["g1"], p["b1"])
-            split = lambda y: y.reshape(m_, H, dh).transpose(0, 1).unsqueeze(0).contiguous()
-            q, k, v = split(h @ p["w_q"]), split(h @ p["w_k"]), split(h @ p["w_v"])
-            kb.kvc_append(cache, i, k, v)
-            heads = kb.gqa_cached_attn(cache, q, i)                       # [1, H, m, dh]
-            x = x + heads[0].transpose(0, 1).reshape(m_, dm) @ p["w_o"]
-            h = ln(x, p["g2"], p["b2"])
-            x = x + torch.relu(h @ p["w_1"]) @ p["w_2"]
+        x = wt["token_table"][torch.tensor(ids, device="cuda")] + wt["position_table"][t:t + len(ids)]
+        for layer in range(shape.n_layers):
+            a = norm(x, wt["norm_gain"][layer, 0], wt["norm_bias"][layer, 0])
+            q, k, v = (as_heads(a @ wt["w_qkv"][layer, n]) for n in range(3))
+            kb.kvc_append(cache, layer, k, v)
+            o = kb.gqa_cached_attn(cache, q, layer)                        # [1, H, m, dh]
+            x = x + o[0].permute(1, 0, 2).reshape(-1, dm) @ wt["w_mix"][layer]
+            b = norm(x, wt["norm_gain"][layer, 1], wt["norm_bias"][layer, 1])
+            x = x + torch.relu(b @ wt["w_up"][layer]) @ wt["w_down"][layer]
         kb.kvc_commit(cache)
-        return (ln(x, P["g_out"], P["b_out"]) @ P["w_out"]).double().cpu().numpy()
+        return (norm(x, wt["final_gain"], wt["final_bias"]) @ wt["w_vocab"]).double().cpu().numpy()
 
-    new = list(prompt)
-    for step in range(w["new_tokens"]):                  # teacher-forced on the oracle's ids
-        got = forward(new)[-1]
+    feed = list(prompt)
+    for step in range(n_new):                            # teacher-forced on the oracle's ids
+        got = run(feed)[-1]
         assert np.abs(got - logits_ref[step]).max() <= 1e-5, step
         top2 = np.sort(logits_ref[step])[-2:]
         if top2[1] - top2[0] >= 1e-4:
-            assert int(np.argmax(got)) == ids_ref[len(prompt) + step]
-        new = [ids_ref[len(prompt) + step]]
-    assert kb.kvc_seq_len(cache) == [len(prompt) + w["new_tokens"] - 1]
+            assert int(np.argmax(got)) == ids_ref[P + step]
+        feed = [ids_ref[P + step]]
+    assert kb.kvc_seq_len(cache) == [P + n_new - 1]
     cache.close()
 
 

@@ -12,7 +12,7 @@ import pytest
 import kvc_synth
 from oracle.kvc_oracle import (OracleKVCache, attend, full_recompute_attention, gqa_cached_attention,
                                kv_bytes, offset_causal_mask, store_round, stored_to_f64)
-from oracle.tiny_decoder import TinyDecoder, generate_no_cache, generate_with_cache
+from oracle.tiny_decoder import DecoderShape, build_tiny_decoder, greedy
 from tests.conftest import golden
 
 
@@ -85,7 +85,7 @@ def test_mask_special_cases_and_counts():
         np.testing.assert_array_equal(offset_causal_mask(T, 0), np.tril(np.ones((T, T), bool)))
     for s in range(0, 40):
         assert offset_causal_mask(1, s).all()
-    # the construction of the TinyDecoder listing, tril(ones(m, t + m), k=t), is the same mask
+    # the same mask as a lower triangle shifted right by s (the diagonal moves by the cache length)
     for T in range(1, 7):
         for s in range(0, 9):
             np.testing.assert_array_equal(offset_causal_mask(T, s), np.tril(np.ones((T, s + T), bool), k=s))
@@ -364,55 +364,75 @@ def test_ragged_lengths_each_sequence_writes_at_its_own_position():
     np.testing.assert_array_equal(c.positions(2), [[3, 4], [7, 8], [1, 2]])
 
 
-# -- the tiny decoder self-check ("KV cache decoding", the listing's main block) -------------------
+# -- the tiny decoder ("KV cache decoding": "Correctness tests", "Prefill and decode") ---------------
 
 @pytest.fixture(scope="module")
 def tiny_runs():
+    """The page's experiment: a 48-id prompt, 160 greedy ids, without and then with the cache."""
     g = golden("work_counters.json")
-    m = TinyDecoder(**g["model"])
+    model = build_tiny_decoder(DecoderShape(**g["model"]))
     prompt = kvc_synth.prompt_ids(g["P"], g["model"]["vocab"], 1)
-    ids_a, logits_a = generate_no_cache(m, prompt, g["N"])
-    pos_a, sc_a = m.positions, m.scores
-    m.positions = m.scores = 0
-    ids_b, logits_b, cache = generate_with_cache(m, prompt, g["N"])
-    return g, m, prompt, (ids_a, logits_a, pos_a, sc_a), (ids_b, logits_b, m.positions, m.scores, cache)
+    runs = {}
+    for use_cache in (False, True):
+        model.tally.positions = model.tally.scores = 0
+        seq, logits, cache = greedy(model, prompt, g["N"], use_cache)
+        runs[use_cache] = dict(seq=seq, logits=logits, cache=cache,
+                               positions=model.tally.positions, scores=model.tally.scores)
+    return g, model, prompt, runs
 
 
 def test_tiny_decoder_equality_and_counters(tiny_runs):
-    g, m, prompt, (ids_a, la, pos_a, sc_a), (ids_b, lb, pos_b, sc_b, cache) = tiny_runs
-    assert ids_a == ids_b
-    assert np.abs(la - lb).max() < g["gap_bound"]
-    assert np.ptp(la) > 1.0                                    # the logits are not all near zero
-    assert (sc_a, sc_b) == (g["scores_uncached"], g["scores_cached"])
-    assert (pos_a, pos_b) == (g["positions_uncached"], g["positions_cached"])
+    g, model, prompt, runs = tiny_runs
+    plain, cached = runs[False], runs[True]
+    assert plain["seq"] == cached["seq"]
+    assert np.abs(plain["logits"] - cached["logits"]).max() < g["gap_bound"]
+    assert np.ptp(plain["logits"]) > 1.0                      # the logits are not all near zero
+    # the page's printed counts for this run
+    assert (plain["scores"], cached["scores"]) == (g["scores_uncached"], g["scores_cached"])
+    assert (plain["positions"], cached["positions"]) == (g["positions_uncached"], g["positions_cached"])
+    # and the closed forms behind them, for the page's larger example too
     P, N = g["large"]["P"], g["large"]["N"]
-    assert sum(P + i for i in range(N)) == g["large"]["positions_uncached"]
+    assert N * P + N * (N - 1) // 2 == g["large"]["positions_uncached"]
     assert P + N - 1 == g["large"]["positions_cached"]
 
 
 def test_tiny_decoder_cache_state(tiny_runs):
-    g, m, prompt, _, (_, _, _, _, cache) = tiny_runs
-    L, H, D = m.n_layers, m.n_heads, m.d_head
-    assert cache.k.shape == (L, 1, H, m.max_len, D)
-    assert cache.committed()[0] == g["P"] + g["N"] - 1           # the last sampled token is not fed
-    assert cache.filled_bytes() == kv_bytes(L, H, D, int(cache.committed()[0]), bytes_per_value=8)
-    assert np.all(cache.k[:, :, :, cache.committed()[0]:] == 0.0)
+    g, model, prompt, runs = tiny_runs
+    cache, s = runs[True]["cache"], model.shape
+    assert cache.k.shape == (s.n_layers, 1, s.n_heads, s.max_len, s.d_head)
+    filled = int(cache.committed()[0])
+    assert filled == g["P"] + g["N"] - 1                      # the id picked last was never run
+    assert cache.filled_bytes() == kv_bytes(s.n_layers, s.n_heads, s.d_head, filled, bytes_per_value=8)
+    assert not cache.k[:, :, :, filled:].any() and not cache.v[:, :, :, filled:].any()
 
 
-def test_tiny_decoder_causality_and_prefill_chunking(tiny_runs):
-    g, m, prompt, (ids_a, la, _, _), _ = tiny_runs
-    P = g["P"]
-    short, long_ = m.new_cache(), m.new_cache()
-    m.forward(ids_a[:P], short)
-    m.forward(ids_a[:P + 20], long_)
-    np.testing.assert_array_equal(short.k[:, :, :, :P], long_.k[:, :, :, :P])
-    np.testing.assert_array_equal(short.v[:, :, :, :P], long_.v[:, :, :, :P])
-    one, chunked = m.new_cache(), m.new_cache()
-    for tok in prompt:
-        last = m.forward([tok], one)[-1]
-    m.forward(prompt[:30], chunked)
-    last_chunked = m.forward(prompt[30:], chunked)[-1]
-    for other, logits in ((one, last), (chunked, last_chunked)):
-        assert other.committed()[0] == P
-        assert np.allclose(other.k, short.k, atol=1e-12) and np.allclose(other.v, short.v, atol=1e-12)
-        assert np.allclose(logits, la[0], atol=1e-9)
+def test_tiny_decoder_rows_of_a_prefix_ignore_later_tokens(tiny_runs):
+    """A position's stored key and value are the same whether 0 or 20 tokens follow it
+    ("Why the causal mask makes caching exact")."""
+    g, model, prompt, runs = tiny_runs
+    P, seq = g["P"], runs[False]["seq"]
+    stores = []
+    for extra in (0, 20):
+        cache = model.new_cache()
+        model(seq[:P + extra], cache)
+        stores.append(cache)
+    for a, b in ((stores[0].k, stores[1].k), (stores[0].v, stores[1].v)):
+        assert np.abs(a[..., :P, :] - b[..., :P, :]).max() <= 1e-12
+
+
+@pytest.mark.parametrize("pieces", [[30, 18], [1] * 48, [7, 1, 23, 17], [47, 1]])
+def test_tiny_decoder_prompt_in_pieces(tiny_runs, pieces):
+    """Running the prompt in consecutive pieces fills the same cache, and its last piece gives the
+    same last-row logits, as one pass over the whole prompt ("Prefill and decode"; the page checks
+    30 + 18 and one id at a time, the other splits put several ids on a non-empty cache too)."""
+    g, model, prompt, runs = tiny_runs
+    whole = model.new_cache()
+    model(prompt, whole)
+    split = model.new_cache()
+    start = 0
+    for n in pieces:
+        last = model(prompt[start:start + n], split)[-1]
+        start += n
+    assert start == g["P"] == int(split.committed()[0])
+    assert np.abs(split.k - whole.k).max() <= 1e-12 and np.abs(split.v - whole.v).max() <= 1e-12
+    assert np.abs(last - runs[False]["logits"][0]).max() <= 1e-9
