@@ -278,6 +278,16 @@ class OracleKVCache:
         self.fill[:, :] = n[None, :]
         self.lens = n
 
+    def set_lengths(self, n) -> None:
+        """Set every layer's fill and the committed length to n_b, growing or shrinking, without writing
+        a row: positions [0, n_b) then hold whatever the store holds there (zeros never written, rows a
+        truncate left behind). Lengths are bookkeeping only (§2.3; §2.4: nothing is copied)."""
+        n = np.broadcast_to(np.asarray(n, dtype=np.int64), (self.B,)).copy()
+        if np.any(n < 0) or np.any(n > self.max_len):
+            raise ValueError("length outside [0, max_len]")
+        self.fill[:, :] = n[None, :]
+        self.lens = n
+
     # -- sizes -----------------------------------------------------------------------------
     def nbytes(self) -> int:
         """Capacity: 2 * L * B * H_kv * max_len * d_h * itemsize (§2.5)."""
@@ -577,6 +587,7 @@ class OracleLatentCache:
     positions = OracleKVCache.positions
     commit = OracleKVCache.commit
     truncate = OracleKVCache.truncate
+    set_lengths = OracleKVCache.set_lengths
 
     def append(self, layer: int, c_new, kr_new):
         """Write a [B, T, r] latent chunk and a [B, T, d_R] RoPE-key chunk at each sequence's fill;

@@ -233,3 +233,29 @@ def test_mla_without_the_rope_key_term_is_caught(monkeypatch):
 
     monkeypatch.setattr(latent_pins, "mla_cached_attention", mla_no_rope)
     _fails(latent_pins.test_absorbed_mla_equals_explicit_per_head_projections, 1, [7, 0, 12])
+
+
+def test_set_lengths_moving_only_the_committed_length_is_caught(monkeypatch):
+    """set_lengths that leaves the per-layer fills where they were: the next append writes at the old
+    fill, not at the new length."""
+    def set_lengths_committed_only(self, n):
+        self.lens = np.broadcast_to(np.asarray(n, dtype=np.int64), (self.B,)).copy()
+
+    monkeypatch.setattr(ko.OracleKVCache, "set_lengths", set_lengths_committed_only)
+    _fails(pins.test_set_lengths_over_zero_rows_matches_the_closed_form)
+
+
+def test_set_lengths_that_zeroes_the_rows_it_uncovers_is_caught(monkeypatch):
+    """set_lengths that clears the rows it declares filled (as if they were new) loses what a truncate
+    left behind."""
+    orig = ko.OracleKVCache.set_lengths
+
+    def set_lengths_zeroing(self, n):
+        old = self.lens.copy()
+        orig(self, n)
+        for b in range(self.B):
+            self.k[:, b, :, old[b]:self.lens[b]] = 0
+            self.v[:, b, :, old[b]:self.lens[b]] = 0
+
+    monkeypatch.setattr(ko.OracleKVCache, "set_lengths", set_lengths_zeroing)
+    _fails(pins.test_set_lengths_after_truncate_restores_the_rows_left_behind)

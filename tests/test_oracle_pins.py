@@ -349,6 +349,59 @@ def test_truncate_then_reappend_same_rows_restores_whole_buffer():
     assert (c.committed() == 14).all()
 
 
+def test_set_lengths_over_zero_rows_matches_the_closed_form():
+    """A fresh cache's unfilled slots are zero ("KV cache decoding", KVCache listing). Declaring n_b of
+    them filled, then appending one row (k, v), gives a query scores 0 for the n_b zero keys and
+    s = q.k / sqrt(d) for its own: the output is e^s / (n_b + e^s) * v."""
+    B, d = 3, 4
+    c = OracleKVCache(2, B, 1, d, 16, "f64")
+    c.set_lengths([3, 0, 5])
+    np.testing.assert_array_equal(c.committed(), [3, 0, 5])
+    np.testing.assert_array_equal(c.seq_len(1), [3, 0, 5])
+    np.testing.assert_array_equal(c.positions(2), [[3, 4], [0, 1], [5, 6]])
+    k = np.arange(B * d, dtype=np.float64).reshape(B, 1, 1, d) / 10
+    v = np.arange(B * d, dtype=np.float64).reshape(B, 1, 1, d) - 5
+    c.append(0, k, v)
+    assert c.k[0, 0, 0, 3].tolist() == k[0, 0, 0].tolist() and c.k[0, 2, 0, 5].tolist() == k[2, 0, 0].tolist()
+    q = np.ones((B, 1, 1, d))
+    out = gqa_cached_attention(c, 0, q)
+    for b, n in enumerate([3, 0, 5]):
+        e = math.exp(float(q[b, 0, 0] @ k[b, 0, 0]) / math.sqrt(d))
+        np.testing.assert_allclose(out[b, 0, 0], e / (n + e) * v[b, 0, 0], rtol=1e-13)
+
+
+def test_set_lengths_after_truncate_restores_the_rows_left_behind():
+    """Truncate clears nothing (§2.4), so moving the lengths back over the same rows makes the cache
+    answer as if it had never been truncated."""
+    B, H, d = 2, 2, 8
+    past = kvc_synth.normal_f32((B, H, 9, d), 4, 1)
+    new = kvc_synth.normal_f32((B, H, 1, d), 4, 2)
+    q = kvc_synth.normal_f32((B, 4, 1, d), 4, 3)
+    kept, moved = OracleKVCache(1, B, H, d, 12, "f16"), OracleKVCache(1, B, H, d, 12, "f16")
+    for c in (kept, moved):
+        c.append(0, past, past)
+        c.commit()
+    kept.truncate([9, 6])
+    moved.truncate([2, 0])
+    moved.set_lengths([9, 6])
+    for c in (kept, moved):
+        c.append(0, new, new)
+    np.testing.assert_array_equal(gqa_cached_attention(moved, 0, q), gqa_cached_attention(kept, 0, q))
+    np.testing.assert_array_equal(moved.k, kept.k)
+
+
+def test_set_lengths_rejects_out_of_range_and_changes_nothing():
+    c = OracleKVCache(2, 2, 1, 4, 8, "bf16")
+    c.set_lengths([4, 2])
+    for bad in ([9, 0], [-1, 3]):
+        with pytest.raises(ValueError):
+            c.set_lengths(bad)
+        np.testing.assert_array_equal(c.committed(), [4, 2])
+        np.testing.assert_array_equal(c.seq_len(0), [4, 2])
+    c.set_lengths([8, 0])                                       # both ends of the range are allowed
+    np.testing.assert_array_equal(c.seq_len(1), [8, 0])
+
+
 def test_ragged_lengths_each_sequence_writes_at_its_own_position():
     c = OracleKVCache(1, 3, 1, 2, 10, "f32")
     c.append(0, np.ones((3, 1, 6, 2), np.float32), np.ones((3, 1, 6, 2), np.float32))
