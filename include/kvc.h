@@ -237,6 +237,21 @@ int kvc_truncate(kvc_handle h, int n, void* stream);
 int kvc_truncate_ragged(kvc_handle h, const int32_t* n_host, void* stream);
 
 /*
+ * kvc_set_lengths — set every layer's fill count and every committed length to n_host[b] (host memory,
+ * B values, copied), growing or shrinking. The rows [0, n_b) are then the cache's content for sequence
+ * b, whatever the store holds there: zeros in a fresh cache (unfilled slots are zero), rows written
+ * earlier after a truncate (truncate frees and clears nothing), or rows the caller wrote into the
+ * store directly (kvc_layer_ptrs). It sets up a ragged batch whose context is already in place without
+ * re-appending it.
+ * Defined by: "KV cache, incremental decode, ...", §2.3 (per-layer fill counts and one committed
+ * length per sequence) and §2.4 ("Rollback": a length is moved and nothing is copied); "KV cache
+ * decoding", "Batching caches of different lengths" (one length per request).
+ * Errors: KVC_E_INVAL (null, any n_b < 0 or n_b > max_len); KVC_E_UNSUPPORTED for a paged cache, whose
+ * blocks are mapped only by kvc_append. Nothing changes on error.
+ */
+int kvc_set_lengths(kvc_handle h, const int32_t* n_host, void* stream);
+
+/*
  * kvc_seq_len — copy lengths into out_host[B]: the committed lengths s_b for layer == -1, or one
  * layer's fill counts ("KV cache, incremental decode, ...", §4 seq_len(layer=None)).
  */
@@ -341,6 +356,13 @@ int kvc_selftest_wait_timeout(kvc_handle h, int limit_us, void* stream);
  * incremented at each successful launch). Instrumentation for benchmarks; 0 for NULL.
  */
 uint64_t kvc_launch_count(kvc_handle h);
+
+/*
+ * kvc_workspace_bytes — device bytes the handle holds for split-K partial results (grown on demand by
+ * gqa_cached_attn, gqa_cached_attn_rope and mla_cached_attn; never by gqa_cached_attn_noalloc).
+ * Instrumentation (no counterpart on the pages); 0 for NULL and before the first split call.
+ */
+size_t kvc_workspace_bytes(kvc_handle h);
 
 #ifdef __cplusplus
 }

@@ -42,6 +42,7 @@ SIGNATURES = {
     "kvc_commit": (_c_int, [_vp, _vp]),
     "kvc_truncate": (_c_int, [_vp, _c_int, _vp]),
     "kvc_truncate_ragged": (_c_int, [_vp, _i32p, _vp]),
+    "kvc_set_lengths": (_c_int, [_vp, _i32p, _vp]),
     "kvc_seq_len": (_c_int, [_vp, _c_int, _i32p]),
     "kvc_positions": (_c_int, [_vp, _c_int, _vp, _vp]),
     "kvc_nbytes": (_sz, [_vp]),
@@ -53,6 +54,7 @@ SIGNATURES = {
     "kvc_last_error": (_c_int, [_vp, ctypes.c_char_p, _sz]),
     "kvc_set_split_keys": (_c_int, [_vp, _c_int]),
     "kvc_launch_count": (ctypes.c_uint64, [_vp]),
+    "kvc_workspace_bytes": (_sz, [_vp]),
     "kvc_selftest_wait_timeout": (_c_int, [_vp, _c_int, _vp]),
     "kvc_synth_fill_normal_f32": (_c_int, [_vp, _sz, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32,
                                            ctypes.c_float, _vp]),
@@ -152,6 +154,43 @@ class Cache:
             pass
 
 
+class _DeviceArray:
+    """A device buffer the library owns, described by `__cuda_array_interface__` so torch can view it."""
+
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (int(ptr), False),
+                                         "version": 3, "strides": None}
+
+
+def device_view(ptr: int, shape, code: int):
+    """A torch tensor over `shape` elements of cache dtype `code` at device address `ptr` (no copy)."""
+    torch = _torch()
+    typestr = {KVC_F32: "<f4", KVC_F16: "<f2", KVC_BF16: "<i2", KVC_FP8_E4M3: "|u1"}[code]
+    t = torch.as_tensor(_DeviceArray(ptr, shape, typestr), device="cuda")
+    return t.view(torch_dtype(code)) if code in (KVC_BF16, KVC_FP8_E4M3) else t
+
+
+class OwnedCache(Cache):
+    """A KV cache whose store the library allocates, zero-fills and frees (kvc_create). `.k` and `.v`
+    are views of the library's store (through kvc_layer_ptrs), valid until `close()`."""
+
+    def __init__(self, L, B, H_kv, d_h, max_len, dtype, stream=None):
+        self.L, self.B, self.H_kv, self.d_h, self.max_len = L, B, H_kv, d_h, max_len
+        self.dtype = dtype if isinstance(dtype, int) else dtype_code(dtype)
+        h = ctypes.c_void_p()
+        self.h = None
+        _check(load().kvc_create(ctypes.byref(h), L, B, H_kv, d_h, max_len, self.dtype, _stream(stream)))
+        self.h = h
+        k0, v0 = kvc_layer_ptrs(self, 0)
+        shape = (L, B, H_kv, max_len, d_h)
+        self.k = device_view(k0, shape, self.dtype)
+        self.v = device_view(v0, shape, self.dtype)
+
+    def close(self):
+        self.k = self.v = None
+        super().close()
+
+
 class PagedCache(Cache):
     """A paged KV cache handle over torch-allocated pools, each [L, n_blocks, H_kv, block_size, d_h]."""
 
@@ -209,7 +248,13 @@ def mla_cached_attn(c: LatentCache, q_lat, q_rope, layer: int, scale: float, s: 
     return out
 
 
-def kvc_create(L, B, H_kv, d_h, max_len, dtype, stream=None) -> Cache:
+def kvc_create(L, B, H_kv, d_h, max_len, dtype, stream=None) -> OwnedCache:
+    """A cache whose store the library allocates and zero-fills (and frees in close())."""
+    return OwnedCache(L, B, H_kv, d_h, max_len, dtype, stream=stream)
+
+
+def kvc_create_external(L, B, H_kv, d_h, max_len, dtype, stream=None) -> Cache:
+    """A cache over torch-allocated, zeroed K and V tensors (kept as `.k` and `.v`)."""
     return Cache(L, B, H_kv, d_h, max_len, dtype, stream=stream)
 
 
@@ -283,6 +328,12 @@ def kvc_truncate_ragged(c: Cache, n, stream=None):
     _check(load().kvc_truncate_ragged(c.h, arr, _stream(stream)), c.h)
 
 
+def kvc_set_lengths(c: Cache, n, stream=None):
+    """Set every layer's fill and every committed length to n[b] (the rows [0, n_b) already in the store)."""
+    arr = (ctypes.c_int32 * c.B)(*[int(x) for x in n])
+    _check(load().kvc_set_lengths(c.h, arr, _stream(stream)), c.h)
+
+
 def kvc_seq_len(c: Cache, layer: int = -1):
     arr = (ctypes.c_int32 * c.B)()
     _check(load().kvc_seq_len(c.h, layer, arr), c.h)
@@ -354,6 +405,10 @@ def kvc_selftest_wait_timeout(c: Cache, limit_us: int, stream=None):
 
 def kvc_launch_count(c: Cache) -> int:
     return int(load().kvc_launch_count(c.h))
+
+
+def kvc_workspace_bytes(c: Cache) -> int:
+    return int(load().kvc_workspace_bytes(c.h))
 
 
 def synth_fill_normal(out, seed: int, stream_id: int, std: float = 1.0, offset: int = 0, stream=None):

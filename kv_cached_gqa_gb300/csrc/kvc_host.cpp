@@ -22,8 +22,10 @@
 #include "kvc_internal.h"
 
 namespace {
-
 thread_local std::string g_err;
+}  // namespace
+
+namespace kvc {
 
 int fail(kvc_handle h, int code, const char* fmt, ...) {
   char buf[512];
@@ -35,6 +37,12 @@ int fail(kvc_handle h, int code, const char* fmt, ...) {
   g_err = buf;
   return code;
 }
+
+}  // namespace kvc
+
+namespace {
+
+using kvc::fail;
 
 int cuda_fail(kvc_handle h, cudaError_t e, const char* what) {
   return fail(h, KVC_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -448,6 +456,33 @@ cudaError_t launch_attention(const AttnPlan& ap, const AttnArgs& a, const SplitP
     case AttnKernel::SplitK: return launch_splitk(a, p, &h->tmap_k_split, &h->tmap_v_split, st);
   }
   return cudaErrorInvalidValue;
+}
+
+}  // namespace kvc
+
+namespace kvc {
+
+int check_attention_call(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
+                         const float* out, bool rope) {
+  if (h->latent) return fail(h, KVC_E_INVAL, "a latent cache is read by mla_cached_attn");
+  if (rope && !h->d_rope) return fail(h, KVC_E_STATE, "no rotary table: call kvc_set_rope first");
+  if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
+  if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
+  if (!q || !out) return fail(h, KVC_E_INVAL, "null q/out");
+  if (H_q < 1 || H_q % h->H) return fail(h, KVC_E_INVAL, "H_q=%d must be a positive multiple of H_kv=%d", H_q, h->H);
+  if (!query_dtype_ok(h->dtype, q_dtype))
+    return fail(h, KVC_E_INVAL, "query dtype %d: F32 or the cache dtype (F16 for an fp8 cache)", q_dtype);
+  if (!aligned(q, 16) || !aligned(out, 16)) return fail(h, KVC_E_INVAL, "q/out must be 16-byte aligned");
+  if (s < KVC_COMMITTED) return fail(h, KVC_E_INVAL, "s=%d", s);
+  for (int b = 0; b < h->B; ++b) {
+    if (s >= 0 && h->lens[b] != s)
+      return fail(h, KVC_E_STATE, "s=%d but sequence %d has committed length %d", s, b, h->lens[b]);
+    if (h->fill[static_cast<size_t>(layer) * h->B + b] != h->lens[b] + T)
+      return fail(h, KVC_E_STATE, "layer %d holds %d rows of sequence %d; attention needs s_b + T = %d "
+                  "(append the chunk to this layer first)", layer, h->fill[static_cast<size_t>(layer) * h->B + b],
+                  b, h->lens[b] + T);
+  }
+  return KVC_OK;
 }
 
 }  // namespace kvc
@@ -875,6 +910,23 @@ int kvc_truncate(kvc_handle h, int n, void* stream) {
   return kvc_truncate_ragged(h, v.get(), stream);
 }
 
+int kvc_set_lengths(kvc_handle h, const int32_t* n, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  if (!n) return fail(h, KVC_E_INVAL, "null lengths");
+  if (h->paged) return fail(h, KVC_E_UNSUPPORTED, "a paged cache takes rows only through kvc_append");
+  for (int b = 0; b < h->B; ++b)
+    if (n[b] < 0 || n[b] > h->max_len)
+      return fail(h, KVC_E_INVAL, "sequence %d: length %d outside [0, max_len=%d]", b, n[b], h->max_len);
+  cudaError_t e = kvc::launch_lens_set(h->d_lens, h->B, n, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "set-lengths launch");
+  h->launches += 1;
+  for (int b = 0; b < h->B; ++b) {
+    h->lens[b] = n[b];
+    for (int l = 0; l < h->L; ++l) h->fill[static_cast<size_t>(l) * h->B + b] = n[b];
+  }
+  return KVC_OK;
+}
+
 int kvc_seq_len(kvc_handle h, int layer, int32_t* out) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
   if (!out) return fail(h, KVC_E_INVAL, "null output");
@@ -906,24 +958,8 @@ int kvc_layer_ptrs(kvc_handle h, int layer, void** k, void** v) {
 static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
                      float* out, bool rope, void* stream) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
-  if (h->latent) return fail(h, KVC_E_INVAL, "a latent cache is read by mla_cached_attn");
-  if (rope && !h->d_rope) return fail(h, KVC_E_STATE, "no rotary table: call kvc_set_rope first");
-  if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
-  if (T < 1) return fail(h, KVC_E_INVAL, "T=%d must be >= 1", T);
-  if (!q || !out) return fail(h, KVC_E_INVAL, "null q/out");
-  if (H_q < 1 || H_q % h->H) return fail(h, KVC_E_INVAL, "H_q=%d must be a positive multiple of H_kv=%d", H_q, h->H);
-  if (!kvc::query_dtype_ok(h->dtype, q_dtype))
-    return fail(h, KVC_E_INVAL, "query dtype %d: F32 or the cache dtype (F16 for an fp8 cache)", q_dtype);
-  if (!aligned(q, 16) || !aligned(out, 16)) return fail(h, KVC_E_INVAL, "q/out must be 16-byte aligned");
-  if (s < KVC_COMMITTED) return fail(h, KVC_E_INVAL, "s=%d", s);
-  for (int b = 0; b < h->B; ++b) {
-    if (s >= 0 && h->lens[b] != s)
-      return fail(h, KVC_E_STATE, "s=%d but sequence %d has committed length %d", s, b, h->lens[b]);
-    if (h->fill[static_cast<size_t>(layer) * h->B + b] != h->lens[b] + T)
-      return fail(h, KVC_E_STATE, "layer %d holds %d rows of sequence %d; attention needs s_b + T = %d "
-                  "(append the chunk to this layer first)", layer, h->fill[static_cast<size_t>(layer) * h->B + b],
-                  b, h->lens[b] + T);
-  }
+  const int crc = kvc::check_attention_call(h, q, q_dtype, layer, s, T, H_q, out, rope);
+  if (crc) return crc;
   static thread_local kvc::SplitPlan plan;   // large: keep it off the stack
   kvc::AttnPlan ap{};
   std::string perr;
@@ -993,6 +1029,8 @@ int kvc_last_error(kvc_handle h, char* buf, size_t n) {
 }
 
 uint64_t kvc_launch_count(kvc_handle h) { return h ? h->launches : 0; }
+
+size_t kvc_workspace_bytes(kvc_handle h) { return h ? h->work_floats * sizeof(float) : 0; }
 
 int kvc_set_split_keys(kvc_handle h, int keys) {
   if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");

@@ -183,6 +183,14 @@ bool mla_tc_shape(kvc_dtype dt, int r, int dR);
 cudaError_t launch_mla_tc(const MlaArgs& a, const SplitPlan& p, const CUtensorMap* tc, const CUtensorMap* tr,
                           cudaStream_t st);
 
+// Record an error message for kvc_last_error (on the handle when there is one, and for the calling
+// thread) and return `code`.
+int fail(kvc_handle h, int code, const char* fmt, ...);
+// The argument and state checks every gqa_cached_attn* entry point makes before it plans or enqueues
+// anything (h non-null): KVC_OK, or the error code with the message recorded.
+int check_attention_call(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
+                         const float* out, bool rope);
+
 // Which attention kernel serves a call, and its work plan (built from the host mirror of the lengths).
 enum class AttnKernel { SplitK, DecodeTC, ChunkTC, PrefillTC };
 struct AttnPlan {

@@ -20,8 +20,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cstdarg>
-#include <cstdio>
 #include <string>
 #include <mutex>
 #include <utility>
@@ -60,45 +58,21 @@ int scratch_address(void** out, std::string* err) {
   return KVC_OK;
 }
 
-int set_err(kvc_handle h, int code, const char* fmt, ...) {
-  char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
-  h->err = buf;
-  return code;
-}
-
 }  // namespace
 
 extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s,
                                        int T, int H_q, float* out, void* stream) {
-  if (!h) return KVC_E_INVAL;
-  // ---- the same argument and state checks as gqa_cached_attn -----------------------------------
-  if (layer < 0 || layer >= h->L) return set_err(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
-  if (T < 1) return set_err(h, KVC_E_INVAL, "T=%d must be >= 1", T);
-  if (!q || !out) return set_err(h, KVC_E_INVAL, "null q/out");
-  if (H_q < 1 || H_q % h->H) return set_err(h, KVC_E_INVAL, "H_q=%d must be a positive multiple of H_kv=%d", H_q, h->H);
-  if (!kvc::query_dtype_ok(h->dtype, q_dtype))
-    return set_err(h, KVC_E_INVAL, "query dtype %d: F32 or the cache dtype (F16 for an fp8 cache)", q_dtype);
-  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
-    return set_err(h, KVC_E_INVAL, "q/out must be 16-byte aligned");
-  if (s < KVC_COMMITTED) return set_err(h, KVC_E_INVAL, "s=%d", s);
-  for (int b = 0; b < h->B; ++b) {
-    if (s >= 0 && h->lens[b] != s)
-      return set_err(h, KVC_E_STATE, "s=%d but sequence %d has committed length %d", s, b, h->lens[b]);
-    if (h->fill[static_cast<size_t>(layer) * h->B + b] != h->lens[b] + T)
-      return set_err(h, KVC_E_STATE, "layer %d holds %d rows of sequence %d; attention needs s_b + T = %d",
-                     layer, h->fill[static_cast<size_t>(layer) * h->B + b], b, h->lens[b] + T);
-  }
+  if (!h) return kvc::fail(nullptr, KVC_E_INVAL, "null handle");
+  // ---- the checks of gqa_cached_attn, shared with it (latent handles rejected there too) -------
+  const int crc = kvc::check_attention_call(h, q, q_dtype, layer, s, T, H_q, out, false);
+  if (crc) return crc;
 
   // ---- the same kernel choice and split plan ----------------------------------------------------
   static thread_local kvc::SplitPlan plan;
   kvc::AttnPlan ap{};
   std::string perr;
   const int prc = kvc::plan_attention(h, T, H_q, &plan, &ap, &perr);
-  if (prc) return set_err(h, prc, "%s", perr.c_str());
+  if (prc) return kvc::fail(h, prc, "%s", perr.c_str());
   const int G = H_q / h->H;
   const int rpt = ap.rows_per_tile;
 
@@ -106,17 +80,17 @@ extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_
   const size_t counter_bytes = (ap.counters * sizeof(int) + 255) / 256 * 256;
   const size_t part_bytes = ap.workspace_floats * sizeof(float);
   if (counter_bytes + part_bytes > kNoallocScratchBytes)
-    return set_err(h, KVC_E_UNSUPPORTED, "this call needs %zu bytes of scratch; the fixed array holds %zu",
+    return kvc::fail(h, KVC_E_UNSUPPORTED, "this call needs %zu bytes of scratch; the fixed array holds %zu",
                    counter_bytes + part_bytes, kNoallocScratchBytes);
   void* base = nullptr;
   std::string err;
   int rc = scratch_address(&base, &err);
-  if (rc) return set_err(h, rc, "%s", err.c_str());
+  if (rc) return kvc::fail(h, rc, "%s", err.c_str());
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (counter_bytes) {
     e = cudaMemsetAsync(base, 0, counter_bytes, st);
-    if (e != cudaSuccess) return set_err(h, KVC_E_CUDA, "clearing the merge counters: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return kvc::fail(h, KVC_E_CUDA, "clearing the merge counters: %s", cudaGetErrorString(e));
   }
 
   kvc::AttnArgs a{};
@@ -131,7 +105,7 @@ extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_
   a.k_scale = h->k_scale[layer];
   a.v_scale = h->v_scale[layer];
   e = kvc::launch_attention(ap, a, plan, h, st);
-  if (e != cudaSuccess) return set_err(h, KVC_E_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return kvc::fail(h, KVC_E_CUDA, "attention launch: %s", cudaGetErrorString(e));
   h->launches += 1;
   return KVC_OK;
 }

@@ -77,7 +77,7 @@ class Mirror:
     `n_blocks` blocks, by default enough for every sequence at max_len)."""
 
     def __init__(self, L, B, H_kv, d_h, max_len, dtype, seed=0, block=None, n_blocks=None, rope=None,
-                 scales=None):
+                 scales=None, owned=False):
         import torch
         from kv_cached_gqa_gb300 import _binding as kb
         self.torch, self.kb = torch, kb
@@ -87,8 +87,8 @@ class Mirror:
             n_blocks = n_blocks or B * (-(-max_len // block))
             self.gpu = kb.PagedCache(L, B, H_kv, d_h, max_len, block, n_blocks, DT[dtype])
             self.ref = OraclePagedKVCache(L, B, H_kv, d_h, max_len, block, n_blocks, dtype)
-        else:
-            self.gpu = kb.Cache(L, B, H_kv, d_h, max_len, DT[dtype])
+        else:   # owned: the library allocates and zero-fills the store (kvc_create)
+            self.gpu = (kb.OwnedCache if owned else kb.Cache)(L, B, H_kv, d_h, max_len, DT[dtype])
             self.ref = OracleKVCache(L, B, H_kv, d_h, max_len, dtype)
         self.n_draws = 0
         self.rope = rope                      # (base, style): keys and queries rotated by position
@@ -153,6 +153,10 @@ class Mirror:
             self.kb.kvc_truncate_ragged(self.gpu, list(n))
         else:
             self.kb.kvc_truncate(self.gpu, int(n))
+
+    def set_lengths(self, n):
+        self.ref.set_lengths(n)
+        self.kb.kvc_set_lengths(self.gpu, list(n))
 
     def forward(self, T, H_q, check=True, what=""):
         """One forward over every layer: append, attend, then commit."""

@@ -35,7 +35,8 @@ def test_headers_declare_the_entry_points():
     for n in ("kvc_create", "kvc_append", "kvc_commit", "kvc_truncate", "kvc_nbytes", "gqa_cached_attn",
               "kvc_truncate_ragged", "kvc_seq_len", "kvc_positions", "kvc_layer_ptrs", "kvc_status",
               "kvc_create_paged", "kvc_block_table", "kvc_set_rope", "kvc_append_rope", "gqa_cached_attn_rope", "kvc_set_kv_scales",
-              "kvc_create_latent", "mla_cached_attn"):
+              "kvc_create_latent", "mla_cached_attn", "kvc_set_lengths", "gqa_cached_attn_noalloc",
+              "kvc_workspace_bytes"):
         assert n in names
 
 
@@ -98,6 +99,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.kvc_create(ctypes.byref(h), 1, 1, 1, 64, 16, 4, None) == -1     # unknown dtype
     assert lib.kvc_append_rope(None, 0, None, None, 0, 1, None) == -1
     assert lib.gqa_cached_attn_rope(None, None, 0, 0, -1, 1, 1, None, None) == -1
+    assert lib.kvc_set_lengths(None, None, None) == -1
+    assert lib.kvc_workspace_bytes(None) == 0
+    lib.kvc_create(None, 1, 1, 1, 64, 16, 0, None)                            # leaves another message
+    assert lib.gqa_cached_attn_noalloc(None, None, 0, 0, -1, 1, 1, None, None) == -1
+    assert _err(lib) == "null handle"                                        # the call's own message
 
 
 def test_binding_fails_loudly_when_library_missing(monkeypatch, tmp_path):
