@@ -182,100 +182,116 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------------
-# the CPU oracle on a bounded sample (run in a child process, one BLAS thread)
+# the CPU oracle on a bounded sample, on every host core: a child process (no GPU visible) spawns one
+# worker process per core, each with one BLAS thread and a share of the sample's sequences
 # ------------------------------------------------------------------------------------------------
 
-def cpu_sample_child(arg):
-    """Time the oracle's attention over a few sequences of layer 0; print a JSON result."""
-    cfg = json.loads(arg)
+def _oracle_sample(sp, b):
+    """The oracle's layer-0 attention of sequence b, ready to run: (callable, algorithmic bytes)."""
     import numpy as np
 
-    import kvc_workloads
     from oracle.kvc_oracle import OracleKVCache, OraclePagedKVCache, gqa_cached_attention, rope_chunk
-    sp = kvc_workloads.spec(cfg["workload"])
+    s_b = int(sp.lengths[b])
+    if sp.mla:
+        from oracle.kvc_oracle import OracleLatentCache, mla_cached_attention
+        c = OracleLatentCache(1, 1, sp.d_h, sp.d_rope, s_b + sp.T, sp.dtype)
+        if s_b:
+            c.append(0, *(x[None] for x in sp.host_prefill_latent(0, b, s_b)))
+            c.commit()
+        c.append(0, *(x[None] for x in sp.host_step_latent(0, 0, b)))
+        ql, qr = (x[None] for x in sp.host_queries_mla(0, 0, b, range(sp.H_q)))
+        return (lambda: mla_cached_attention(c, 0, ql, qr, sp.mla_scale)), sp.attn_bytes([b])
 
     def rot(x, start):                 # the workload's rotary positions, if it has them
         return rope_chunk(x, [start], sp.rope_base, sp.rope_style) if sp.rope_base else x
 
-    if sp.mla:
-        from oracle.kvc_oracle import OracleLatentCache, mla_cached_attention
-        caches, queries = [], []
-        for b in range(cfg["n_seq"]):
-            s_b = int(sp.lengths[b])
-            c = OracleLatentCache(1, 1, sp.d_h, sp.d_rope, s_b + sp.T, sp.dtype)
-            if s_b:
-                c.append(0, *(x[None] for x in sp.host_prefill_latent(0, b, s_b)))
-                c.commit()
-            c.append(0, *(x[None] for x in sp.host_step_latent(0, 0, b)))
-            caches.append(c)
-            queries.append(tuple(x[None] for x in sp.host_queries_mla(0, 0, b, range(sp.H_q))))
-        t_end = time.perf_counter() + cfg["seconds"]
-        passes, elapsed, times = 0, 0.0, []
-        while time.perf_counter() < t_end or passes < cfg.get("min_passes", 1):
-            t0 = time.perf_counter()
-            for c, (ql, qr) in zip(caches, queries):
-                mla_cached_attention(c, 0, ql, qr, sp.mla_scale)
-            times.append(time.perf_counter() - t0)
-            elapsed += times[-1]
-            passes += 1
-        print(json.dumps({"bytes_per_pass": sp.attn_bytes(range(cfg["n_seq"])), "passes": passes, "seconds": elapsed,
-                          "pass_seconds": times, "n_seq": cfg["n_seq"], "layer_bytes": sp.attn_bytes(),
-                          "step_bytes": sp.step_bytes()}))
-        return
-    seqs = list(range(cfg["n_seq"]))
-    caches, queries = [], []
-    for b in seqs:
-        s_b = int(sp.lengths[b])
-        if sp.block:
-            c = OraclePagedKVCache(1, 1, sp.H_kv, sp.d_h, s_b + sp.T, sp.block,
-                                   -(-(s_b + sp.T) // sp.block), sp.dtype)
-        else:
-            c = OracleKVCache(1, 1, sp.H_kv, sp.d_h, s_b + sp.T, sp.dtype)
-        if s_b:
-            kk = np.stack([sp.host_prefill_rows(0, b, h, s_b)[0] for h in range(sp.H_kv)])[None]
-            vv = np.stack([sp.host_prefill_rows(0, b, h, s_b)[1] for h in range(sp.H_kv)])[None]
-            c.append(0, rot(kk, 0), vv)
-            c.commit()
-        kn = np.stack([sp.host_step_rows(0, 0, b, h)[0] for h in range(sp.H_kv)])[None]
-        vn = np.stack([sp.host_step_rows(0, 0, b, h)[1] for h in range(sp.H_kv)])[None]
-        c.append(0, rot(kn, s_b), vn)
-        caches.append(c)
-        queries.append(rot(sp.host_queries(0, 0, b, range(sp.H_q))[None], s_b))
-    bytes_per_pass = sp.attn_bytes(seqs)
-    t_end = time.perf_counter() + cfg["seconds"]
-    passes, elapsed = 0, 0.0
+    if sp.block:
+        c = OraclePagedKVCache(1, 1, sp.H_kv, sp.d_h, s_b + sp.T, sp.block, -(-(s_b + sp.T) // sp.block), sp.dtype)
+    else:
+        c = OracleKVCache(1, 1, sp.H_kv, sp.d_h, s_b + sp.T, sp.dtype)
+    if s_b:
+        rows = [sp.host_prefill_rows(0, b, h, s_b) for h in range(sp.H_kv)]
+        c.append(0, rot(np.stack([r[0] for r in rows])[None], 0), np.stack([r[1] for r in rows])[None])
+        c.commit()
+    new = [sp.host_step_rows(0, 0, b, h) for h in range(sp.H_kv)]
+    c.append(0, rot(np.stack([r[0] for r in new])[None], s_b), np.stack([r[1] for r in new])[None])
+    q = rot(sp.host_queries(0, 0, b, range(sp.H_q))[None], s_b)
+    return (lambda: gqa_cached_attention(c, 0, q)), sp.attn_bytes([b])
+
+
+def _oracle_worker(cfg, seqs, barrier, results):
+    """One core's share: build its sequences' caches, meet the others at the barrier, then run
+    passes over them (a fixed count in lockstep, one barrier per pass, or free-running for a time)."""
+    import kvc_workloads
+    sp = kvc_workloads.spec(cfg["workload"])
+    jobs = [_oracle_sample(sp, b) for b in seqs]
+    nbytes = sum(n for _, n in jobs)
+    barrier.wait()
     times = []
-    while time.perf_counter() < t_end or passes < cfg.get("min_passes", 1):
+    t_end = time.perf_counter() + cfg["seconds"]
+    while (len(times) < cfg["passes"]) if cfg["passes"] else (time.perf_counter() < t_end or not times):
+        if cfg["passes"]:
+            barrier.wait()
         t0 = time.perf_counter()
-        for c, q in zip(caches, queries):
-            gqa_cached_attention(c, 0, q)
-        dt = time.perf_counter() - t0
-        times.append(dt)
-        elapsed += dt
-        passes += 1
-    print(json.dumps({"bytes_per_pass": bytes_per_pass, "passes": passes, "seconds": elapsed,
-                      "pass_seconds": times, "n_seq": len(seqs), "layer_bytes": sp.attn_bytes(),
-                      "step_bytes": sp.step_bytes()}))
+        for run, _ in jobs:
+            run()
+        times.append(time.perf_counter() - t0)
+    results.put({"seqs": list(seqs), "bytes": nbytes, "times": times})
 
 
-def run_cpu_sample(workload, n_seq, seconds, min_passes=1):
+def cpu_sample_child(arg):
+    """Spread a sample of the batch's sequences (layer 0) over one worker per core; print a JSON result."""
+    import multiprocessing as mp
+
+    import kvc_workloads
+    cfg = json.loads(arg)
+    sp = kvc_workloads.spec(cfg["workload"])
+    n_seq = min(cfg["n_seq"], sp.B)
+    workers = max(1, min(cfg["workers"], n_seq))
+    order = sorted(range(n_seq), key=lambda b: -int(sp.lengths[b]))     # longest first, dealt round-robin
+    shares = [order[w::workers] for w in range(workers)]
+    ctx = mp.get_context("spawn")
+    barrier, results = ctx.Barrier(workers), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(cfg, share, barrier, results)) for share in shares]
+    for p in procs:
+        p.start()
+    outs = [results.get(timeout=1200) for _ in procs]
+    for p in procs:
+        p.join()
+    print(json.dumps({"workers": outs, "n_seq": n_seq, "n_workers": workers, "cores": os.cpu_count(),
+                      "sample_bytes": sp.attn_bytes(range(n_seq)), "layer_bytes": sp.attn_bytes(),
+                      "step_bytes": sp.step_bytes(), "B": sp.B, "L": sp.L}))
+
+
+def run_cpu_sample(workload, n_seq, seconds=0.0, passes=0):
+    """The oracle child: every host core (one BLAS thread per worker process), no GPU visible."""
+    cores = os.cpu_count() or 1
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    arg = json.dumps({"workload": workload, "n_seq": n_seq, "seconds": seconds, "min_passes": min_passes})
+    arg = json.dumps({"workload": workload, "n_seq": n_seq, "workers": cores, "seconds": seconds,
+                      "passes": passes})
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample-child", arg],
-                       capture_output=True, text=True, env=env, cwd=ROOT, timeout=900)
+                       capture_output=True, text=True, env=env, cwd=ROOT, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError(f"oracle sample failed:\n{r.stderr[-2000:]}")
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def cpu_baseline_entry(workload, seconds, n_seq=2):
-    res = run_cpu_sample(workload, n_seq, seconds)
-    gbs = res["bytes_per_pass"] * res["passes"] / res["seconds"] / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"layer 0 attention of {res['n_seq']} of the batch's sequences (all their heads), "
-                       f"float64 NumPy oracle, {res['passes']} passes in {res['seconds']:.1f} s, one thread; "
-                       f"GB/s over the same algorithmic bytes as the GPU line"),
+def _sample_text(res, how):
+    return (f"layer 0 attention of {res['n_seq']} of the batch's {res['B']} sequences (all their heads), "
+            f"float64 NumPy oracle on {res['n_workers']} worker processes of one BLAS thread each "
+            f"({res['cores']} host cores), {how}; GB/s over the same algorithmic bytes as the GPU line; "
+            f"a whole step ({res['L']} layers, {res['B']} sequences) scaled linearly from it")
+
+
+def cpu_baseline_entry(workload, seconds, n_seq=None):
+    """Throughput of the oracle with every core busy: the sum of the workers' rates over one window."""
+    cores = os.cpu_count() or 1
+    res = run_cpu_sample(workload, n_seq or cores, seconds=seconds)
+    gbs = sum(w["bytes"] * len(w["times"]) / sum(w["times"]) for w in res["workers"]) / 1e9
+    passes = sum(len(w["times"]) for w in res["workers"])
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": res["n_workers"], "kind": "oracle",
+            "sample": _sample_text(res, f"{passes} passes over about {seconds:.0f} s"),
             "steps_per_s_equiv": round(gbs * 1e9 / res["step_bytes"], 6)}
 
 
@@ -312,21 +328,23 @@ def run_reference(args):
         return 0
     import kvc_workloads
     sp = kvc_workloads.spec(args.workload)
-    n_seq = 4
-    per_step = []
-    res = run_cpu_sample(args.workload, n_seq, 0.0, min_passes=args.warmup + args.steps)
-    per_step = res["pass_seconds"][args.warmup:]
-    t = sum(per_step)
-    gbs = res["bytes_per_pass"] * len(per_step) / t / 1e9
+    res = run_cpu_sample(args.workload, os.cpu_count() or 1, passes=args.warmup + args.steps)
+    # a step is one lockstep pass of every worker (they start together at a barrier): its time is the
+    # slowest worker's
+    step_s = [max(w["times"][i] for w in res["workers"]) for i in range(args.warmup, args.warmup + args.steps)]
+    t = sum(step_s)
+    gbs = res["sample_bytes"] * len(step_s) / t / 1e9
+    sample = _sample_text(res, f"each step one lockstep pass of every worker ({args.steps} timed after "
+                               f"{args.warmup} warm-up)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1e3 * t / len(per_step), 3), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(1e3 * t / len(step_s), 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": sp.dtype, "data": "synthetic (seeded Philox draws)",
-        "config": workload_config(sp, "each step is the oracle over a bounded sample: layer 0 of "
-                                      f"{n_seq} sequences"),
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"layer 0 attention of {n_seq} sequences per step, float64 NumPy, one thread"},
+        "config": workload_config(sp, f"each step is the oracle over a bounded sample: layer 0 of "
+                                      f"{res['n_seq']} sequences"),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": res["n_workers"], "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
