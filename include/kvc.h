@@ -51,7 +51,8 @@ enum {
   KVC_E_CUDA = -4,           /* a CUDA runtime/driver call failed (message in kvc_last_error) */
   KVC_E_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait gave up; reported by kvc_status */
   KVC_E_UNSUPPORTED = -6,    /* a size this build has no kernel for (d_h not in {32, 64, 128}, ...) */
-  KVC_E_NOMEM = -7           /* device or host allocation failed */
+  KVC_E_NOMEM = -7,          /* device or host allocation failed */
+  KVC_E_DEVICE_BOUNDS = -8   /* debug builds: a guard band or a kernel's index check caught a stray store */
 };
 
 /* Rotary-position pair layouts (kvc_set_rope). */
@@ -308,8 +309,9 @@ int gqa_cached_attn_rope(kvc_handle h, const void* q_dev, kvc_dtype q_dtype, int
 
 /*
  * kvc_status — synchronise `stream` and report device-side failures: KVC_E_DEVICE_TIMEOUT if a
- * kernel's bounded wait gave up since the last call (the flag is then cleared), KVC_E_CUDA on a
- * sticky CUDA error, else KVC_OK.
+ * kernel's bounded wait gave up since the last call (the flag is then cleared), KVC_E_DEVICE_BOUNDS
+ * if (debug builds) a kernel's index check skipped a store, KVC_E_CUDA on a sticky CUDA error, else
+ * KVC_OK.
  */
 int kvc_status(kvc_handle h, void* stream);
 
@@ -356,6 +358,19 @@ int kvc_selftest_wait_timeout(kvc_handle h, int limit_us, void* stream);
  * incremented at each successful launch). Instrumentation for benchmarks; 0 for NULL.
  */
 uint64_t kvc_launch_count(kvc_handle h);
+
+/*
+ * kvc_debug_check_guards — the stand-in for a memory checker (no counterpart on the pages). In a
+ * library built with KVC_DEBUG_BOUNDS (libkvc_debug.so), every device buffer the library allocates
+ * for the handle (its store when kvc_create* allocated it, the lengths, status word, merge counters,
+ * split workspace, block table and rotary table) has a 64 KiB guard band of byte 0xA5 on each side,
+ * and every kernel checks the index of each global store against its buffer, skipping and reporting
+ * (through kvc_status, KVC_E_DEVICE_BOUNDS) one that fails. This call synchronises `stream` and
+ * compares every guard band with its byte: KVC_OK, or KVC_E_DEVICE_BOUNDS naming the buffer, the side
+ * and the farthest stray byte. Stores the caller owns (kvc_create_external, caller pools) have no
+ * guards. A release build returns KVC_E_UNSUPPORTED.
+ */
+int kvc_debug_check_guards(kvc_handle h, void* stream);
 
 /*
  * kvc_workspace_bytes — device bytes the handle holds for split-K partial results (grown on demand by

@@ -10,7 +10,10 @@ from __future__ import annotations
 import ctypes
 import os
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkvc.so")
+# KVC_DEBUG_BOUNDS=1 selects the debug build: guard bands around every library buffer and an index
+# check on every kernel store (kvc_debug_check_guards); it computes the same results, more slowly.
+_LIB_NAME = "libkvc_debug.so" if os.environ.get("KVC_DEBUG_BOUNDS") == "1" else "libkvc.so"
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", _LIB_NAME)
 _lib = None
 
 KVC_F32, KVC_F16, KVC_BF16, KVC_FP8_E4M3 = 0, 1, 2, 3
@@ -19,7 +22,7 @@ ROPE_STYLE = {"half": KVC_ROPE_HALF, "interleaved": KVC_ROPE_INTERLEAVED}
 KVC_COMMITTED = -1
 KVC_MAX_BATCH = 1024
 ERRORS = {0: "KVC_OK", -1: "KVC_E_INVAL", -2: "KVC_E_CAPACITY", -3: "KVC_E_STATE", -4: "KVC_E_CUDA",
-          -5: "KVC_E_DEVICE_TIMEOUT", -6: "KVC_E_UNSUPPORTED", -7: "KVC_E_NOMEM"}
+          -5: "KVC_E_DEVICE_TIMEOUT", -6: "KVC_E_UNSUPPORTED", -7: "KVC_E_NOMEM", -8: "KVC_E_DEVICE_BOUNDS"}
 
 # exported symbols and their C signatures (restype, argtypes)
 _c_int, _vp, _sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
@@ -55,6 +58,7 @@ SIGNATURES = {
     "kvc_set_split_keys": (_c_int, [_vp, _c_int]),
     "kvc_launch_count": (ctypes.c_uint64, [_vp]),
     "kvc_workspace_bytes": (_sz, [_vp]),
+    "kvc_debug_check_guards": (_c_int, [_vp, _vp]),
     "kvc_selftest_wait_timeout": (_c_int, [_vp, _c_int, _vp]),
     "kvc_synth_fill_normal_f32": (_c_int, [_vp, _sz, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32,
                                            ctypes.c_float, _vp]),
@@ -409,6 +413,11 @@ def kvc_launch_count(c: Cache) -> int:
 
 def kvc_workspace_bytes(c: Cache) -> int:
     return int(load().kvc_workspace_bytes(c.h))
+
+
+def kvc_debug_check_guards(c: Cache, stream=None):
+    """Debug builds: raise KvcError (KVC_E_DEVICE_BOUNDS) if a guard band of a library buffer was written."""
+    _check(load().kvc_debug_check_guards(c.h, _stream(stream)), c.h)
 
 
 def synth_fill_normal(out, seed: int, stream_id: int, std: float = 1.0, offset: int = 0, stream=None):

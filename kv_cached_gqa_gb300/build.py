@@ -2,6 +2,11 @@
 
 Each translation unit under `csrc/` compiles in parallel to `_build/`, then links into
 `_lib/libkvc.so`. A rebuild happens only when a source or header is newer than the library.
+
+The same sources built with KVC_DEBUG_BOUNDS give `_lib/libkvc_debug.so` (objects in
+`_build_debug/`): guard bands around every buffer the library allocates and an index check on every
+global store of every kernel, the stand-in for a memory checker in tests (the binding loads it when
+the environment sets KVC_DEBUG_BOUNDS=1).
 """
 from __future__ import annotations
 
@@ -17,8 +22,11 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libkvc.so")
+LIB_DEBUG = os.path.join(LIBDIR, "libkvc_debug.so")
+DEBUG_FLAGS = ["-DKVC_DEBUG_BOUNDS"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -40,15 +48,15 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps() + [os.path.abspath(__file__)])
 
 
-def _compile(nvcc, src, extra):
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(nvcc, src, outdir, extra):
+    obj = os.path.join(outdir, os.path.basename(src) + ".o")
     cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -56,26 +64,37 @@ def _compile(nvcc, src, extra):
     return obj, r.stderr
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every CUDA/C++ source for sm_103a and link `_lib/libkvc.so`; returns its path."""
-    if not force and up_to_date():
+def _link(nvcc, objs, lib):
+    tmp = lib + ".tmp"
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = True) -> str:
+    """Compile every CUDA/C++ source for sm_103a and link `_lib/libkvc.so` (and, with `debug`,
+    `_lib/libkvc_debug.so`, in the same parallel pass); returns the release library's path."""
+    targets = [(LIB, BUILD, list(extra_flags))]
+    if debug:
+        targets.append((LIB_DEBUG, BUILD_DEBUG, list(extra_flags) + DEBUG_FLAGS))
+    targets = [t for t in targets if force or not up_to_date(t[0])]
+    if not targets:
         return LIB
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
+    for _, outdir, _ in targets:
+        os.makedirs(outdir, exist_ok=True)
     srcs = _sources()
-    with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        results = list(ex.map(lambda s: _compile(nvcc, s, list(extra_flags)), srcs))
+    jobs = [(src, outdir, flags) for _, outdir, flags in targets for src in srcs]
+    with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
+        results = list(ex.map(lambda j: _compile(nvcc, *j), jobs))
     if verbose:
         for _, err in results:
             if err.strip():
                 print(err, file=sys.stderr)
-    tmp = LIB + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    for k, (lib, _, _) in enumerate(targets):
+        _link(nvcc, [o for o, _ in results[k * len(srcs):(k + 1) * len(srcs)]], lib)
     return LIB
 
 

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     }
     out = Pack<Tc>::from_f32(x);
   }
-  *reinterpret_cast<uint4*>(dst) = out;
+  if (dev::in_bounds(dst_row, is_v ? a.v_rows : a.k_rows, a.status)) *reinterpret_cast<uint4*>(dst) = out;
 }
 
 __global__ void lens_add_kernel(int32_t* lens, int B, int delta) {

@@ -448,12 +448,12 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
           if (r < nrows) {
             const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
             if (nsplit == 1) {
-              a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = o[r] / ctl->l[r] * a.v_scale;
+              put_out(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d, o[r] / ctl->l[r] * a.v_scale);
             } else {
-              a.part_o[(item_row0 + r) * kDh + d] = o[r];
+              put_part_o(a, (item_row0 + r) * kDh + d, o[r]);
               if (d == 0) {
-                a.part_ml[(item_row0 + r) * 2] = ctl->m[r];
-                a.part_ml[(item_row0 + r) * 2 + 1] = ctl->l[r];
+                put_part_ml(a, (item_row0 + r) * 2, ctl->m[r]);
+                put_part_ml(a, (item_row0 + r) * 2 + 1, ctl->l[r]);
               }
             }
           }
@@ -506,7 +506,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
                 acc = fmaf(wm[r * kMergeSplits + sp],
                            __ldcg(a.part_o + (first_row + static_cast<long long>(sp) * NR + r) * kDh + d), acc);
               const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-              if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc * linv[r] * a.v_scale;
+              if (!aborted) put_out(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d, acc * linv[r] * a.v_scale);
             }
           } else {
             for (int r = 0; r < nrows && d_ok; ++r) {
@@ -522,7 +522,7 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
                 m = mn;
               }
               const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-              if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d] = acc / l * a.v_scale;
+              if (!aborted) put_out(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d, acc / l * a.v_scale);
             }
           }
           if (tid == 64) *counter = 0;

@@ -136,6 +136,33 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }
 
+// ---- debug index checks (KVC_DEBUG_BOUNDS) ------------------------------------------------------
+// In a debug build a global store whose index falls outside its buffer is skipped and reported through
+// the status word (kvc_status returns KVC_E_DEVICE_BOUNDS); a release build compiles the check away.
+__device__ __forceinline__ bool in_bounds(long long i, long long n, int* status) {
+#ifdef KVC_DEBUG_BOUNDS
+  if (i < 0 || i >= n) {
+    atomicExch(status, kStatusBounds);
+    return false;
+  }
+#else
+  (void)i; (void)n; (void)status;
+#endif
+  return true;
+}
+template <typename A>
+__device__ __forceinline__ void put_out(const A& a, long long i, float v) {
+  if (in_bounds(i, a.out_elems, a.status)) a.out[i] = v;
+}
+template <typename A>
+__device__ __forceinline__ void put_part_o(const A& a, long long i, float v) {
+  if (in_bounds(i, a.part_o_elems, a.status)) a.part_o[i] = v;
+}
+template <typename A>
+__device__ __forceinline__ void put_part_ml(const A& a, long long i, float v) {
+  if (in_bounds(i, a.part_ml_elems, a.status)) a.part_ml[i] = v;
+}
+
 // ---- programmatic dependent launch ---------------------------------------------------------------
 // Every kernel of the library is launched so that it may start while its stream predecessor is
 // still finishing. Each kernel first does set-up that touches no global data another kernel writes,

@@ -72,16 +72,58 @@ EncodeTiledFn encode_fn(std::string* err) {
   return fn;
 }
 
+// ---- device buffers the handle owns --------------------------------------------------------------
+// A debug build (KVC_DEBUG_BOUNDS) allocates kGuard more bytes on each side of every buffer and fills
+// them with kGuardByte; kvc_debug_check_guards compares them with that byte, so a kernel that wrote
+// past either end of a library buffer (the store, the lengths, the workspace, the counters, the block
+// table, the rotary table) is caught after the fact. The guards keep the payload 256-byte aligned.
+#ifdef KVC_DEBUG_BOUNDS
+constexpr size_t kGuard = 64 * 1024;
+#else
+constexpr size_t kGuard = 0;
+#endif
+constexpr unsigned char kGuardByte = 0xA5;
+
+cudaError_t dev_alloc(kvc_handle h, void** p, size_t bytes, const char* what, cudaStream_t st, bool async) {
+  void* base = nullptr;
+  cudaError_t e = async ? cudaMallocAsync(&base, bytes + 2 * kGuard, st) : cudaMalloc(&base, bytes + 2 * kGuard);
+  if (e != cudaSuccess) return e;
+  unsigned char* payload = static_cast<unsigned char*>(base) + kGuard;
+  if (kGuard) {
+    e = cudaMemsetAsync(base, kGuardByte, kGuard, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(payload + bytes, kGuardByte, kGuard, st);
+    if (e != cudaSuccess) {
+      if (async) cudaFreeAsync(base, st); else cudaFree(base);
+      return e;
+    }
+  }
+  h->bufs.push_back({base, payload, bytes, what});
+  *p = payload;
+  return cudaSuccess;
+}
+
+// Free a buffer dev_alloc gave out (stream-ordered when `async`); NULL is a no-op.
+void dev_free(kvc_handle h, void* p, cudaStream_t st, bool async) {
+  if (!p) return;
+  for (size_t i = 0; i < h->bufs.size(); ++i) {
+    if (h->bufs[i].payload != p) continue;
+    if (async) cudaFreeAsync(h->bufs[i].base, st); else cudaFree(h->bufs[i].base);
+    h->bufs.erase(h->bufs.begin() + static_cast<long>(i));
+    return;
+  }
+}
+
 int init_device_state(kvc_handle h, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&h->device);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaGetDevice");
   e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaDeviceGetAttribute");
-  e = cudaMalloc(&h->d_lens, sizeof(int32_t) * h->B);
+  e = dev_alloc(h, reinterpret_cast<void**>(&h->d_lens), sizeof(int32_t) * h->B, "lengths", st, false);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(lengths)");
-  e = cudaMalloc(&h->d_status, sizeof(int));
+  e = dev_alloc(h, reinterpret_cast<void**>(&h->d_status), sizeof(int), "status word", st, false);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(status)");
-  e = cudaMalloc(&h->d_counters, sizeof(int) * kvc::kMaxUnits * h->H);
+  e = dev_alloc(h, reinterpret_cast<void**>(&h->d_counters), sizeof(int) * kvc::kMaxUnits * h->H, "merge counters",
+                st, false);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(counters)");
   e = cudaMemsetAsync(h->d_lens, 0, sizeof(int32_t) * h->B, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->d_status, 0, sizeof(int), st);
@@ -89,7 +131,7 @@ int init_device_state(kvc_handle h, cudaStream_t st) {
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync");
   if (h->paged) {                                   // every logical block starts unmapped (-1)
     const size_t tb = sizeof(int32_t) * h->table.size();
-    e = cudaMalloc(&h->d_table, tb);
+    e = dev_alloc(h, reinterpret_cast<void**>(&h->d_table), tb, "block table", st, false);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaMalloc(block table)");
     e = cudaMemsetAsync(h->d_table, 0xFF, tb, st);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync(block table)");
@@ -129,16 +171,7 @@ int init_device_state(kvc_handle h, cudaStream_t st) {
 void release(kvc_handle h) {
   if (!h) return;
   cudaDeviceSynchronize();
-  if (h->owns_store) {
-    cudaFree(h->k);
-    cudaFree(h->v);
-  }
-  cudaFree(h->d_lens);
-  cudaFree(h->d_status);
-  cudaFree(h->work);
-  cudaFree(h->d_counters);
-  cudaFree(h->d_table);
-  cudaFree(h->d_rope);
+  for (const auto& buf : h->bufs) cudaFree(buf.base);     // the store too, when the library owns it
   delete h;
 }
 
@@ -242,9 +275,9 @@ int ensure_workspace(kvc_handle h, size_t need, cudaStream_t st) {
   if (need <= h->work_floats) return KVC_OK;
   const size_t grow = need + need / 4;
   float* p = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&p), grow * sizeof(float), st);
+  cudaError_t e = dev_alloc(h, reinterpret_cast<void**>(&p), grow * sizeof(float), "split workspace", st, true);
   if (e != cudaSuccess) return fail(h, KVC_E_NOMEM, "workspace cudaMallocAsync: %s", cudaGetErrorString(e));
-  if (h->work) cudaFreeAsync(h->work, st);
+  dev_free(h, h->work, st, true);
   h->work = p;
   h->work_floats = grow;
   return KVC_OK;
@@ -499,8 +532,8 @@ int kvc_create(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_len, kv
   if (!h) return fail(nullptr, KVC_E_NOMEM, "host allocation failed");
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = store_bytes(h), bytes2 = store_bytes(h, true);
-  cudaError_t e = cudaMalloc(&h->k, bytes);
-  if (e == cudaSuccess) e = cudaMalloc(&h->v, bytes2);
+  cudaError_t e = dev_alloc(h, &h->k, bytes, "K store", st, false);
+  if (e == cudaSuccess) e = dev_alloc(h, &h->v, bytes2, "V store", st, false);
   h->owns_store = true;
   if (e != cudaSuccess) {
     rc = fail(nullptr, KVC_E_NOMEM, "cudaMalloc of %zu + %zu bytes failed: %s", bytes, bytes2, cudaGetErrorString(e));
@@ -582,8 +615,8 @@ int kvc_create_paged(kvc_handle* out, int L, int B, int H_kv, int d_h, int max_l
     h->v = v_pool;
   } else {
     h->owns_store = true;
-    cudaError_t e = cudaMalloc(&h->k, bytes);
-    if (e == cudaSuccess) e = cudaMalloc(&h->v, bytes);
+    cudaError_t e = dev_alloc(h, &h->k, bytes, "K pool", st, false);
+    if (e == cudaSuccess) e = dev_alloc(h, &h->v, bytes, "V pool", st, false);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->k, 0, bytes, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->v, 0, bytes, st);
     if (e != cudaSuccess) {
@@ -640,8 +673,8 @@ int kvc_create_latent(kvc_handle* out, int L, int B, int r, int d_rope, int max_
   } else {
     const size_t b1 = store_bytes(h), b2 = store_bytes(h, true);
     h->owns_store = true;
-    cudaError_t e = cudaMalloc(&h->k, b1);
-    if (e == cudaSuccess) e = cudaMalloc(&h->v, b2);
+    cudaError_t e = dev_alloc(h, &h->k, b1, "latent store", st, false);
+    if (e == cudaSuccess) e = dev_alloc(h, &h->v, b2, "RoPE-key store", st, false);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->k, 0, b1, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->v, 0, b2, st);
     if (e != cudaSuccess) {
@@ -751,6 +784,9 @@ int mla_cached_attn(kvc_handle h, const void* q_lat, const void* q_rope, kvc_dty
   a.c_store = h->k; a.kr_store = h->v;
   a.layer = layer; a.B = h->B; a.H = H; a.T = T; a.r = h->D; a.dR = h->Dv; a.max_len = h->max_len;
   a.scale = scale; a.cache_dtype = h->dtype;
+  a.out_elems = static_cast<long long>(h->B) * H * T * h->D;
+  a.part_o_elems = h->work ? static_cast<long long>(plan.n_items) * kvc::kMlaRows * h->D : 0;
+  a.part_ml_elems = h->work ? static_cast<long long>(plan.n_items) * kvc::kMlaRows * 2 : 0;
   cudaError_t e = tc ? kvc::launch_mla_tc(a, plan, &h->tmap_k_tc, &h->tmap_v_tc, st) : kvc::launch_mla(a, plan, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "latent attention launch");
   h->launches += 1;
@@ -797,6 +833,9 @@ static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v
   }
   a.k_scale = h->k_scale[layer];
   a.v_scale = h->v_scale[layer];
+  a.k_rows = static_cast<long long>(store_bytes(h) / (static_cast<size_t>(h->D) * kvc::itemsize(h->dtype)));
+  a.v_rows = static_cast<long long>(store_bytes(h, true) / (static_cast<size_t>(h->Dv) * kvc::itemsize(h->dtype)));
+  a.status = h->d_status;
   cudaError_t e = kvc::launch_append(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "append launch");
   h->launches += 1;
@@ -822,7 +861,7 @@ int kvc_set_rope(kvc_handle h, double base, kvc_rope_style style, void* stream) 
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!h->d_rope) {
     const size_t bytes = sizeof(float2) * static_cast<size_t>(h->max_len) * (h->D / 2);
-    cudaError_t e = cudaMalloc(&h->d_rope, bytes);
+    cudaError_t e = dev_alloc(h, reinterpret_cast<void**>(&h->d_rope), bytes, "rotary table", st, false);
     if (e != cudaSuccess) {
       h->d_rope = nullptr;
       return fail(h, KVC_E_NOMEM, "rotary table (%zu bytes): %s", bytes, cudaGetErrorString(e));
@@ -988,6 +1027,9 @@ static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, 
   }
   a.k_scale = h->k_scale[layer];
   a.v_scale = h->v_scale[layer];
+  a.out_elems = static_cast<long long>(h->B) * H_q * T * h->D;
+  a.part_o_elems = h->work ? static_cast<long long>(plan.n_items) * rpt * h->D : 0;
+  a.part_ml_elems = h->work ? static_cast<long long>(plan.n_items) * rpt * 2 : 0;
   cudaError_t e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
   h->launches += 1;
@@ -1014,9 +1056,37 @@ int kvc_status(kvc_handle h, void* stream) {
   if (flag) {
     const int zero = 0;
     cudaMemcpy(h->d_status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (flag == kvc::kStatusBounds)
+      return fail(h, KVC_E_DEVICE_BOUNDS, "a kernel's bounds check caught an index past its buffer and skipped the store");
     return fail(h, KVC_E_DEVICE_TIMEOUT, "a kernel's bounded wait gave up (status %d)", flag);
   }
   return KVC_OK;
+}
+
+int kvc_debug_check_guards(kvc_handle h, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+#ifndef KVC_DEBUG_BOUNDS
+  (void)stream;
+  return fail(h, KVC_E_UNSUPPORTED, "this library was built without KVC_DEBUG_BOUNDS (no guard bands)");
+#else
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+  std::vector<unsigned char> band(kGuard);
+  for (const auto& buf : h->bufs) {
+    for (int side = 0; side < 2; ++side) {
+      const unsigned char* src = side == 0 ? static_cast<const unsigned char*>(buf.base)
+                                           : static_cast<const unsigned char*>(buf.payload) + buf.bytes;
+      e = cudaMemcpy(band.data(), src, kGuard, cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) return cuda_fail(h, e, "guard read");
+      for (size_t i = 0; i < kGuard; ++i)
+        if (band[i] != kGuardByte)
+          return fail(h, KVC_E_DEVICE_BOUNDS, "%s: the guard band %s it was overwritten, %zu bytes %s its %s",
+                      buf.what, side == 0 ? "before" : "after", side == 0 ? kGuard - i : i + 1,
+                      side == 0 ? "before" : "past", side == 0 ? "start" : "end");
+    }
+  }
+  return KVC_OK;
+#endif
 }
 
 int kvc_last_error(kvc_handle h, char* buf, size_t n) {

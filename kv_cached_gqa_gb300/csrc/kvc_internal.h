@@ -33,8 +33,10 @@ inline bool query_dtype_ok(kvc_dtype cache, int q) {
   return cache == KVC_FP8_E4M3 ? q == KVC_F16 : (q == cache && q != KVC_FP8_E4M3);
 }
 
-// Device status word values written by kernels whose bounded waits give up.
+// Device status word values: a kernel's bounded wait gave up; (debug builds) a store's index failed
+// its bound and was skipped.
 constexpr int kStatusTimeout = 1;
+constexpr int kStatusBounds = 3;
 
 // Where a store keeps its rows. A contiguous store is [L, B, H, max_len, D]. A paged store is a
 // pool of fixed-size blocks, [L, n_blocks, H, block, D], and a block table [B, max_blocks] that maps
@@ -83,6 +85,8 @@ struct AppendArgs {
   Rope rope;                // rotate K rows by their positions before storing them (V untouched)
   float k_scale = 1.f;      // fp8 caches: stored code = e4m3(x / scale)
   float v_scale = 1.f;
+  long long k_rows = 0, v_rows = 0;   // rows of each store (debug index checks)
+  int* status = nullptr;              // device status word (debug index checks)
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 
@@ -132,6 +136,7 @@ struct AttnArgs {
   Rope rope;                // rotate each query row by its position s_b + t before attending
   float k_scale = 1.f;      // fp8 caches: scores use code * k_scale, outputs code * v_scale
   float v_scale = 1.f;
+  long long out_elems = 0, part_o_elems = 0, part_ml_elems = 0;   // buffer sizes (debug index checks)
 };
 // Workspace floats the plan needs (0 when no unit splits).
 size_t splitk_workspace_floats(const SplitPlan& p, int D);
@@ -172,6 +177,7 @@ struct MlaArgs {
   int layer, B, H, T, r, dR, max_len;
   float scale;              // softmax scale (1 / sqrt of the per-head query-key width)
   kvc_dtype cache_dtype;
+  long long out_elems = 0, part_o_elems = 0, part_ml_elems = 0;   // buffer sizes (debug index checks)
 };
 constexpr int kMlaRows = 16;                 // query rows per CTA
 int mla_tile_keys(kvc_dtype dt);             // keys per shared-memory tile
@@ -294,6 +300,15 @@ struct kvc_cache {
   std::vector<long long> plan_n_eff;  // planner scratch
   std::vector<int> plan_nsplit;
   std::vector<std::pair<int, int>> plan_order;
+  // every device buffer the library allocated for this handle: (allocation base, payload, bytes,
+  // what); a debug build (KVC_DEBUG_BOUNDS) puts guard bands of a known byte on both sides of each
+  struct DevBuf {
+    void* base;
+    void* payload;
+    size_t bytes;
+    const char* what;
+  };
+  std::vector<DevBuf> bufs;
   uint64_t launches = 0;          // kernels enqueued by this handle
   int num_sms = 0;
   int device = 0;

@@ -242,12 +242,12 @@ mla_kernel(const MlaArgs a, const __grid_constant__ SplitPlan plan) {
     for (int j = 0; j < kMaxDpt; ++j) {
       const int d = tid + j * kThreads;
       if (d >= a.r) continue;
-      if (nsplit == 1) a.out[orow + d] = o[r][j] / st_l[r];
-      else a.part_o[(item_row0 + r) * a.r + d] = o[r][j];
+      if (nsplit == 1) put_out(a, orow + d, o[r][j] / st_l[r]);
+      else put_part_o(a, (item_row0 + r) * a.r + d, o[r][j]);
     }
     if (nsplit > 1 && tid == 0) {
-      a.part_ml[(item_row0 + r) * 2] = st_m[r];
-      a.part_ml[(item_row0 + r) * 2 + 1] = st_l[r];
+      put_part_ml(a, (item_row0 + r) * 2, st_m[r]);
+      put_part_ml(a, (item_row0 + r) * 2 + 1, st_l[r]);
     }
   }
   if (nsplit == 1) return;
@@ -275,7 +275,7 @@ mla_kernel(const MlaArgs a, const __grid_constant__ SplitPlan plan) {
       m = mn;
     }
     const int gr = row0 + r, t = gr / a.H, h = gr % a.H;
-    a.out[((static_cast<long long>(b) * a.H + h) * a.T + t) * a.r + d] = acc / l;
+    put_out(a, ((static_cast<long long>(b) * a.H + h) * a.T + t) * a.r + d, acc / l);
   }
   if (tid == 0) *counter = 0;
 }

@@ -416,12 +416,12 @@ mla_tc_kernel(const MlaArgs a, const __grid_constant__ SplitPlan plan,
 #pragma unroll
         for (int mb = 0; mb < Lo::kOBlocks; ++mb) {
           const int d = mb * 128 + dcol;
-          if (nsplit == 1) a.out[orow + d] = o[mb][r] / ctl->l[r];
-          else a.part_o[(item_row0 + r) * R + d] = o[mb][r];
+          if (nsplit == 1) put_out(a, orow + d, o[mb][r] / ctl->l[r]);
+          else put_part_o(a, (item_row0 + r) * R + d, o[mb][r]);
         }
         if (nsplit > 1 && dcol == 0) {
-          a.part_ml[(item_row0 + r) * 2] = ctl->m[r];
-          a.part_ml[(item_row0 + r) * 2 + 1] = ctl->l[r];
+          put_part_ml(a, (item_row0 + r) * 2, ctl->m[r]);
+          put_part_ml(a, (item_row0 + r) * 2 + 1, ctl->l[r]);
         }
       }
     } else if (tid == 64) {
@@ -473,7 +473,7 @@ mla_tc_kernel(const MlaArgs a, const __grid_constant__ SplitPlan plan,
               for (int sp = 0; sp < nsplit; ++sp)
                 acc = fmaf(wm[r * kMergeSplits + sp],
                            __ldcg(a.part_o + (first_row + static_cast<long long>(sp) * kNR + r) * R + d), acc);
-              if (!aborted) a.out[orow + d] = acc * linv[r];
+              if (!aborted) put_out(a, orow + d, acc * linv[r]);
             }
           }
         } else {
@@ -494,7 +494,7 @@ mla_tc_kernel(const MlaArgs a, const __grid_constant__ SplitPlan plan,
                 acc = acc * c_old + __ldcg(a.part_o + row * R + d) * c_new;
                 m = mn;
               }
-              if (!aborted) a.out[orow + d] = acc / l;
+              if (!aborted) put_out(a, orow + d, acc / l);
             }
           }
         }

@@ -104,6 +104,9 @@ extern "C" int gqa_cached_attn_noalloc(kvc_handle h, const void* q, kvc_dtype q_
   a.pg = kvc_paging(h);
   a.k_scale = h->k_scale[layer];
   a.v_scale = h->v_scale[layer];
+  a.out_elems = static_cast<long long>(h->B) * H_q * T * h->D;
+  a.part_o_elems = static_cast<long long>(plan.n_items) * rpt * h->D;
+  a.part_ml_elems = static_cast<long long>(plan.n_items) * rpt * 2;
   e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return kvc::fail(h, KVC_E_CUDA, "attention launch: %s", cudaGetErrorString(e));
   h->launches += 1;

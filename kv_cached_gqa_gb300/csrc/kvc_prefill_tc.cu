@@ -530,7 +530,7 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
             for (int c = 0; c < kDh; c += 32) {
               float ov[32];
               tmem_ld32(tmem_o + c, ov);                         // warp-wide: every lane takes part
-              if (row_ok) {
+              if (row_ok && in_bounds(prow * kDh + c + 31, a.part_o_elems, a.status)) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 4)
                   *reinterpret_cast<float4*>(a.part_o + prow * kDh + c + i) =
@@ -538,8 +538,8 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
               }
             }
             if (row_ok) {
-              a.part_ml[prow * 2] = m_ref;
-              a.part_ml[prow * 2 + 1] = l;
+              put_part_ml(a, prow * 2, m_ref);
+              put_part_ml(a, prow * 2 + 1, l);
             }
           } else if (lane == 0) {
             atomicExch(a.status, kStatusTimeout);
@@ -585,10 +585,12 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
                   acc[i + 3] = fmaf(w, o.w, acc[i + 3]);
                 }
               }
+              if (in_bounds(dst - a.out + c + 31, a.out_elems, a.status)) {
 #pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(dst + c + i) =
-                    make_float4(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv, acc[i + 3] * inv);
+                for (int i = 0; i < 32; i += 4)
+                  *reinterpret_cast<float4*>(dst + c + i) =
+                      make_float4(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv, acc[i + 3] * inv);
+              }
             }
           }
           if (tid == 64) *counter = 0;
@@ -609,7 +611,7 @@ prefill_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
           for (int c = 0; c < kDh; c += 32) {
             float ov[32];
             tmem_ld32(tmem_o + c, ov);                           // warp-wide: every lane takes part
-            if (row_ok) {
+            if (row_ok && in_bounds(dst - a.out + c + 31, a.out_elems, a.status)) {
 #pragma unroll
               for (int i = 0; i < 32; i += 4)
                 *reinterpret_cast<float4*>(dst + c + i) =

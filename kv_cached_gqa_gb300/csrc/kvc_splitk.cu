@@ -412,12 +412,12 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
     if (aborted) continue;
     if (nsplit == 1) {
       const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-      a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / sm->l[r] * a.v_scale;
+      put_out(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d, o / sm->l[r] * a.v_scale);
     } else {
-      a.part_o[(item_row0 + r) * D + d] = o;
+      put_part_o(a, (item_row0 + r) * D + d, o);
       if (d == 0) {
-        a.part_ml[(item_row0 + r) * 2] = sm->m[r];
-        a.part_ml[(item_row0 + r) * 2 + 1] = sm->l[r];
+        put_part_ml(a, (item_row0 + r) * 2, sm->m[r]);
+        put_part_ml(a, (item_row0 + r) * 2 + 1, sm->l[r]);
       }
     }
   }
@@ -448,7 +448,7 @@ splitk_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       m = mn;
     }
     const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-    if (!aborted) a.out[((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d] = o / l * a.v_scale;
+    if (!aborted) put_out(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * D + d, o / l * a.v_scale);
   }
   if (tid == 0) *counter = 0;
 }

@@ -47,6 +47,16 @@ def test_library_exports_every_declared_symbol(lib):
         assert name in _binding.SIGNATURES, f"{name} has no binding"
 
 
+def test_debug_library_exports_the_same_symbols(lib):
+    from kv_cached_gqa_gb300 import build
+    dbg = ctypes.CDLL(build.LIB_DEBUG)
+    for name in declared_symbols():
+        assert hasattr(dbg, name), name
+    dbg.kvc_debug_check_guards.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert dbg.kvc_debug_check_guards(None, None) == -1
+    assert lib.kvc_debug_check_guards(None, None) == -1
+
+
 def test_library_is_built_for_sm_103a_only():
     from kv_cached_gqa_gb300 import build
     assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
