@@ -499,14 +499,30 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
               linv[r] = 1.f / lsum;
             }
             named_sync(1, kSoftmaxThreads);
-            for (int r = 0; r < nrows && d_ok; ++r) {
-              float acc = 0.f;
-  #pragma unroll 4
-              for (int sp = 0; sp < nsplit; ++sp)
-                acc = fmaf(wm[r * kMergeSplits + sp],
-                           __ldcg(a.part_o + (first_row + static_cast<long long>(sp) * NR + r) * kDh + d), acc);
-              const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-              if (!aborted) put_out(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d, acc * linv[r] * a.v_scale);
+            if (d_ok) {
+              // every row's partial of a split in one batch of independent loads (no store between
+              // them), the output stores after the last split
+              float acc[NR];
+  #pragma unroll
+              for (int r = 0; r < NR; ++r) acc[r] = 0.f;
+              for (int sp = 0; sp < nsplit; ++sp) {
+                const float* src = a.part_o + (first_row + static_cast<long long>(sp) * NR) * kDh + d;
+                float x[NR];
+  #pragma unroll
+                for (int r = 0; r < NR; ++r) x[r] = r < nrows ? __ldcg(src + r * kDh) : 0.f;
+  #pragma unroll
+                for (int r = 0; r < NR; ++r) acc[r] = fmaf(wm[r * kMergeSplits + sp], x[r], acc[r]);
+              }
+              if (!aborted) {
+  #pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                  if (r < nrows) {
+                    const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
+                    put_out(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d,
+                            acc[r] * linv[r] * a.v_scale);
+                  }
+                }
+              }
             }
           } else {
             for (int r = 0; r < nrows && d_ok; ++r) {
