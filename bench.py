@@ -47,6 +47,8 @@ def parse_args(argv=None):
                    help="profiling only: fewer layers of the same per-layer shape (not a bench line)")
     p.add_argument("--graph", action="store_true",
                    help="replay the whole step from one CUDA graph (for launch-bound small workloads)")
+    p.add_argument("--separate", action="store_true",
+                   help="append and attend with two calls per layer instead of gqa_cached_attn_append")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=12.0)
@@ -419,16 +421,28 @@ def run_ours(args):
     lengths = [int(x) for x in sp.lengths]
     stream = torch.cuda.current_stream()
 
+    # one call per layer where the decode kernel stores the chunk itself (a single launch); the other
+    # kernels would take the append kernel as a second launch, so they keep the two calls
+    fused = not args.separate and "decode_tc_kernel" in attention_kernel_name(sp)
+
+    def layer_step(layer, qs, k, v, out, ev=None):
+        """One layer: the chunk's append and its attention (one call unless --separate); events, when
+        given, bracket the attention call (the fused call, which includes the append)."""
+        if not fused:
+            wl.append(layer, k, v)
+        if ev is not None:
+            ev[0].record(stream)
+        if fused:
+            wl.append_attend(layer, k, v, qs, out=out)
+        else:
+            wl.attend(qs, layer, out=out)
+        if ev is not None:
+            ev[1].record(stream)
+
     def step(ev=None):
         for layer, (*qs, k, v) in enumerate(inputs):
-            wl.append(layer, k, v)
-            if ev is not None:
-                if layer % TIMED_EVERY == 0:
-                    ev[layer][0].record(stream)
-            wl.attend(qs, layer, out=outs[layer])
-            if ev is not None:
-                if layer % TIMED_EVERY == 0:
-                    ev[layer][1].record(stream)
+            timed = ev is not None and layer % TIMED_EVERY == 0
+            layer_step(layer, qs, k, v, outs[layer], ev[layer] if timed else None)
         kb.kvc_commit(wl.cache)
         kb.kvc_truncate_ragged(wl.cache, lengths)
 
@@ -521,8 +535,7 @@ def run_ours(args):
             for layer in range(sp.L):
                 stream.wait_event(ev_in[st][layer])
                 *qs, k, v = dev_in[st][layer]
-                wl.append(layer, k, v)
-                wl.attend(qs, layer, out=dev_out[st][layer])
+                layer_step(layer, qs, k, v, dev_out[st][layer])
                 ev_done[st][layer].record(stream)
                 copy_stream.wait_event(ev_done[st][layer])
                 with torch.cuda.stream(copy_stream):
@@ -565,14 +578,15 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": sp.dtype,
         "data": "synthetic (seeded Philox draws; approximately N(0,1))",
         "config": dict(workload_config(sp, None if not args.layers else "PROFILING CASE: fewer layers, not a bench line"),
-                       graph=bool(args.graph)),
+                       graph=bool(args.graph),
+                       layer_calls="gqa_cached_attn_append" if fused else "kvc_append + attention call"),
         "steps_per_s": round(job_rate(1, ms, world), 3),
         "graph_replay": {"value": round(job_rate(sp.step_bytes(), graph_ms, world) / 1e9, 2), "unit": "GB/s",
                          "ms_per_step": round(graph_ms, 4), "steps_per_s": round(job_rate(1, graph_ms, world), 3),
                          "note": "the same step captured once in a CUDA graph and replayed (no host launches)"},
         "pct_of_peak": {"measured_hbm": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / 8000.0, 2)},
-        "roofline": roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args),
+        "roofline": roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args, fused),
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -586,13 +600,14 @@ def run_ours(args):
     return 0
 
 
-def roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args):
+def roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args, fused=False):
     """The attention kernel against its roofline: HBM GB/s, or dense tensor TFLOP/s when the call's
     arithmetic intensity (causal-counted flops per algorithmic byte) is above the ridge point."""
     t_sus, t_burst, t_kind = measured_tensor_peak()
     flops = sp.attn_flops()
     ridge = t_sus * 1e12 / (peak * 1e9)
-    timing = f"CUDA events around the attention call of every {TIMED_EVERY}th layer" + (
+    call = "gqa_cached_attn_append call (the chunk's append fused into the kernel)" if fused else "attention call"
+    timing = f"CUDA events around the {call} of every {TIMED_EVERY}th layer" + (
         " (in a pass without the graph)" if args.graph else " inside the timed region")
     e = {"kernel": attention_kernel_name(sp)}
     if flops / sp.attn_bytes() > ridge:

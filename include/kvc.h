@@ -4,7 +4,7 @@
  * One decode (or prefill, or verify) forward of a decoder with a KV cache, per layer l:
  *   kvc_append(l, k_new, v_new)   write the chunk's post-RoPE keys/values at positions [s_b, s_b + T)
  *   gqa_cached_attn(q, l, ...)    attend the chunk's T queries over all s_b + T stored keys
- * and once after the last layer:
+ * (or both in one call: gqa_cached_attn_append(l, k_new, v_new, q, ...)), and once after the last layer:
  *   kvc_commit()                  s_b += T for every sequence
  * ("KV cache, incremental decode, incremental UTF-8 detokenizer, generate", §2.1-§2.4 and §4
  * "The interface"; "KV cache decoding", steps 1-7).
@@ -306,6 +306,30 @@ int gqa_cached_attn(kvc_handle h, const void* q_dev, kvc_dtype q_dtype, int laye
  */
 int gqa_cached_attn_rope(kvc_handle h, const void* q_dev, kvc_dtype q_dtype, int layer, int s, int T,
                          int H_q, float* out_dev, void* stream);
+
+/*
+ * gqa_cached_attn_append — one layer's step in one call: store the chunk's K/V rows at positions
+ * [s_b, s_b + T) (what kvc_append, or with rope != 0 kvc_append_rope, does), then attend its T queries
+ * over all s_b + T stored rows (what gqa_cached_attn / gqa_cached_attn_rope with s = KVC_COMMITTED
+ * does). Defined by: "KV cache, incremental decode, ...", §2.3 (write the new keys and values at
+ * absolute positions [s, s + T), then attend with causal_mask(T, s + T, q_offset = s)) and §4 (update,
+ * then attention over the returned rows).
+ * k_new_dev, v_new_dev: [B, H_kv, T, d_h] in `in_dtype` (kvc_append's rule); q_dev, out_dev and
+ * q_dtype: gqa_cached_attn's. The caller keeps ownership of every buffer; the chunk is copied into the
+ * store before the call's kernels finish, so its buffers may be reused once the stream reaches them.
+ * Results are bit-identical to the two separate calls: the stored rows are rounded (and rotated) the
+ * same way and the attention reads exactly the stored values. On the tensor-core decode kernel (16-bit
+ * caches with d_h 64 or 128, fp8 caches with d_h 128, G * T <= 16) this is ONE launch: the CTA that
+ * attends over a new row's tile stores the row first. Other shapes launch the append kernel, then the
+ * attention kernel.
+ * Precondition: the layer holds no rows appended since the last commit/truncate (its fill equals the
+ * committed lengths), else KVC_E_STATE. Every error of kvc_append and gqa_cached_attn applies; on any
+ * error nothing changes (a paged cache may keep blocks mapped for the coming positions when a CUDA
+ * launch itself fails, as kvc_append does).
+ */
+int gqa_cached_attn_append(kvc_handle h, int layer, const void* k_new_dev, const void* v_new_dev,
+                           kvc_dtype in_dtype, const void* q_dev, kvc_dtype q_dtype, int T, int H_q,
+                           float* out_dev, int rope, void* stream);
 
 /*
  * kvc_status — synchronise `stream` and report device-side failures: KVC_E_DEVICE_TIMEOUT if a

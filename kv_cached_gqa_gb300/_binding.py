@@ -53,6 +53,8 @@ SIGNATURES = {
     "gqa_cached_attn": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
     "gqa_cached_attn_rope": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
     "gqa_cached_attn_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
+    "gqa_cached_attn_append": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _c_int,
+                                        _vp]),
     "kvc_status": (_c_int, [_vp, _vp]),
     "kvc_last_error": (_c_int, [_vp, ctypes.c_char_p, _sz]),
     "kvc_set_split_keys": (_c_int, [_vp, _c_int]),
@@ -382,6 +384,25 @@ def gqa_cached_attn_rope(c: Cache, q, layer: int, s: int = KVC_COMMITTED, out=No
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     _check(load().gqa_cached_attn_rope(c.h, _ptr(q), dtype_code(q.dtype), layer, s, int(q.shape[2]),
                                        int(q.shape[1]), _ptr(out), _stream(stream)), c.h)
+    return out
+
+
+def gqa_cached_attn_append(c: Cache, layer: int, k_new, v_new, q, out=None, rope: bool = False, stream=None):
+    """kvc_append (kvc_append_rope with rope=True) of k_new, v_new [B, H_kv, T, d_h], then
+    gqa_cached_attn (gqa_cached_attn_rope) of q [B, H_q, T, d_h] over the committed lengths, in one call
+    -> out [B, H_q, T, d_h] float32."""
+    torch = _torch()
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype or k_new.dim() != 4:
+        raise ValueError("k_new and v_new must both be [B, H_kv, T, d_h] of one dtype")
+    if tuple(k_new.shape[:2]) != (c.B, c.H_kv) or k_new.shape[3] != c.d_h:
+        raise ValueError("k_new shape does not match the cache")
+    if q.dim() != 4 or q.shape[0] != c.B or q.shape[3] != c.d_h or q.shape[2] != k_new.shape[2]:
+        raise ValueError("q must be [B, H_q, T, d_h] with the chunk's T")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _check(load().gqa_cached_attn_append(c.h, layer, _ptr(k_new), _ptr(v_new), dtype_code(k_new.dtype), _ptr(q),
+                                         dtype_code(q.dtype), int(q.shape[2]), int(q.shape[1]), _ptr(out),
+                                         1 if rope else 0, _stream(stream)), c.h)
     return out
 
 

@@ -24,6 +24,7 @@
 // up sets the device status word and the CTA skips the rest of its work, frees its TMEM and exits.
 #include <type_traits>
 
+#include "kvc_append.cuh"
 #include "kvc_device.cuh"
 #include "kvc_internal.h"
 
@@ -210,10 +211,29 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
     }
+    // fused append: the new rows [s_b, s_b + T) that fall in this split are stored by this warp before
+    // it loads the first K tile holding one of them (no other CTA loads those tiles). It stores them as
+    // soon as the ring is full (the producer would otherwise wait for a free stage there), or earlier
+    // when that tile comes first.
+    const int new_lo = max(s_b, k_begin), new_hi = min(s_b + a.T, k_end);
+    const int i_new = (a.app.k_new != nullptr && new_lo < new_hi) ? min((new_lo - k_begin) / kTK, kStages) : -1;
     int issued = 0;
     for (int i = 0; i < 2 * nkt; ++i) {
       const int st = i % kStages;
       const bool isv = i >= nkt;
+      if (i == i_new) {
+        constexpr int kGroups = DH * sizeof(Tc) / 16;       // 16-byte groups per stored row
+        const int n = (new_hi - new_lo) * 2 * kGroups;
+        for (int e = lane; e < n; e += 32) {
+          const int r = e / (2 * kGroups), c = e % (2 * kGroups);
+          const long long row = (static_cast<long long>(b) * a.H_kv + kvh) * a.T + (new_lo - s_b + r);
+          app::append_group_any<Tc>(a.app, row, c % kGroups, c >= kGroups);
+        }
+        // the stored rows are visible to this warp's tile loads (async proxy) before they are issued
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
       const int y = k_begin + (isv ? i - nkt : i) * kTK;
       const TilePiece pc = tile_piece<kTK>(a, b, kvh, y, lane);   // a block-table read overlaps the wait
       const uint32_t full = smem_u32(&ctl->full[st]);

@@ -798,9 +798,10 @@ int kvc_destroy(kvc_handle h) {
   return KVC_OK;
 }
 
-static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
-                       int T, bool rope, void* stream) {
-  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+// The checks of an append (nothing changes): on success *delta is the layer's fill minus the committed
+// lengths (uniform over the batch).
+static int check_append(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
+                        int T, bool rope, int* delta_out) {
   if (rope && h->latent) return fail(h, KVC_E_UNSUPPORTED, "fused RoPE is for K/V caches");
   if (rope && !h->d_rope) return fail(h, KVC_E_STATE, "no rotary table: call kvc_set_rope first");
   if (layer < 0 || layer >= h->L) return fail(h, KVC_E_INVAL, "layer %d out of range [0, %d)", layer, h->L);
@@ -811,17 +812,21 @@ static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v
   if (!aligned(k_new, 16) || !aligned(v_new, 16))
     return fail(h, KVC_E_INVAL, "k_new/v_new must be 16-byte aligned");
   int delta = 0;
-  int rc = layer_delta(h, layer, &delta);
+  const int rc = layer_delta(h, layer, &delta);
   if (rc) return rc;
   for (int b = 0; b < h->B; ++b) {
     const long long end = static_cast<long long>(h->fill[static_cast<size_t>(layer) * h->B + b]) + T;
     if (end > h->max_len)
       return fail(h, KVC_E_CAPACITY, "sequence %d: %lld positions exceed max_len=%d", b, end, h->max_len);
   }
-  if (h->paged) {
-    rc = paged_grow(h, layer, T, static_cast<cudaStream_t>(stream));
-    if (rc) return rc;
-  }
+  *delta_out = delta;
+  return KVC_OK;
+}
+
+// What the append kernel (or the decode kernel's fused append) needs to store a [B, H, T, D] chunk at
+// the layer's fill.
+static kvc::AppendArgs append_args(kvc_handle h, int layer, const void* k_new, const void* v_new,
+                                   kvc_dtype in_dtype, int T, int delta, bool rope) {
   kvc::AppendArgs a{};
   a.k_store = h->k; a.v_store = h->v; a.k_new = k_new; a.v_new = v_new; a.lens = h->d_lens;
   a.layer = layer; a.B = h->B; a.H = h->H; a.D = h->D; a.Dv = h->Dv; a.T = T; a.max_len = h->max_len;
@@ -836,6 +841,20 @@ static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v
   a.k_rows = static_cast<long long>(store_bytes(h) / (static_cast<size_t>(h->D) * kvc::itemsize(h->dtype)));
   a.v_rows = static_cast<long long>(store_bytes(h, true) / (static_cast<size_t>(h->Dv) * kvc::itemsize(h->dtype)));
   a.status = h->d_status;
+  return a;
+}
+
+static int append_impl(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
+                       int T, bool rope, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  int delta = 0;
+  int rc = check_append(h, layer, k_new, v_new, in_dtype, T, rope, &delta);
+  if (rc) return rc;
+  if (h->paged) {
+    rc = paged_grow(h, layer, T, static_cast<cudaStream_t>(stream));
+    if (rc) return rc;
+  }
+  const kvc::AppendArgs a = append_args(h, layer, k_new, v_new, in_dtype, T, delta, rope);
   cudaError_t e = kvc::launch_append(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "append launch");
   h->launches += 1;
@@ -994,11 +1013,11 @@ int kvc_layer_ptrs(kvc_handle h, int layer, void** k, void** v) {
   return KVC_OK;
 }
 
-static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
-                     float* out, bool rope, void* stream) {
-  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
-  const int crc = kvc::check_attention_call(h, q, q_dtype, layer, s, T, H_q, out, rope);
-  if (crc) return crc;
+// Plan and launch the attention of a call whose checks passed. With `fused` the chunk has not been
+// stored yet: the tensor-core decode kernel stores it itself (one launch); any other kernel gets the
+// append kernel launched first (two launches).
+static int attn_launch(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int T, int H_q, float* out,
+                       bool rope, const kvc::AppendArgs* fused, void* stream) {
   static thread_local kvc::SplitPlan plan;   // large: keep it off the stack
   kvc::AttnPlan ap{};
   std::string perr;
@@ -1030,10 +1049,60 @@ static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, 
   a.out_elems = static_cast<long long>(h->B) * H_q * T * h->D;
   a.part_o_elems = h->work ? static_cast<long long>(plan.n_items) * rpt * h->D : 0;
   a.part_ml_elems = h->work ? static_cast<long long>(plan.n_items) * rpt * 2 : 0;
-  cudaError_t e = kvc::launch_attention(ap, a, plan, h, st);
+  cudaError_t e = cudaSuccess;
+  if (fused) {
+    if (h->paged) {
+      const int grc = paged_grow(h, layer, T, st);
+      if (grc) return grc;
+    }
+    if (ap.kernel == kvc::AttnKernel::DecodeTC) {
+      a.app = *fused;
+    } else {
+      e = kvc::launch_append(*fused, st);
+      if (e != cudaSuccess) return cuda_fail(h, e, "append launch");
+      h->launches += 1;
+    }
+  }
+  e = kvc::launch_attention(ap, a, plan, h, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
   h->launches += 1;
   return KVC_OK;
+}
+
+static int attn_impl(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,
+                     float* out, bool rope, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  const int crc = kvc::check_attention_call(h, q, q_dtype, layer, s, T, H_q, out, rope);
+  if (crc) return crc;
+  return attn_launch(h, q, q_dtype, layer, T, H_q, out, rope, nullptr, stream);
+}
+
+// kvc_append followed by gqa_cached_attn over the committed lengths, in one call.
+static int attn_append_impl(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
+                            const void* q, kvc_dtype q_dtype, int T, int H_q, float* out, bool rope, void* stream) {
+  if (!h) return fail(nullptr, KVC_E_INVAL, "null handle");
+  int delta = 0;
+  int rc = check_append(h, layer, k_new, v_new, in_dtype, T, rope, &delta);
+  if (rc) return rc;
+  if (delta != 0)
+    return fail(h, KVC_E_STATE, "layer %d already holds %d rows appended since the last commit; this call "
+                "appends the chunk itself", layer, delta);
+  // the attention's checks as they stand once the chunk is in (every fill = committed length + T)
+  const size_t f0 = static_cast<size_t>(layer) * h->B;
+  for (int b = 0; b < h->B; ++b) h->fill[f0 + b] += T;
+  rc = kvc::check_attention_call(h, q, q_dtype, layer, KVC_COMMITTED, T, H_q, out, rope);
+  for (int b = 0; b < h->B; ++b) h->fill[f0 + b] -= T;
+  if (rc) return rc;
+  const kvc::AppendArgs app = append_args(h, layer, k_new, v_new, in_dtype, T, 0, rope);
+  rc = attn_launch(h, q, q_dtype, layer, T, H_q, out, rope, &app, stream);
+  if (rc) return rc;
+  for (int b = 0; b < h->B; ++b) h->fill[f0 + b] += T;
+  return KVC_OK;
+}
+
+int gqa_cached_attn_append(kvc_handle h, int layer, const void* k_new, const void* v_new, kvc_dtype in_dtype,
+                           const void* q, kvc_dtype q_dtype, int T, int H_q, float* out, int rope, void* stream) {
+  return attn_append_impl(h, layer, k_new, v_new, in_dtype, q, q_dtype, T, H_q, out, rope != 0, stream);
 }
 
 int gqa_cached_attn(kvc_handle h, const void* q, kvc_dtype q_dtype, int layer, int s, int T, int H_q,

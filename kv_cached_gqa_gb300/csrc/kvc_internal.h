@@ -137,6 +137,10 @@ struct AttnArgs {
   float k_scale = 1.f;      // fp8 caches: scores use code * k_scale, outputs code * v_scale
   float v_scale = 1.f;
   long long out_elems = 0, part_o_elems = 0, part_ml_elems = 0;   // buffer sizes (debug index checks)
+  // Fused append (tensor-core decode kernel only): when app.k_new is set, the chunk's rows have not
+  // been stored yet; the CTA whose split holds a new row stores it, exactly as the append kernel
+  // would, before it loads the tile that holds the row.
+  AppendArgs app{};
 };
 // Workspace floats the plan needs (0 when no unit splits).
 size_t splitk_workspace_floats(const SplitPlan& p, int D);

@@ -186,6 +186,11 @@ class GpuWorkload:
         fn = self.kb.gqa_cached_attn_rope if self.spec.rope_base else self.kb.gqa_cached_attn
         return fn(self.cache, qs[0], layer, out=out)
 
+    def append_attend(self, layer, k, v, qs, out=None):
+        """The workload's layer step in one call: gqa_cached_attn_append (rotating keys and queries when
+        the workload uses RoPE). K/V workloads only."""
+        return self.kb.gqa_cached_attn_append(self.cache, layer, k, v, qs[0], out=out, rope=bool(self.spec.rope_base))
+
     def __getattr__(self, name):                      # shape fields and host redraws of the spec
         return getattr(self.__dict__["spec"], name)
 

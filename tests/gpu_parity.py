@@ -143,6 +143,24 @@ class Mirror:
             self.kb.kvc_set_split_keys(self.gpu, 0)
         return got, want
 
+    def append_attend(self, layer, T, H_q, split_keys=0):
+        """The draws of append() then attend(), handed to the GPU in one gqa_cached_attn_append call
+        (the oracle appends, then attends): (got, want)."""
+        k = self.draw((self.B, self.H, T, self.d))
+        v = self.draw((self.B, self.H, T, self.d))
+        k_in = k if self.rope is None else rope_chunk(k, self.ref.seq_len(layer), *self.rope)
+        self.ref.append(layer, k_in, v)
+        q = self.draw((self.B, H_q, T, self.d))
+        q_att = q if self.rope is None else rope_chunk(q, self.ref.committed(), *self.rope)
+        want = gqa_cached_attention(self.ref, layer, q_att)
+        if split_keys:
+            self.kb.kvc_set_split_keys(self.gpu, split_keys)
+        got = self.kb.gqa_cached_attn_append(self.gpu, layer, self.dev(k), self.dev(v), self.dev(q),
+                                             rope=self.rope is not None).cpu().numpy()
+        if split_keys:
+            self.kb.kvc_set_split_keys(self.gpu, 0)
+        return got, want
+
     def commit(self):
         self.ref.commit()
         self.kb.kvc_commit(self.gpu)
