@@ -47,8 +47,9 @@ def parse_args(argv=None):
                    help="profiling only: fewer layers of the same per-layer shape (not a bench line)")
     p.add_argument("--graph", action="store_true",
                    help="replay the whole step from one CUDA graph (for launch-bound small workloads)")
-    p.add_argument("--separate", action="store_true",
-                   help="append and attend with two calls per layer instead of gqa_cached_attn_append")
+    p.add_argument("--fused", action="store_true",
+                   help="one gqa_cached_attn_append call per layer instead of kvc_append + the attention call "
+                        "(decode workloads)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-seconds", type=float, default=12.0)
@@ -90,7 +91,7 @@ TIMED_EVERY = 4
 # stands only while these are unchanged since its ncu capture.
 _SHARED_SOURCES = ("kvc_device.cuh", "kvc_host.cpp", "kvc_internal.h")
 KERNEL_SOURCES = {
-    "decode_tc_kernel": ("kvc_decode_tc.cu", "kvc_splitk.cu") + _SHARED_SOURCES,
+    "decode_tc_kernel": ("kvc_decode_tc.cu", "kvc_splitk.cu", "kvc_append.cuh") + _SHARED_SOURCES,
     "prefill_tc_kernel": ("kvc_prefill_tc.cu",) + _SHARED_SOURCES,
     "mla_tc_kernel": ("kvc_mla_tc.cu",) + _SHARED_SOURCES,
     "mla_kernel": ("kvc_mla.cu",) + _SHARED_SOURCES,
@@ -421,12 +422,12 @@ def run_ours(args):
     lengths = [int(x) for x in sp.lengths]
     stream = torch.cuda.current_stream()
 
-    # one call per layer where the decode kernel stores the chunk itself (a single launch); the other
-    # kernels would take the append kernel as a second launch, so they keep the two calls
-    fused = not args.separate and "decode_tc_kernel" in attention_kernel_name(sp)
+    # --fused: one call per layer where the decode kernel stores the chunk itself (a single launch); the
+    # other kernels would take the append kernel as a second launch, so they keep the two calls
+    fused = args.fused and "decode_tc_kernel" in attention_kernel_name(sp)
 
     def layer_step(layer, qs, k, v, out, ev=None):
-        """One layer: the chunk's append and its attention (one call unless --separate); events, when
+        """One layer: the chunk's append and its attention (one call with --fused); events, when
         given, bracket the attention call (the fused call, which includes the append)."""
         if not fused:
             wl.append(layer, k, v)
@@ -566,7 +567,9 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
     peak, peak_kind = measured_peaks()
-    attn_gbs = sp.attn_bytes() / (attn_avg_ms * 1e-3) / 1e9
+    # the timed call's algorithmic bytes: the attention's, plus the chunk's append when it is fused in
+    call_bytes = sp.attn_bytes() + (sp.append_bytes() if fused else 0)
+    attn_gbs = call_bytes / (attn_avg_ms * 1e-3) / 1e9
     value = job_rate(sp.step_bytes(), ms, world) / 1e9
     cpu = None
     if not args.no_cpu_baseline:
@@ -586,7 +589,7 @@ def run_ours(args):
                          "note": "the same step captured once in a CUDA graph and replayed (no host launches)"},
         "pct_of_peak": {"measured_hbm": round(100 * value / world / peak, 2),
                         "nominal_8tbs": round(100 * value / world / 8000.0, 2)},
-        "roofline": roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args, fused),
+        "roofline": roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args, fused, call_bytes),
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -600,7 +603,7 @@ def run_ours(args):
     return 0
 
 
-def roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args, fused=False):
+def roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args, fused=False, call_bytes=None):
     """The attention kernel against its roofline: HBM GB/s, or dense tensor TFLOP/s when the call's
     arithmetic intensity (causal-counted flops per algorithmic byte) is above the ridge point."""
     t_sus, t_burst, t_kind = measured_tensor_peak()
@@ -610,7 +613,8 @@ def roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args, fused=False
     timing = f"CUDA events around the {call} of every {TIMED_EVERY}th layer" + (
         " (in a pass without the graph)" if args.graph else " inside the timed region")
     e = {"kernel": attention_kernel_name(sp)}
-    if flops / sp.attn_bytes() > ridge:
+    call_bytes = call_bytes or sp.attn_bytes()
+    if flops / call_bytes > ridge:
         tflops = flops / (attn_avg_ms * 1e-3) / 1e12
         e.update({"bound": "tensor", "achieved": round(tflops, 2), "peak": t_sus, "unit": "TFLOP/s",
                   "frac": round(tflops / t_sus, 4), "peak_source": f"{t_kind} bf16_tflops_sustained",
@@ -620,7 +624,7 @@ def roofline_entry(sp, attn_avg_ms, attn_gbs, peak, peak_kind, args, fused=False
     else:
         e.update({"bound": "hbm", "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
                   "frac": round(attn_gbs / peak, 4), "peak_source": f"{peak_kind} hbm_gbs"})
-    e.update({"bytes_per_launch": sp.attn_bytes(), "launch_ms": round(attn_avg_ms, 5), "timing": timing,
+    e.update({"bytes_per_launch": call_bytes, "launch_ms": round(attn_avg_ms, 5), "timing": timing,
               "traffic": traffic_per_launch(sp)})
     return e
 

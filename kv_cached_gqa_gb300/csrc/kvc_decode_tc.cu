@@ -124,6 +124,20 @@ __device__ __forceinline__ uint32_t sw128(int rows, int row, int col) {
   return atom * (rows * 128) + row * 128 + ((((c >> 3) ^ (row & 7))) << 4) + (c & 7) * 2;
 }
 
+// The fused append's stores: rows [t0, t0 + n) of the chunk for (b, kvh), K and V, one 16-byte group per
+// thread t of nt and pass. Kept out of line: it runs once per CTA at most, and inlined into the kernel it
+// slowed the main loop of the fp8 instantiation by about 15%.
+template <typename Tc, int DH>
+__device__ __noinline__ void store_new_rows(const AppendArgs& app, int b, int kvh, int H_kv, int T, int t0, int n,
+                                            int t, int nt) {
+  constexpr int kGroups = DH * sizeof(Tc) / 16;             // 16-byte groups per stored row
+  for (int e = t; e < n * 2 * kGroups; e += nt) {
+    const int r = e / (2 * kGroups), c = e % (2 * kGroups);
+    const long long row = (static_cast<long long>(b) * H_kv + kvh) * T + (t0 + r);
+    app::append_group_any<Tc>(app, row, c % kGroups, c >= kGroups);
+  }
+}
+
 // Bounded wait that ignores the abort flag (used only to drain in-flight copies and MMAs).
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = now_ns();
@@ -134,7 +148,7 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
 
 template <typename Tc, int NR, int DH>
 __global__ void __launch_bounds__(kThreads, 2)
-decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
+decode_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ SplitPlan plan,
                  const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
   constexpr bool kF8 = std::is_same<Tc, fp8>::value;           // fp8 cache: tiles widened to float16
   using Tm = typename std::conditional<kF8, __half, Tc>::type;  // MMA operand type
@@ -204,6 +218,10 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
   const uint32_t tmem = ctl->tmem;
   const uint32_t tmem_o = tmem + (kTmemCols - NR);
   volatile int* abort_flag = &ctl->abort;
+  // fused append: the new rows [s_b, s_b + T) that fall in this split, and the first K tile holding one
+  // (-1: none)
+  const int new_lo = max(s_b, k_begin), new_hi = min(s_b + a.T, k_end);
+  const int i_new = (a.app.k_new != nullptr && new_lo < new_hi) ? (new_lo - k_begin) / kTK : -1;
 
   if (warp == 0) {
     // ---------------------------------- TMA producer (whole warp) -------------------------------
@@ -211,24 +229,15 @@ decode_tc_kernel(const AttnArgs a, const __grid_constant__ SplitPlan plan,
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
     }
-    // fused append: the new rows [s_b, s_b + T) that fall in this split are stored by this warp before
-    // it loads the first K tile holding one of them (no other CTA loads those tiles). It stores them as
-    // soon as the ring is full (the producer would otherwise wait for a free stage there), or earlier
-    // when that tile comes first.
-    const int new_lo = max(s_b, k_begin), new_hi = min(s_b + a.T, k_end);
-    const int i_new = (a.app.k_new != nullptr && new_lo < new_hi) ? min((new_lo - k_begin) / kTK, kStages) : -1;
+    // fused append: this warp stores the split's new rows before it loads the first K tile holding one
+    // (no other CTA loads those tiles): as soon as the ring is full, where it would otherwise wait for a
+    // free stage, or earlier when that tile comes first
     int issued = 0;
     for (int i = 0; i < 2 * nkt; ++i) {
       const int st = i % kStages;
       const bool isv = i >= nkt;
-      if (i == i_new) {
-        constexpr int kGroups = DH * sizeof(Tc) / 16;       // 16-byte groups per stored row
-        const int n = (new_hi - new_lo) * 2 * kGroups;
-        for (int e = lane; e < n; e += 32) {
-          const int r = e / (2 * kGroups), c = e % (2 * kGroups);
-          const long long row = (static_cast<long long>(b) * a.H_kv + kvh) * a.T + (new_lo - s_b + r);
-          app::append_group_any<Tc>(a.app, row, c % kGroups, c >= kGroups);
-        }
+      if (i == min(i_new, kStages)) {
+        store_new_rows<Tc, DH>(a.app, b, kvh, a.H_kv, a.T, new_lo - s_b, new_hi - new_lo, lane, 32);
         // the stored rows are visible to this warp's tile loads (async proxy) before they are issued
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __syncwarp();

@@ -110,6 +110,9 @@ CASES = [
     ("f16", 64, 4, 4, 129, [1, 200]),
     # chunks of more than 32 query rows per K/V head on the tensor-core chunk kernel
     ("bf16", 128, 32, 8, 9, [0, 300]),         # 36 rows: one partial row tile
+    ("bf16", 128, 32, 8, 7, [129, 1]),         # 28 rows: four copies of the rows, 32 keys each
+    ("f16", 128, 24, 8, 11, [500, 7]),         # G = 3, 33 rows: two copies of the rows
+    ("bf16", 128, 32, 8, 16, [2047, 64]),      # 64 rows: two copies, every MMA row used
     ("f16", 128, 32, 8, 64, [5, 700]),         # 256 rows: two full row tiles
     ("bf16", 128, 16, 2, 17, [130, 0, 3]),     # G = 8, 136 rows: a ragged last tile
     ("f16", 128, 8, 8, 200, [0, 129]),         # G = 1, 200 rows, diagonal masking over many tiles
