@@ -75,6 +75,7 @@ struct __align__(8) Ctl {
   unsigned long long s_ready[Lo::kSTiles];                     // one per K tile, used once
   unsigned long long k_conv[2];                                // fp8: a K tile widened into buffer c
   unsigned long long o_full, done;
+  unsigned long long cl_ready, cl_done;                        // cluster merge: partials in, reads done
   uint32_t tmem;
   int abort, last;
   float red[4][NR];
@@ -138,6 +139,42 @@ __device__ __noinline__ void store_new_rows(const AppendArgs& app, int b, int kv
   }
 }
 
+// ---- thread-block clusters: the splits of one unit merged through distributed shared memory ---------
+constexpr int kMaxCluster = 16;             // splits per unit the cluster merge takes (non-portable size)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// one arrival on an mbarrier of another CTA of the cluster, releasing this CTA's earlier writes
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+// bounded wait on a local mbarrier that other CTAs of the cluster arrive on (acquire at cluster scope)
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = now_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+    if (now_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // Bounded wait that ignores the abort flag (used only to drain in-flight copies and MMAs).
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = now_ns();
@@ -146,7 +183,11 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <typename Tc, int NR, int DH>
+// kCl: the plan gives every unit the same number of splits and the launch makes the splits of each
+// (unit, K/V head) one thread-block cluster (item order puts them next to each other, so the cluster
+// rank is the split); the splits' partials are merged through distributed shared memory by the CTA of
+// split 0 instead of through L2 by the CTA that finishes last.
+template <typename Tc, int NR, int DH, bool kCl>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ SplitPlan plan,
                  const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
@@ -199,6 +240,10 @@ decode_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ Spl
     for (int s = 0; s < Lo::kSTiles; ++s) mbar_init(smem_u32(&ctl->s_ready[s]), 1);
     mbar_init(smem_u32(&ctl->o_full), 1);
     mbar_init(smem_u32(&ctl->done), 1);
+    if (kCl) {
+      mbar_init(smem_u32(&ctl->cl_ready), nsplit > 1 ? nsplit - 1 : 1);
+      mbar_init(smem_u32(&ctl->cl_done), 1);
+    }
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -206,6 +251,9 @@ decode_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ Spl
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // cluster merge: every CTA of the cluster has its barriers initialised before any arrives remotely
+  // (every thread of every CTA of the cluster passes here, once, unconditionally)
+  if constexpr (kCl) asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
   // from here on the lengths and the queries, which earlier kernels write, are read
   pdl_wait();
   pdl_trigger();
@@ -478,6 +526,9 @@ decode_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ Spl
             const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
             if (nsplit == 1) {
               put_out(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh + d, o[r] / ctl->l[r] * a.v_scale);
+            } else if (kCl) {
+              // this split's partial output stays in its own shared memory (the P buffers are free)
+              reinterpret_cast<float*>(p_base)[r * kDh + d] = o[r];
             } else {
               put_part_o(a, (item_row0 + r) * kDh + d, o[r]);
               if (d == 0) {
@@ -490,7 +541,62 @@ decode_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ Spl
       } else if (tid == 64) {
         atomicExch(a.status, kStatusTimeout);
       }
-      if (nsplit > 1) {
+      if (kCl && nsplit > 1) {
+        // ---- cluster merge: split 0 reads every split's (m, l, o) from its CTA's shared memory ----
+        named_sync(1, kSoftmaxThreads);                       // this CTA's partial is in place
+        const int t = tid - 64;
+        if (cluster_rank() != 0) {
+          if (t == 0) {
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
+            arrive_remote(map_rank(smem_u32(&ctl->cl_ready), 0));
+            // stay (the teardown waits for this thread) until split 0 has read this CTA's memory
+            if (!mbar_wait_cluster(smem_u32(&ctl->cl_done), 0)) atomicExch(a.status, kStatusTimeout);
+          }
+        } else {
+          if (t == 0) ctl->last = mbar_wait_cluster(smem_u32(&ctl->cl_ready), 0) ? 1 : 0;
+          named_sync(1, kSoftmaxThreads);
+          if (ctl->last && !aborted) {
+            const uint32_t m_at = smem_u32(&ctl->m[0]), l_at = smem_u32(&ctl->l[0]), o_at = smem_u32(p_base);
+            for (int i = t; i < nrows * kDh; i += kSoftmaxThreads) {
+              const int r = i / kDh, dd = i % kDh;
+              // every split's (m, l, o) of this output in flight at once
+              float ms[kMaxCluster], ls[kMaxCluster], os[kMaxCluster];
+  #pragma unroll
+              for (int sp = 0; sp < kMaxCluster; ++sp) {
+                ms[sp] = -INFINITY;
+                ls[sp] = 0.f;
+                os[sp] = 0.f;
+                if (sp < nsplit) {
+                  ms[sp] = ld_cluster(map_rank(m_at + 4 * r, sp));
+                  ls[sp] = ld_cluster(map_rank(l_at + 4 * r, sp));
+                  os[sp] = ld_cluster(map_rank(o_at + 4 * (r * kDh + dd), sp));
+                }
+              }
+              float mx = -INFINITY;
+  #pragma unroll
+              for (int sp = 0; sp < kMaxCluster; ++sp)
+                if (ls[sp] > 0.f) mx = fmaxf(mx, ms[sp]);
+              float lsum = 0.f, acc = 0.f;
+  #pragma unroll
+              for (int sp = 0; sp < kMaxCluster; ++sp) {
+                if (ls[sp] > 0.f) {
+                  const float w = exp2f(ms[sp] - mx);
+                  lsum = fmaf(w, ls[sp], lsum);
+                  acc = fmaf(w, os[sp], acc);
+                }
+              }
+              const int gr = row0 + r, tq = gr / a.G, g = gr % a.G;
+              put_out(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + tq) * kDh + dd,
+                      acc / lsum * a.v_scale);
+            }
+          } else if (t == 0) {
+            atomicExch(a.status, kStatusTimeout);
+          }
+          named_sync(1, kSoftmaxThreads);                     // every read of the other CTAs is done
+          if (t == 0)
+            for (int sp = 1; sp < nsplit; ++sp) arrive_remote(map_rank(smem_u32(&ctl->cl_done), sp));
+        }
+      } else if (nsplit > 1) {
         // ---- the CTA that finishes a unit's last split merges its partials -----------------------
         __threadfence();
         named_sync(1, kSoftmaxThreads);
@@ -586,12 +692,53 @@ decode_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ Spl
   }
 }
 
+// Cluster sizes past the portable 8 (up to 16) allowed for a kernel, once per device.
+template <auto Kernel>
+cudaError_t ensure_cluster_size() {
+  static unsigned long long done = 0;          // bit d: set on device d
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0;
+  if (bit && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess && bit) __atomic_fetch_or(&done, bit, __ATOMIC_RELEASE);
+  return e;
+}
+
 template <typename Tc, int NR, int DH>
 cudaError_t run(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk, const CUtensorMap* tv,
-                cudaStream_t st) {
-  auto kern = decode_tc_kernel<Tc, NR, DH>;
-  const size_t smem = smem_bytes<NR, DH, std::is_same<Tc, fp8>::value>();
-  cudaError_t e = ensure_smem_limit<decode_tc_kernel<Tc, NR, DH>>(smem);
+                int cluster, cudaStream_t st) {
+  constexpr bool kF8 = std::is_same<Tc, fp8>::value;
+  const size_t smem = smem_bytes<NR, DH, kF8>();
+  if constexpr (!kF8) {
+    if (cluster > 1) {
+      auto kern = decode_tc_kernel<Tc, NR, DH, true>;
+      cudaError_t e = ensure_smem_limit<decode_tc_kernel<Tc, NR, DH, true>>(smem);
+      if (e == cudaSuccess) e = ensure_cluster_size<decode_tc_kernel<Tc, NR, DH, true>>();
+      if (e == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(p.n_items);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, kern, a, p, *tk, *tv);
+        if (e == cudaSuccess) return e;
+      }
+      (void)cudaGetLastError();                // a cluster that cannot be placed: the L2 merge instead
+    }
+  }
+  auto kern = decode_tc_kernel<Tc, NR, DH, false>;
+  cudaError_t e = ensure_smem_limit<decode_tc_kernel<Tc, NR, DH, false>>(smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(p.n_items), dim3(kThreads), smem, st, a, p, *tk, *tv);
 }
@@ -610,13 +757,16 @@ bool decode_tc_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* til
 }
 
 cudaError_t launch_decode_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
-                             const CUtensorMap* tv, cudaStream_t st) {
+                             const CUtensorMap* tv, int cluster, cudaStream_t st) {
   if (p.rows_per_tile != 16) return cudaErrorInvalidValue;
+  if (cluster > kMaxCluster) cluster = 0;
   if (a.cache_dtype == KVC_FP8_E4M3)
-    return a.D == 128 ? run<fp8, 16, 128>(a, p, tk, tv, st) : cudaErrorInvalidValue;
+    return a.D == 128 ? run<fp8, 16, 128>(a, p, tk, tv, 0, st) : cudaErrorInvalidValue;
   if (a.D == 128)
-    return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16, 128>(a, p, tk, tv, st) : run<__half, 16, 128>(a, p, tk, tv, st);
-  return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16, 64>(a, p, tk, tv, st) : run<__half, 16, 64>(a, p, tk, tv, st);
+    return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16, 128>(a, p, tk, tv, cluster, st)
+                                     : run<__half, 16, 128>(a, p, tk, tv, cluster, st);
+  return a.cache_dtype == KVC_BF16 ? run<__nv_bfloat16, 16, 64>(a, p, tk, tv, cluster, st)
+                                   : run<__half, 16, 64>(a, p, tk, tv, cluster, st);
 }
 
 }  // namespace kvc

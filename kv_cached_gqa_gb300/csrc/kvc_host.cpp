@@ -477,13 +477,20 @@ int plan_attention(kvc_handle h, int T, int H_q, SplitPlan* plan, AttnPlan* out,
   plan->split_keys = max_chunk;
   out->workspace_floats = plan->n_items > n_units * h->H ? splitk_workspace_floats(*plan, h->D) : 0;
   out->counters = static_cast<size_t>(n_units) * h->H;
+  // one wave of the decode kernel with the same number of splits for every unit (16-bit caches): the
+  // splits of each (unit, K/V head) merge as one thread-block cluster, through distributed shared
+  // memory, which takes the merge's L2 round trips off the end of the launch
+  out->cluster = 0;
+  if (kind == AttnKernel::DecodeTC && h->dtype != KVC_FP8_E4M3 && items <= slots && nsplit[0] > 1 &&
+      nsplit[0] <= 16 && std::all_of(nsplit.begin(), nsplit.begin() + n_units, [&](int x) { return x == nsplit[0]; }))
+    out->cluster = nsplit[0];
   return KVC_OK;
 }
 
 cudaError_t launch_attention(const AttnPlan& ap, const AttnArgs& a, const SplitPlan& p, kvc_handle h,
                              cudaStream_t st) {
   switch (ap.kernel) {
-    case AttnKernel::DecodeTC: return launch_decode_tc(a, p, &h->tmap_k_tc, &h->tmap_v_tc, st);
+    case AttnKernel::DecodeTC: return launch_decode_tc(a, p, &h->tmap_k_tc, &h->tmap_v_tc, ap.cluster, st);
     case AttnKernel::ChunkTC: return launch_chunk_tc(a, p, &h->tmap_k_tc, &h->tmap_v_tc, st);
     case AttnKernel::PrefillTC: return launch_prefill_tc(a, p, &h->tmap_k_tc, &h->tmap_v_tc, st);
     case AttnKernel::SplitK: return launch_splitk(a, p, &h->tmap_k_split, &h->tmap_v_split, st);

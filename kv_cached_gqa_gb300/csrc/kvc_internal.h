@@ -152,8 +152,11 @@ cudaError_t launch_splitk(const AttnArgs& a, const SplitPlan& p, const CUtensorM
 // Tensor-core decode/verify kernel (16-bit caches, d_h = 128, up to 32 query rows per K/V head per
 // row tile). Returns false when the shape has no tensor-core kernel.
 bool decode_tc_shape(kvc_dtype dt, int D, int rows, int* rows_per_tile, int* tile_keys, int* max_tiles);
+// cluster > 1: every unit has `cluster` splits and each (unit, K/V head)'s splits run as one thread-block
+// cluster whose partials merge through distributed shared memory (16-bit caches; falls back to the L2
+// merge when the cluster cannot be placed).
 cudaError_t launch_decode_tc(const AttnArgs& a, const SplitPlan& p, const CUtensorMap* tk,
-                             const CUtensorMap* tv, cudaStream_t st);
+                             const CUtensorMap* tv, int cluster, cudaStream_t st);
 
 // Tensor-core chunk kernels: 16-bit caches, d_h = 128, 128 query rows per CTA. launch_chunk_tc:
 // at most 128 rows per K/V head (one CTA per (sequence, K/V head), one per SM); launch_prefill_tc:
@@ -206,6 +209,7 @@ enum class AttnKernel { SplitK, DecodeTC, ChunkTC, PrefillTC };
 struct AttnPlan {
   AttnKernel kernel;
   int rows_per_tile;
+  int cluster = 0;           // decode kernel: splits per unit when they merge as one cluster (else 0)
   size_t workspace_floats;   // split partials (0 when no unit splits)
   size_t counters;           // merge counters the kernel may use (units x H_kv)
 };

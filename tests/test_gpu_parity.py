@@ -181,6 +181,32 @@ def test_split_size_does_not_change_results(split):
     m.close()
 
 
+@pytest.mark.parametrize("dtype,d,Hq,Hkv,T,split", [
+    ("f16", 64, 9, 3, 1, 0),          # the planner's own splits (9 per unit on this shape)
+    ("f16", 64, 9, 3, 1, 1024),       # 3 splits per unit
+    ("bf16", 128, 32, 8, 1, 0),
+    ("bf16", 128, 32, 8, 1, 256),     # 9 splits: a cluster past the portable size of 8
+    ("bf16", 128, 16, 4, 4, 128),     # 17 splits: more than a cluster holds, the L2 merge instead
+    ("f16", 128, 8, 2, 2, 384),
+])
+def test_uniform_splits_merge_in_a_cluster(dtype, d, Hq, Hkv, T, split):
+    """Every sequence as long as the others and one wave of CTAs: the splits of each (sequence, K/V
+    head) run as one thread-block cluster and merge through distributed shared memory."""
+    B, s0 = 4, 2048
+    m = Mirror(L=2, B=B, H_kv=Hkv, d_h=d, max_len=s0 + 2 * T + 4, dtype=dtype, seed=17 + split)
+    for layer in range(2):
+        m.append(layer, s0)
+    m.commit()
+    for step in range(2):
+        for layer in range(2):
+            m.append(layer, T)
+            got, want = m.attend(layer, Hq, T, split_keys=split)
+            check_outputs(got, want, dtype, f"cluster merge split={split} step {step} layer {layer}")
+        m.commit()
+    m.check_state()
+    m.close()
+
+
 def test_query_in_cache_dtype_equals_rounded_f32_query():
     m = Mirror(L=1, B=2, H_kv=2, d_h=64, max_len=300, dtype="f16", seed=4)
     m.append(0, 250)
