@@ -109,10 +109,16 @@ def _torch():
     return torch
 
 
+_DTYPE_CODES = None
+
+
 def dtype_code(t) -> int:
-    torch = _torch()
-    return {torch.float32: KVC_F32, torch.float16: KVC_F16, torch.bfloat16: KVC_BF16,
-            torch.float8_e4m3fn: KVC_FP8_E4M3}[t]
+    global _DTYPE_CODES
+    if _DTYPE_CODES is None:                  # built once: this runs on every call of the hot path
+        torch = _torch()
+        _DTYPE_CODES = {torch.float32: KVC_F32, torch.float16: KVC_F16, torch.bfloat16: KVC_BF16,
+                        torch.float8_e4m3fn: KVC_FP8_E4M3}
+    return _DTYPE_CODES[t]
 
 
 def torch_dtype(code: int):
