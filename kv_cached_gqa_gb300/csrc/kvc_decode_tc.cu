@@ -310,15 +310,67 @@ decode_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ Spl
         mbar_drain(smem_u32(&ctl->full[i % kStages]), (i / kStages) & 1);
   } else {
     // ---- warps 1-5, while warp 0 already streams: Q^T and zeroed P^T ----------------------------
-    if (a.rope.table != nullptr) {                           // rotated queries: element by element
-      for (int i = tid - 32; i < NR * kDh; i += kThreads - 32) {
-        const int r = i / kDh, d = i % kDh;
-        float x = 0.f;
-        if (r < nrows) {
+    if (a.rope.table != nullptr) {
+      // rotated queries, four elements a step: each thread issues every query, partner and cos/sin load
+      // of its share before it rotates any (one round of memory latency, not one per element); the
+      // arithmetic is load_query_rot's, element for element
+      using Q = typename QueryOf<Tc>::T;
+      constexpr int kStagers = kThreads - 32, kQuads = NR * kDh / 4, kIter = (kQuads + kStagers - 1) / kStagers;
+      constexpr int kHalf = kDh / 2;
+      const bool style0 = a.rope.style == 0;                 // pairs (e, e + d_h/2); else (2i, 2i + 1)
+      uint4 xr[kIter], yr[kIter];
+      float4 c0[kIter], c1[kIter];
+  #pragma unroll
+      for (int k = 0; k < kIter; ++k) {
+        const int i = (tid - 32) + k * kStagers, r = (4 * i) / kDh, d = (4 * i) % kDh;
+        xr[k] = yr[k] = make_uint4(0u, 0u, 0u, 0u);
+        c0[k] = c1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < kQuads && r < nrows) {
           const int gr = row0 + r, t = gr / a.G, g = gr % a.G;
-          x = load_query_rot<Tc>(a, ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh, d, s_b + t);
+          const long long row = ((static_cast<long long>(b) * a.H_q + kvh * a.G + g) * a.T + t) * kDh;
+          // (cos, sin) pairs of position s_b + t, two per float4
+          const float4* cs = reinterpret_cast<const float4*>(a.rope.table + static_cast<long long>(s_b + t) * kHalf);
+          xr[k] = load_query4_raw<Tc>(a.q, a.q_dtype, row + d);
+          if (style0) {
+            yr[k] = load_query4_raw<Tc>(a.q, a.q_dtype, row + (d < kHalf ? d + kHalf : d - kHalf));
+            const int p0 = d < kHalf ? d : d - kHalf;        // pairs p0 .. p0 + 3
+            c0[k] = cs[p0 / 2];
+            c1[k] = cs[p0 / 2 + 1];
+          } else {
+            c0[k] = cs[d / 4];                              // pairs d/2 and d/2 + 1
+          }
         }
-        *reinterpret_cast<Tm*>(sm + Lo::kQOff + sw128(NR, r, d)) = from_f32<Tm>(x);
+      }
+  #pragma unroll
+      for (int k = 0; k < kIter; ++k) {
+        const int i = (tid - 32) + k * kStagers, r = (4 * i) / kDh, d = (4 * i) % kDh;
+        if (i < kQuads) {
+          float x[4], y[4];
+          if (a.q_dtype == KVC_F32) {
+            x[0] = __uint_as_float(xr[k].x); x[1] = __uint_as_float(xr[k].y);
+            x[2] = __uint_as_float(xr[k].z); x[3] = __uint_as_float(xr[k].w);
+            y[0] = __uint_as_float(yr[k].x); y[1] = __uint_as_float(yr[k].y);
+            y[2] = __uint_as_float(yr[k].z); y[3] = __uint_as_float(yr[k].w);
+          } else {                                            // four 16-bit elements in the low 8 bytes
+            const Q* xq = reinterpret_cast<const Q*>(&xr[k]);
+            const Q* yq = reinterpret_cast<const Q*>(&yr[k]);
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) { x[c] = to_f32<Q>(xq[c]); y[c] = to_f32<Q>(yq[c]); }
+          }
+          if (!style0) { y[0] = x[1]; y[1] = x[0]; y[2] = x[3]; y[3] = x[2]; }
+          const float2 cs[4] = {make_float2(c0[k].x, c0[k].y), make_float2(style0 ? c0[k].z : c0[k].x, style0 ? c0[k].w : c0[k].y),
+                                make_float2(style0 ? c1[k].x : c0[k].z, style0 ? c1[k].y : c0[k].w),
+                                make_float2(style0 ? c1[k].z : c0[k].z, style0 ? c1[k].w : c0[k].w)};
+          Tm out[4];
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const bool second = style0 ? d >= kHalf : (c & 1) != 0;
+            float v = rope_rotate(x[c], y[c], cs[c], second);
+            if constexpr (sizeof(Q) == 2) v = to_f32<Q>(from_f32<Q>(v));
+            out[c] = from_f32<Tm>(v);
+          }
+          *reinterpret_cast<uint2*>(sm + Lo::kQOff + sw128(NR, r, d)) = *reinterpret_cast<const uint2*>(out);
+        }
       }
     } else {                                                  // four elements per load, all loads first
       constexpr int kStagers = kThreads - 32, kQuads = NR * kDh / 4, kIter = (kQuads + kStagers - 1) / kStagers;
