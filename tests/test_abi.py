@@ -36,7 +36,7 @@ def test_headers_declare_the_entry_points():
               "kvc_truncate_ragged", "kvc_seq_len", "kvc_positions", "kvc_layer_ptrs", "kvc_status",
               "kvc_create_paged", "kvc_block_table", "kvc_set_rope", "kvc_append_rope", "gqa_cached_attn_rope", "kvc_set_kv_scales",
               "kvc_create_latent", "mla_cached_attn", "kvc_set_lengths", "gqa_cached_attn_noalloc",
-              "kvc_workspace_bytes"):
+              "kvc_workspace_bytes", "gqa_cached_attn_append"):
         assert n in names
 
 
@@ -114,6 +114,9 @@ def test_host_validation_without_gpu(lib):
     lib.kvc_create(None, 1, 1, 1, 64, 16, 0, None)                            # leaves another message
     assert lib.gqa_cached_attn_noalloc(None, None, 0, 0, -1, 1, 1, None, None) == -1
     assert _err(lib) == "null handle"                                        # the call's own message
+    lib.kvc_create(None, 1, 1, 1, 64, 16, 0, None)
+    assert lib.gqa_cached_attn_append(None, 0, None, None, 0, None, 0, 1, 1, None, 0, None) == -1
+    assert _err(lib) == "null handle"
 
 
 def test_binding_fails_loudly_when_library_missing(monkeypatch, tmp_path):
